@@ -1,0 +1,389 @@
+"""Benchmark of the routed-MoE expert stage (and the dense quantised GEMMs).
+
+One step = one moe_expert_stage_w4_iq4 call over the 5268-token prompt
+workload (T=5268, D=2048, F=768, E=128, top-8): routing, grouping, W4 gate/up +
+SwiGLU + q8_1, IQ4_NL down and the weighted combine.  The dense W4A16
+(M=2048, K=5120, N=17408) and FP8 block-128 (M=2048, K=5120, N=5120) products
+are timed in the same run and reported under "quant_gemm".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the stage on its own
+prompt (independent problems, no collective); value = tokens of all ranks /
+max time over ranks ("scaling": "weak").
+
+--impl reference times the CPU oracle (the plain fp64 C implementation the
+tests check against) on the host cores, on bounded token samples of the same
+workload; rank 0 alone runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synthetic import workloads as wl  # noqa: E402
+
+STAGE = "moe_t5268_d2048_f768_e128_k8"
+GEMM_W4 = "w4a16_m2048_k5120_n17408"
+GEMM_FP8 = "fp8blk128_m2048_k5120_n5120"
+METRIC = "MoE expert-stage prefill tokens/s; quant-GEMM TFLOP/s vs GB300 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(key)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if v is not None:
+                    out[key] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qmm_clocks_{os.getpid()}_{gpu_index}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[4:8]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.remove(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def setup_dist(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("QMM_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+def time_oracle_stage(g: dict, k: int, ntok: int, cores: int) -> tuple[float, int]:
+    """Seconds the CPU oracle takes for the stage on the first `ntok` tokens
+    (routing over all tokens, then the full chain for the sample)."""
+    os.environ["OMP_NUM_THREADS"] = str(cores)
+    import oracle
+    toks = np.arange(ntok, dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.moe_expert_stage(g["X"], g["logits"], g["Wgu_c"], g["Wgu_s"], g["gu_scale2"], g["Wd_idx"], g["Wd_s"],
+                            k, tokens=toks)
+    return time.perf_counter() - t0, ntok
+
+
+def cpu_baseline_sample(g: dict, k: int, target_s: float = 12.0) -> dict:
+    cores = os.cpu_count() or 1
+    dt, n = time_oracle_stage(g, k, 2, cores)                  # calibration
+    ntok = int(max(2, min(512, target_s / max(dt / n, 1e-6))))
+    dt, n = time_oracle_stage(g, k, ntok, cores)
+    return {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {g['X'].shape[0]} tokens of {STAGE} (routing over all tokens), "
+                      f"{dt:.1f} s, fp32 dequant + fp64 accumulation, OpenMP over outputs"}
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[STAGE]
+    g = wl.generate(w)
+    cores = os.cpu_count() or 1
+    dt, n = time_oracle_stage(g, w.k, 2, cores)
+    per_tok = dt / n
+    # each step a bounded sample: the whole --steps/--warmup run stays within ~3 minutes
+    ntok = int(max(2, min(256, 150.0 / max(args.steps + args.warmup, 1) / max(per_tok, 1e-6))))
+    for _ in range(args.warmup):
+        time_oracle_stage(g, w.k, ntok, cores)
+    times = []
+    for _ in range(args.steps):
+        dt, _ = time_oracle_stage(g, w.k, ntok, cores)
+        times.append(dt)
+    total = sum(times)
+    value = ntok * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": STAGE, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "k": w.k,
+                   "sample_tokens_per_step": ntok},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {ntok} tokens of {STAGE} per step (routing over all {w.T} tokens)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def stage_units(w):
+    P = w.T * w.k
+    flops = {"gate_up": 2.0 * P * w.D * 2 * w.F, "down": 2.0 * P * w.F * w.D}
+    bytes_ = {
+        "route": w.T * w.E * 4 + 4 * P * 4,                          # logits in; ids, w, src, row out
+        "gather": 2 * P * w.D * 2,                                   # X rows read, X_perm written
+        "combine": P * w.D * 4 + w.T * w.D * 4 + P * 8,              # Yslot read, Y written, row/w
+    }
+    return flops, bytes_
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import block_quantized_weight_route_gb300 as q
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    q.build_library()
+    peaks, peak_src = load_peaks()
+
+    w = wl.WORKLOADS[STAGE]
+    g = wl.generate(w)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+    X = d(g["X"].view(np.int16))
+    logits = d(g["logits"])
+    Wgu_c, Wgu_s, s2 = d(g["Wgu_c"]), d(g["Wgu_s"]), d(g["gu_scale2"])
+    Wd_idx, Wd_s = d(g["Wd_idx"]), d(g["Wd_s"].view(np.int16))
+    ws = torch.empty(q.moe_expert_stage_workspace_size(w.T, w.D, w.F, w.E, w.k), dtype=torch.uint8, device=device)
+    Y = torch.empty((w.T, w.D), dtype=torch.float32, device=device)
+
+    def step():
+        q.moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, s2, Wd_idx, Wd_s, w.k, ws=ws, Y=Y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    q.qmm_check_status()
+
+    # ---- timed region: K steps, inputs (340 MB of weights per step) larger than L2
+    q.qmm_profile_enable(True)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    phase_ms = []
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        phase_ms.append(q.qmm_profile_read())
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    q.qmm_profile_enable(False)
+    q.qmm_check_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = max_over_ranks(world, sum(step_ms) / 1e3, device)
+    value = w.T * world * args.steps / total_s
+
+    phases = {k: statistics.mean(p[k] for p in phase_ms) for k in q.PROFILE_PHASES}
+    flops, bytes_ = stage_units(w)
+    pk_t = peaks["bf16_tflops_sustained"]
+    phase_roof = {}
+    for name, ms in phases.items():
+        if name in flops:
+            ach = flops[name] / (ms * 1e-3) / 1e12
+            phase_roof[name] = {"ms": ms, "bound": "tensor", "achieved": ach, "peak": pk_t, "unit": "TFLOP/s",
+                                "frac": ach / pk_t}
+        else:
+            ach = bytes_[name] / (ms * 1e-3) / 1e9
+            phase_roof[name] = {"ms": ms, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"]}
+    dom = max(phases, key=phases.get)
+    roof = dict(phase_roof[dom])
+    roof.pop("ms")
+    roof["kernel"] = dom
+    roof["traffic"] = None
+    roof["peak_source"] = f"{peak_src} ({'sustained' if roof['bound'] == 'tensor' else 'copy'})"
+
+    # ---- end to end through the public API: pinned host inputs in, Y back out, every step
+    Xh = torch.from_numpy(g["X"].view(np.int16)).pin_memory()
+    Lh = torch.from_numpy(g["logits"]).pin_memory()
+    Yh = torch.empty((w.T, w.D), dtype=torch.float32).pin_memory()
+    Xd, Ld = torch.empty_like(X), torch.empty_like(logits)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        Xd.copy_(Xh, non_blocking=True)
+        Ld.copy_(Lh, non_blocking=True)
+        q.moe_expert_stage_w4_iq4(Xd, Ld, Wgu_c, Wgu_s, s2, Wd_idx, Wd_s, w.k, ws=ws, Y=Y)
+        Yh.copy_(Y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(world, e0.elapsed_time(e1) / 1e3, device)
+    e2e = {"value": w.T * world * args.steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": int(Xh.numel() * 2 + Lh.numel() * 4), "d2h_bytes_per_step": int(Yh.numel() * 4)}
+
+    del ws, Y, X, Xd, Ld, Wgu_c, Wgu_s, Wd_idx, Wd_s
+    torch.cuda.empty_cache()
+
+    quant = {} if args.no_gemm else bench_dense(q, torch, device, args, peaks, peak_src)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f16 operands, f32 accumulate", "data": "synthetic",
+        "config": {"workload": STAGE, "T": w.T, "D": w.D, "F": w.F, "E": w.E, "k": w.k,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (340 MB of expert weights read per step)"},
+        "roofline": roof, "phases": phase_roof, "quant_gemm": quant, "e2e": e2e, "clocks": clk,
+        "gpu_launches": 8 * args.steps, "wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(g, w.k)
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def bench_dense(q, torch, device, args, peaks, peak_src):
+    """Dense W4A16 and FP8 block-128 GEMMs: per-launch CUDA events, L2 flushed before each launch."""
+    out = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    for name in (GEMM_W4, GEMM_FP8):
+        w = wl.WORKLOADS[name]
+        g = wl.generate(w)
+        d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+        X = d(g["X"].view(np.int16))
+        if w.kind == "w4a16":
+            Wc, Ws = d(g["Wc"]), d(g["Ws"])
+            Y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+            call = lambda: q.qmm_w4a16(X, Wc, Ws, float(g["scale2"]), out_dtype=torch.bfloat16, Y=Y)  # noqa: E731
+        else:
+            W, S = d(g["W"]), d(g["S"])
+            Y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+            call = lambda: q.qmm_fp8_blk128(X, W, S, Y=Y)  # noqa: E731
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        q.qmm_check_status()
+        ms = statistics.mean(times)
+        tfl = w.flops() / (ms * 1e-3) / 1e12
+        out[name] = {"ms": ms, "tflops": tfl, "peak": peaks["bf16_tflops"], "frac": tfl / peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} (burst bf16)", "l2": "flushed before each launch"}
+        del X, Y
+        torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--no-gemm", action="store_true", help="skip the dense GEMM measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = setup_dist(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

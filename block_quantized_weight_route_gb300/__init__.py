@@ -1,0 +1,222 @@
+"""Python binding of the block-quantised prefill GEMM / routed-MoE expert-stage
+library (C ABI in include/qmm.h, CUDA kernels for sm_103a in csrc/).
+
+Argument marshalling only: every step runs in the library's kernels, on the
+current torch CUDA stream.  There is no CPU path; if the shared library is
+missing or the device is not a GB300 the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB, build_library  # noqa: F401
+
+QMM_WS_FIELDS = 15
+WS_FIELD_NAMES = ("ids", "w", "counts", "offsets", "src", "row", "chunk_counts", "tiles", "tile_count",
+                  "X_perm", "Hq", "Hd", "Hs", "Yslot", "total")
+
+_STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE",
+           3: "QMM_ERR_UNSUPPORTED_DEVICE", 4: "QMM_ERR_WORKSPACE", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT"}
+
+
+class QmmError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"CUDA library not built ({LIB}); run block_quantized_weight_route_gb300.build")
+        L = ctypes.CDLL(LIB)
+        P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.qmm_last_error.restype = ctypes.c_char_p
+        L.qmm_last_error.argtypes = []
+        L.qmm_check_status.restype = i32
+        L.qmm_check_status.argtypes = [P]
+        L.qmm_w4a16.restype = i32
+        L.qmm_w4a16.argtypes = [P, i32, i32, i32, P, P, ctypes.c_float, P, i32, P]
+        L.qmm_fp8_blk128.restype = i32
+        L.qmm_fp8_blk128.argtypes = [P, i32, i32, i32, P, P, P, P]
+        L.moe_route_workspace_size.restype = sz
+        L.moe_route_workspace_size.argtypes = [i32, i32, i32]
+        L.moe_route_permute.restype = i32
+        L.moe_route_permute.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+        L.moe_expert_stage_workspace_size.restype = sz
+        L.moe_expert_stage_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.moe_expert_stage_workspace_layout.restype = i32
+        L.moe_expert_stage_workspace_layout.argtypes = [i32, i32, i32, i32, i32, P]
+        L.qmm_profile_enable.restype = i32
+        L.qmm_profile_enable.argtypes = [i32]
+        L.qmm_profile_read.restype = i32
+        L.qmm_profile_read.argtypes = [P]
+        L.moe_expert_stage_w4_iq4.restype = i32
+        L.moe_expert_stage_w4_iq4.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, st: int) -> None:
+    if st != 0:
+        raise QmmError(fn, st, lib().qmm_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtypes, shape=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+_F16 = (torch.float16, torch.int16, torch.uint16)
+_U8 = (torch.uint8, torch.int8)
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def qmm_check_status(device=None) -> None:
+    """Synchronise the current stream and raise if a kernel wait timed out."""
+    _check("qmm_check_status", lib().qmm_check_status(_stream(device)))
+
+
+def qmm_w4a16(X, Wc, Ws, scale2: float, out_dtype=torch.float32, Y=None):
+    """Y[M,N] = scale2 * X . dequant(Wc, Ws)^T  (e2m1 codes, E4M3 per-16 scales)."""
+    M, K = X.shape
+    N = Wc.shape[0]
+    _need(X, "X", _BF16, (M, K))
+    _need(Wc, "Wc", _U8, (N, K // 2))
+    _need(Ws, "Ws", _U8, (N, K // 16))
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out_dtype must be float32 or bfloat16")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=out_dtype, device=X.device)
+    _need(Y, "Y", (out_dtype,), (M, N))
+    st = lib().qmm_w4a16(_ptr(X), M, K, N, _ptr(Wc), _ptr(Ws), float(scale2), _ptr(Y),
+                         0 if out_dtype == torch.float32 else 1, _stream(X.device))
+    _check("qmm_w4a16", st)
+    return Y
+
+
+def qmm_fp8_blk128(X, W, S, Y=None):
+    """Y[M,N] (bf16) = sum over 128x128 blocks of S[n/128, kb] * X . e4m3(W)^T."""
+    M, K = X.shape
+    N = W.shape[0]
+    _need(X, "X", _BF16, (M, K))
+    _need(W, "W", _U8 + (torch.float8_e4m3fn,), (N, K))
+    _need(S, "S", (torch.float32,), (N // 128, K // 128))
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _need(Y, "Y", _BF16, (M, N))
+    st = lib().qmm_fp8_blk128(_ptr(X), M, K, N, _ptr(W), _ptr(S), _ptr(Y), _stream(X.device))
+    _check("qmm_fp8_blk128", st)
+    return Y
+
+
+def moe_route_workspace_size(T: int, E: int, k: int) -> int:
+    return int(lib().moe_route_workspace_size(T, E, k))
+
+
+def moe_route_permute(logits, k: int, ws=None) -> dict:
+    """Top-k routing and stable per-expert grouping; returns ids, w, counts,
+    offsets, src, row as CUDA tensors."""
+    T, E = logits.shape
+    _need(logits, "logits", (torch.float32,), (T, E))
+    dev = logits.device
+    out = dict(ids=torch.empty((T, k), dtype=torch.int32, device=dev),
+               w=torch.empty((T, k), dtype=torch.float32, device=dev),
+               counts=torch.empty(E, dtype=torch.int32, device=dev),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+               src=torch.empty(T * k, dtype=torch.int32, device=dev),
+               row=torch.empty((T, k), dtype=torch.int32, device=dev))
+    need = moe_route_workspace_size(T, E, k)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(ws, "ws", _U8)
+    st = lib().moe_route_permute(_ptr(logits), T, E, k, _ptr(out["ids"]), _ptr(out["w"]), _ptr(out["counts"]),
+                                 _ptr(out["offsets"]), _ptr(out["src"]), _ptr(out["row"]), _ptr(ws), ws.numel(),
+                                 _stream(dev))
+    _check("moe_route_permute", st)
+    return out
+
+
+def moe_expert_stage_workspace_size(T: int, D: int, F: int, E: int, k: int) -> int:
+    return int(lib().moe_expert_stage_workspace_size(T, D, F, E, k))
+
+
+def moe_expert_stage_workspace_layout(T: int, D: int, F: int, E: int, k: int) -> dict:
+    arr = (ctypes.c_size_t * QMM_WS_FIELDS)()
+    _check("moe_expert_stage_workspace_layout",
+           lib().moe_expert_stage_workspace_layout(T, D, F, E, k, ctypes.cast(arr, ctypes.c_void_p)))
+    return dict(zip(WS_FIELD_NAMES, [int(v) for v in arr]))
+
+
+def moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, k: int, ws=None, Y=None):
+    """The routed expert stage: route, W4 gate/up + SwiGLU + q8_1, IQ4_NL down,
+    weighted combine.  Returns Y [T, D] fp32 (and leaves intermediates in ws)."""
+    T, D = X.shape
+    E = logits.shape[1]
+    F = Wgu_c.shape[1] // 2
+    _need(X, "X", _BF16, (T, D))
+    _need(logits, "logits", (torch.float32,), (T, E))
+    _need(Wgu_c, "Wgu_c", _U8, (E, 2 * F, D // 2))
+    _need(Wgu_s, "Wgu_s", _U8, (E, 2 * F, D // 16))
+    _need(gu_scale2, "gu_scale2", (torch.float32,), (E,))
+    _need(Wd_idx, "Wd_idx", _U8, (E, D, F // 2))
+    _need(Wd_s, "Wd_s", _F16, (E, D, F // 32))
+    dev = X.device
+    if ws is None:
+        ws = torch.empty(max(moe_expert_stage_workspace_size(T, D, F, E, k), 256), dtype=torch.uint8, device=dev)
+    _need(ws, "ws", _U8)
+    if Y is None:
+        Y = torch.empty((T, D), dtype=torch.float32, device=dev)
+    _need(Y, "Y", (torch.float32,), (T, D))
+    st = lib().moe_expert_stage_w4_iq4(_ptr(X), _ptr(logits), T, D, F, E, k, _ptr(Wgu_c), _ptr(Wgu_s),
+                                       _ptr(gu_scale2), _ptr(Wd_idx), _ptr(Wd_s), _ptr(Y), _ptr(ws), ws.numel(),
+                                       _stream(dev))
+    _check("moe_expert_stage_w4_iq4", st)
+    return Y
+
+
+PROFILE_PHASES = ("route", "gather", "gate_up", "down", "combine")
+
+
+def qmm_profile_enable(on: bool) -> None:
+    _check("qmm_profile_enable", lib().qmm_profile_enable(1 if on else 0))
+
+
+def qmm_profile_read() -> dict:
+    """Phase times (ms) of the last profiled expert-stage call (waits for it)."""
+    arr = (ctypes.c_float * len(PROFILE_PHASES))()
+    _check("qmm_profile_read", lib().qmm_profile_read(ctypes.cast(arr, ctypes.c_void_p)))
+    return dict(zip(PROFILE_PHASES, [float(v) for v in arr]))
+
+
+def workspace_view(ws: torch.Tensor, layout: dict, name: str, dtype, shape) -> torch.Tensor:
+    """A typed view of one region of an expert-stage workspace."""
+    n = 1
+    for s in shape:
+        n *= s
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    off = layout[name]
+    return ws[off:off + nbytes].view(dtype).view(*shape)

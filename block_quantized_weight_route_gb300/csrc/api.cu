@@ -1,0 +1,445 @@
+// C ABI (include/qmm.h): argument checks, tensor-map encoding, workspace
+// layout and the launch sequence of each entry point.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/qmm.h"
+#include "qmm_internal.h"
+
+namespace qmm {
+
+__device__ uint32_t g_qmm_err;   // device error word (first kernel-side failure code)
+
+namespace {
+
+thread_local std::string t_last_error;
+
+qmm_status fail(qmm_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+qmm_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(QMM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    bool ready = false;
+    bool profile = false;
+    bool events_ready = false;
+    bool profiled_once = false;
+    cudaEvent_t ev[QMM_PROFILE_PHASES + 1];
+    qmm_status status = QMM_OK;
+    std::string why;
+    int sms = 0;
+    uint32_t* err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device one-time set-up: architecture check, SM count, error word address.
+qmm_status device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(QMM_ERR_UNSUPPORTED_DEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (major != 10 || minor != 3) {
+            d.status = QMM_ERR_UNSUPPORTED_DEVICE;
+            char buf[128];
+            snprintf(buf, sizeof buf, "compute capability %d.%d; this library is built for sm_103a only", major,
+                     minor);
+            d.why = buf;
+        } else {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_qmm_err);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+            d.err = static_cast<uint32_t*>(p);
+            e = cudaMemset(d.err, 0, sizeof(uint32_t));
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+            if (!g_encode) {
+                cudaDriverEntryPointQueryResult q;
+                void* fn = nullptr;
+                e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+                if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                    return fail(QMM_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+            }
+        }
+        d.ready = true;
+    }
+    if (d.status != QMM_OK) return fail(d.status, "%s", d.why.c_str());
+    *out = &d;
+    return QMM_OK;
+}
+
+// 2-D tiled tensor map over a row-major [outer][inner] matrix.
+qmm_status make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(QMM_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for a %llux%llu map", (int)r,
+                    (unsigned long long)outer, (unsigned long long)inner);
+    return QMM_OK;
+}
+
+// Record phase boundary i of a profiled expert-stage call.
+cudaError_t mark(DeviceState* d, int i, cudaStream_t s) {
+    if (!d->profile) return cudaSuccess;
+    if (!d->events_ready) {
+        for (int j = 0; j <= QMM_PROFILE_PHASES; ++j) {
+            cudaError_t e = cudaEventCreate(&d->ev[j]);
+            if (e != cudaSuccess) return e;
+        }
+        d->events_ready = true;
+    }
+    d->profiled_once = true;
+    return cudaEventRecord(d->ev[i], s);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int route_chunks(int T) { return (T + kRouteChunk - 1) / kRouteChunk; }
+int max_tile_entries(int T, int E, int k) { return (int)(((long)T * k + 127) / 128) + E; }
+
+// Workspace regions of the expert stage, in the order of the QMM_WS_FIELDS list.
+void stage_layout(int T, int D, int F, int E, int k, size_t* off) {
+    const size_t P = (size_t)T * k;
+    size_t sz[QMM_WS_FIELDS - 1] = {
+        P * 4,                                      // ids
+        P * 4,                                      // w
+        (size_t)E * 4,                              // counts
+        (size_t)(E + 1) * 4,                        // offsets
+        P * 4,                                      // src
+        P * 4,                                      // row
+        (size_t)route_chunks(T) * E * 4,            // chunk counts
+        (size_t)max_tile_entries(T, E, k) * 16,     // tile list
+        16,                                         // tile count
+        P * D * 2,                                  // X_perm
+        P * F,                                      // Hq
+        P * (F / 32) * 2,                           // Hd
+        P * (F / 32) * 2,                           // Hs
+        P * D * 4,                                  // Yslot
+    };
+    size_t o = 0;
+    for (int i = 0; i < QMM_WS_FIELDS - 1; ++i) {
+        off[i] = o;
+        o = align_up(o + sz[i], 256);
+    }
+    off[QMM_WS_FIELDS - 1] = o;
+}
+
+}  // namespace
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+const char* qmm_last_error(void) { return t_last_error.c_str(); }
+
+qmm_status qmm_check_status(cudaStream_t stream) {
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t code = 0;
+    e = cudaMemcpy(&code, d->err, sizeof code, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (code != 0) {
+        cudaMemset(d->err, 0, sizeof code);
+        return fail(QMM_ERR_TIMEOUT, "a kernel wait timed out (device code %u)", code);
+    }
+    return QMM_OK;
+}
+
+qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, const uint8_t* Ws, float scale2,
+                     void* Y, qmm_dtype ydt, cudaStream_t stream) {
+    if (!X || !Wc || !Ws || !Y) return fail(QMM_ERR_INVALID_ARG, "qmm_w4a16: null pointer");
+    if (!aligned16(X) || !aligned16(Wc) || !aligned16(Ws) || !aligned16(Y))
+        return fail(QMM_ERR_INVALID_ARG, "qmm_w4a16: buffers must be 16-byte aligned");
+    if (ydt != QMM_F32 && ydt != QMM_BF16) return fail(QMM_ERR_INVALID_ARG, "qmm_w4a16: bad output type");
+    if (M < 1 || K < 64 || N < 32 || K % 64 || N % 32)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE, "qmm_w4a16: need M >= 1, K %% 64 == 0, N %% 32 == 0 (M=%d K=%d N=%d)",
+                    M, K, N);
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    CUtensorMap ta, tb;
+    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
+        return st;
+    if ((st = make_tmap(&tb, Wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, 32, 256,
+                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+        return st;
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.m_tiles = (M + 127) / 128;
+    p.n_tiles = (N + 255) / 256;
+    p.n_step = 256;
+    p.w_scale = Ws;
+    p.scale2_dense = scale2;
+    p.Y = Y;
+    p.ydt = (ydt == QMM_BF16) ? 1 : 0;
+    p.ldy = N;
+    p.err = d->err;
+    const int tiles = p.m_tiles * p.n_tiles;
+    cudaError_t e = launch_w4a16_dense(ta, tb, p, tiles < d->sms ? tiles : d->sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_w4a16 launch");
+    return QMM_OK;
+}
+
+qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t* W, const float* S, uint16_t* Y,
+                          cudaStream_t stream) {
+    if (!X || !W || !S || !Y) return fail(QMM_ERR_INVALID_ARG, "qmm_fp8_blk128: null pointer");
+    if (!aligned16(X) || !aligned16(W) || !aligned16(S) || !aligned16(Y))
+        return fail(QMM_ERR_INVALID_ARG, "qmm_fp8_blk128: buffers must be 16-byte aligned");
+    if (M < 1 || K < 128 || N < 128 || K % 128 || N % 128)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE,
+                    "qmm_fp8_blk128: need M >= 1, K %% 128 == 0, N %% 128 == 0 (M=%d K=%d N=%d)", M, K, N);
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    CUtensorMap ta, tb;
+    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
+        return st;
+    if ((st = make_tmap(&tb, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) != QMM_OK)
+        return st;
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.m_tiles = (M + 127) / 128;
+    p.n_tiles = N / 128;
+    p.n_step = 128;
+    p.blk_scale = S;
+    p.Y = Y;
+    p.ydt = 1;
+    p.ldy = N;
+    p.err = d->err;
+    const int tiles = p.m_tiles * p.n_tiles;
+    cudaError_t e = launch_fp8_blk128(ta, tb, p, tiles < d->sms ? tiles : d->sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_fp8_blk128 launch");
+    return QMM_OK;
+}
+
+size_t moe_route_workspace_size(int T, int E, int k) {
+    (void)k;
+    if (T < 0 || E < 1) return 0;
+    return align_up((size_t)route_chunks(T) * E * 4, 256);
+}
+
+static qmm_status check_route_shape(const char* who, int T, int E, int k) {
+    if (T < 0 || k < 1 || k > 16 || E < k || E > 512)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE, "%s: need T >= 0, 1 <= k <= 16, k <= E <= 512 (T=%d E=%d k=%d)", who,
+                    T, E, k);
+    return QMM_OK;
+}
+
+qmm_status moe_route_permute(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
+                             int32_t* offsets, int32_t* src, int32_t* row, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+    qmm_status st = check_route_shape("moe_route_permute", T, E, k);
+    if (st != QMM_OK) return st;
+    if (!counts || !offsets || (T > 0 && (!logits || !ids || !w || !src || !row || !ws)))
+        return fail(QMM_ERR_INVALID_ARG, "moe_route_permute: null pointer");
+    if (ws_bytes < moe_route_workspace_size(T, E, k))
+        return fail(QMM_ERR_WORKSPACE, "moe_route_permute: workspace %zu < %zu bytes", ws_bytes,
+                    moe_route_workspace_size(T, E, k));
+    DeviceState* d = nullptr;
+    if ((st = device_state(&d)) != QMM_OK) return st;
+    cudaError_t e;
+    if (T == 0) {
+        if ((e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream)) != cudaSuccess ||
+            (e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), stream)) != cudaSuccess)
+            return cuda_fail(e, "moe_route_permute");
+        return QMM_OK;
+    }
+    RouteBufs b{ids, w, counts, offsets, src, row, static_cast<int32_t*>(ws), nullptr, nullptr, 0};
+    e = launch_route(logits, T, E, k, b, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_route_permute launch");
+    return QMM_OK;
+}
+
+static qmm_status check_stage_shape(int T, int D, int F, int E, int k) {
+    qmm_status st = check_route_shape("moe_expert_stage_w4_iq4", T, E, k);
+    if (st != QMM_OK) return st;
+    if (D < 128 || D % 128 || F < 128 || F % 128 || F > 1024)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE,
+                    "moe_expert_stage_w4_iq4: need D %% 128 == 0, F %% 128 == 0, F <= 1024 (D=%d F=%d)", D, F);
+    return QMM_OK;
+}
+
+size_t moe_expert_stage_workspace_size(int T, int D, int F, int E, int k) {
+    if (T < 0 || D < 0 || F < 32 || E < 1 || k < 1) return 0;
+    size_t off[QMM_WS_FIELDS];
+    stage_layout(T, D, F, E, k, off);
+    return off[QMM_WS_FIELDS - 1];
+}
+
+qmm_status moe_expert_stage_workspace_layout(int T, int D, int F, int E, int k, size_t* offsets_out) {
+    if (!offsets_out) return fail(QMM_ERR_INVALID_ARG, "moe_expert_stage_workspace_layout: null pointer");
+    qmm_status st = check_stage_shape(T, D, F, E, k);
+    if (st != QMM_OK) return st;
+    stage_layout(T, D, F, E, k, offsets_out);
+    return QMM_OK;
+}
+
+qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T, int D, int F, int E, int k,
+                                   const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2,
+                                   const uint8_t* Wd_idx, const uint16_t* Wd_s, float* Y, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream) {
+    qmm_status st = check_stage_shape(T, D, F, E, k);
+    if (st != QMM_OK) return st;
+    if (!Wgu_c || !Wgu_s || !gu_scale2 || !Wd_idx || !Wd_s || (T > 0 && (!X || !logits || !Y || !ws)))
+        return fail(QMM_ERR_INVALID_ARG, "moe_expert_stage_w4_iq4: null pointer");
+    if (!aligned16(X) || !aligned16(logits) || !aligned16(Wgu_c) || !aligned16(Wgu_s) || !aligned16(Wd_idx) ||
+        !aligned16(Wd_s) || !aligned16(Y) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return fail(QMM_ERR_INVALID_ARG,
+                    "moe_expert_stage_w4_iq4: buffers must be 16-byte aligned (workspace 256-byte aligned)");
+    const size_t need = moe_expert_stage_workspace_size(T, D, F, E, k);
+    if (ws_bytes < need) return fail(QMM_ERR_WORKSPACE, "moe_expert_stage_w4_iq4: workspace %zu < %zu bytes", ws_bytes, need);
+    DeviceState* d = nullptr;
+    if ((st = device_state(&d)) != QMM_OK) return st;
+    if (T == 0) return QMM_OK;
+
+    size_t off[QMM_WS_FIELDS];
+    stage_layout(T, D, F, E, k, off);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    auto at = [&](int i) { return static_cast<void*>(base + off[i]); };
+    const int P = T * k;
+    const int max_entries = max_tile_entries(T, E, k);
+
+    cudaError_t e;
+    if ((e = mark(d, 0, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
+    RouteBufs rb{static_cast<int32_t*>(at(0)), static_cast<float*>(at(1)), static_cast<int32_t*>(at(2)),
+                 static_cast<int32_t*>(at(3)), static_cast<int32_t*>(at(4)), static_cast<int32_t*>(at(5)),
+                 static_cast<int32_t*>(at(6)), static_cast<int4*>(at(7)), static_cast<int32_t*>(at(8)),
+                 max_entries};
+    e = launch_route(logits, T, E, k, rb, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "expert stage: routing");
+    if ((e = mark(d, 1, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
+    uint16_t* Xp = static_cast<uint16_t*>(at(9));
+    e = launch_gather_rows(X, rb.src, P, D, Xp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "expert stage: gather");
+    if ((e = mark(d, 2, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
+
+    int8_t* Hq = static_cast<int8_t*>(at(10));
+    __half* Hd = static_cast<__half*>(at(11));
+    __half* Hs = static_cast<__half*>(at(12));
+    float* Yslot = static_cast<float*>(at(13));
+
+    // gate/up + SwiGLU + q8_1
+    CUtensorMap ta, tb;
+    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
+        return st;
+    if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, 128,
+                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+        return st;
+    GemmParams g{};
+    g.K = D;
+    g.F = F;
+    g.n_tiles = F / 128;
+    g.n_step = 128;
+    g.tiles = rb.tiles;
+    g.num_entries = rb.num_entries;
+    g.max_entries = max_entries;
+    g.w_scale = Wgu_s;
+    g.scale2 = gu_scale2;
+    g.Hq = Hq;
+    g.Hd = Hd;
+    g.Hs = Hs;
+    g.err = d->err;
+    e = launch_w4_gate_up_swiglu(ta, tb, g, d->sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "expert stage: gate/up launch");
+    if ((e = mark(d, 3, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
+
+    // down (IQ4_NL x q8_1)
+    CUtensorMap ta2, tb2;
+    if ((st = make_tmap(&ta2, Hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, F, P, F, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+        QMM_OK)
+        return st;
+    if ((st = make_tmap(&tb2, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
+                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+        return st;
+    GemmParams q{};
+    q.N = D;
+    q.K = F;
+    q.n_tiles = D / 128;
+    q.n_step = 128;
+    q.tiles = rb.tiles;
+    q.num_entries = rb.num_entries;
+    q.max_entries = max_entries;
+    q.dH = Hd;
+    q.dW = reinterpret_cast<const __half*>(Wd_s);
+    q.Y = Yslot;
+    q.ydt = 0;
+    q.ldy = D;
+    q.err = d->err;
+    e = launch_iq4_down(ta2, tb2, q, d->sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "expert stage: down launch");
+    if ((e = mark(d, 4, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
+
+    e = launch_combine(Yslot, rb.row, rb.w, T, k, D, Y, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "expert stage: combine");
+    if ((e = mark(d, 5, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
+    return QMM_OK;
+}
+
+qmm_status qmm_profile_enable(int on) {
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    d->profile = on != 0;
+    return QMM_OK;
+}
+
+qmm_status qmm_profile_read(float* ms_out) {
+    if (!ms_out) return fail(QMM_ERR_INVALID_ARG, "qmm_profile_read: null pointer");
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    if (!d->profiled_once) return fail(QMM_ERR_INVALID_ARG, "qmm_profile_read: no profiled call yet");
+    cudaError_t e = cudaEventSynchronize(d->ev[QMM_PROFILE_PHASES]);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_profile_read");
+    for (int i = 0; i < QMM_PROFILE_PHASES; ++i) {
+        e = cudaEventElapsedTime(&ms_out[i], d->ev[i], d->ev[i + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "qmm_profile_read");
+    }
+    return QMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,664 @@
+// Warp-specialised block-quantised GEMM for sm_103a (one CTA per SM, persistent).
+//
+//   warp 0        : TMA producer (activations tile + raw quantised weight tile)
+//   warp 1        : TMEM owner and MMA issuer (one thread issues tcgen05.mma)
+//   warps 2..3    : idle
+//   epilogue warps: read fp32 accumulators from TMEM, scale / fold / quantise, store
+//   converter warps: turn raw weight codes (and int8 activations) into the exact
+//                    16-bit operand tiles the tensor core reads, in shared memory
+//
+// Tile: 128 rows (tokens) x BN columns (weight rows), K step 64.  The MMA is
+// tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16), fp32 accumulation in
+// TMEM.  Operands are K-major in the canonical 128-byte-swizzled layout.
+//
+// The quantised formats it reads (page titles / sections):
+//  - W4: e2m1 codes with one E4M3 scale per 16 K and an fp32 scale2 applied once
+//    in the epilogue ("perf: strix-hip BF16 GEMMs via hipBLASLt", commit "f16a
+//    twins").  e2m1 x E4M3 is exact in bf16, so the dequantised operand is exact.
+//  - FP8 with one fp32 scale per 128x128 block: each 128-K block is accumulated
+//    unscaled and folded once with its scale (same page, FP8 block-scaling twin).
+//  - IQ4_NL x q8_1: one exact integer dot per 32-K block (both operands are small
+//    integers, exact in f16, block sums < 2^24 exact in fp32), folded with the
+//    two fp16 block scales ("Run Edge0-145B Q3_K on AMD HIP (Linux, gfx1100)",
+//    commit 4cb5224: gate/up, SwiGLU, q8_1 H, IQ4_NL down).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "qmm_internal.h"
+
+namespace qmm {
+
+enum class AMode { BF16_TMA, I8_CONV };
+enum class BMode { W4, FP8, IQ4 };
+enum class Epi { STORE, SWIGLU_Q81, FOLD_FP8, FOLD_IQ4 };
+
+template <AMode A_, BMode B_, Epi E_, int BN_, int CONV_WARPS_, int EPI_WARPS_, int TSTAGES_, int CSTAGES_,
+          bool GROUPED_>
+struct GemmCfg {
+    static constexpr AMode A = A_;
+    static constexpr BMode B = B_;
+    static constexpr Epi EPI = E_;
+    static constexpr bool GROUPED = GROUPED_;
+    static constexpr int BM = 128, BN = BN_, BK = 64, UMMA_K = 16;
+    static constexpr int CONV_WARPS = CONV_WARPS_, EPI_WARPS = EPI_WARPS_;
+    static constexpr int EPI_BASE = 4, CONV_BASE = 4 + EPI_WARPS_;
+    static constexpr int THREADS = 32 * (4 + EPI_WARPS_ + CONV_WARPS_);
+    static constexpr int TSTAGES = TSTAGES_, CSTAGES = CSTAGES_;
+    static constexpr bool A_DIRECT = (A_ == AMode::BF16_TMA);
+    // raw (TMA) stage
+    static constexpr int A_RAW_BYTES = BM * BK * (A_DIRECT ? 2 : 1);
+    static constexpr int B_ROW_BYTES = (B_ == BMode::FP8) ? 64 : 32;   // bytes of codes per weight row per k-block
+    static constexpr int B_RAW_BYTES = BN * B_ROW_BYTES;
+    static constexpr int TSTAGE_BYTES = A_RAW_BYTES + B_RAW_BYTES;
+    // converted stage
+    static constexpr int A_CONV_BYTES = A_DIRECT ? 0 : BM * BK * 2;
+    static constexpr int B_CONV_BYTES = BN * BK * 2;
+    static constexpr int CSTAGE_BYTES = A_CONV_BYTES + B_CONV_BYTES;
+    // accumulation groups
+    static constexpr bool FOLD = (E_ == Epi::FOLD_FP8 || E_ == Epi::FOLD_IQ4);
+    static constexpr int GROUP_K = (E_ == Epi::FOLD_FP8) ? 128 : (E_ == Epi::FOLD_IQ4 ? 32 : 0);   // 0: whole K
+    static constexpr int NBUF = 512 / BN;
+    static constexpr bool BF16_OPERANDS = (B_ != BMode::IQ4);
+    static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, BF16_OPERANDS);
+    // epilogue staging for the IQ4 fold, per epilogue warp: dW [KG][64] and dH [KG][32] fp16
+    static constexpr int KG_MAX = 32;   // K / 32 groups at most (K <= 1024)
+    static constexpr int EPI_SMEM = (E_ == Epi::FOLD_IQ4) ? EPI_WARPS_ * KG_MAX * 96 * 2 : 0;
+    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * NBUF + 1;
+    static constexpr int SMEM_BYTES =
+        1024 /*align slack*/ + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES + EPI_SMEM + BAR_COUNT * 8 + 64;
+    static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(BN % 32 == 0 && BN <= 256, "BN");
+    static_assert(!FOLD || EPI_WARPS == 8, "fold epilogue splits columns over two warpgroups");
+    static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
+};
+
+struct TileInfo {
+    int expert, row0, rows, n0;
+};
+
+template <class C>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
+    TileInfo ti;
+    if constexpr (C::GROUPED) {
+        const int entry = t / p.n_tiles, nt = t - entry * p.n_tiles;
+        const int4 g = p.tiles[entry];
+        ti.expert = g.x;
+        ti.row0 = g.y;
+        ti.rows = g.z;
+        ti.n0 = nt * p.n_step;
+    } else {
+        const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+        ti.expert = 0;
+        ti.row0 = mt * C::BM;
+        ti.rows = min(C::BM, p.M - ti.row0);
+        ti.n0 = nt * p.n_step;
+    }
+    return ti;
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr) : "memory");
+    return v;
+}
+
+// bf16 value 2^112 in both halves: f16 bits >> 3 read as bf16 are the f16 value
+// times 2^-112 (exponent bias 15 vs 127), so this factor restores it exactly.
+constexpr uint32_t kBf16x2_2p112 = 0x77807780u;
+// Select mask for the f16 -> bf16 shift: bits 15/31 keep the sign from the f16
+// word, bits 12/28 take the (always zero) low mantissa bit of the f16 word to
+// clear the sign bits that the shift moved there.
+constexpr uint32_t kF16ToBf16Mask = 0x90009000u;
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a), y = *reinterpret_cast<__nv_bfloat162*>(&b);
+    __nv_bfloat162 r = __hmul2(x, y);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+    __half2 x = *reinterpret_cast<__half2*>(&a), y = *reinterpret_cast<__half2*>(&b);
+    __half2 r = __hsub2(x, y);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// E4M3 scale byte -> bf16x2 of (scale * 2^112), exact.
+__device__ __forceinline__ uint32_t w4_scale_bf16x2(uint32_t byte) {
+    uint32_t h[2];
+    cvt_e4m3x4_f16x2(byte & 0xFFu, h);
+    const float s = __half2float(__ushort_as_half((unsigned short)(h[0] & 0xFFFFu))) * 5.192296858534828e33f;   // 2^112
+    const __nv_bfloat16 b = __float2bfloat16_rn(s);
+    const uint32_t u = __bfloat16_as_ushort(b);
+    return u | (u << 16);
+}
+
+// IQ4_NL codebook + 128 as bytes (index 0..15), four per word.
+constexpr uint32_t kIq4T0 = 0x3F2D1801u;   // -127 -104  -83  -65
+constexpr uint32_t kIq4T1 = 0x766A5D4Fu;   //  -49  -35  -22  -10
+constexpr uint32_t kIq4T2 = 0xA6998D81u;   //    1   13   25   38
+constexpr uint32_t kIq4T3 = 0xF1D9C5B5u;   //   53   69   89  113
+// f16 bits 0x64XX are 1024 + XX; subtracting 1152 leaves XX - 128.
+constexpr uint32_t kF16x2_1152 = 0x64806480u;
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* tstage = smem;
+    uint8_t* cstage = tstage + C::TSTAGES * C::TSTAGE_BYTES;
+    uint8_t* epi_smem = cstage + C::CSTAGES * C::CSTAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + C::EPI_SMEM);
+    uint64_t* full_t = bars;
+    uint64_t* empty_t = full_t + C::TSTAGES;
+    uint64_t* full_c = empty_t + C::TSTAGES;
+    uint64_t* empty_c = full_c + C::CSTAGES;
+    uint64_t* acc_full = empty_c + C::CSTAGES;
+    uint64_t* acc_empty = acc_full + C::NBUF;
+    uint64_t* drain_bar = acc_empty + C::NBUF;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::TSTAGES; ++i) {
+            mbar_init(&full_t[i], 1);
+            mbar_init(&empty_t[i], C::A_DIRECT ? 1 : C::CONV_WARPS);
+        }
+        for (int i = 0; i < C::CSTAGES; ++i) {
+            mbar_init(&full_c[i], C::CONV_WARPS);
+            mbar_init(&empty_c[i], 1);
+        }
+        for (int i = 0; i < C::NBUF; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], C::EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int kblocks = p.K / C::BK;
+    int num_tiles;
+    if constexpr (C::GROUPED) {
+        const int entries = min(*p.num_entries, p.max_entries);
+        num_tiles = entries * p.n_tiles;
+    } else {
+        num_tiles = p.m_tiles * p.n_tiles;
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile<C>(p, t);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                    mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                    tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
+                    uint8_t* bdst = st + C::A_RAW_BYTES;
+                    const int kx = kb * C::B_ROW_BYTES;
+                    if constexpr (C::EPI == Epi::SWIGLU_Q81) {
+                        // gate rows e*2F + n0 .. +BN/2, up rows e*2F + F + n0 .. +BN/2
+                        const int base = ti.expert * 2 * p.F + ti.n0;
+                        tma_load_2d(bdst, &tmB, &full_t[s], kx, base);
+                        tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, &tmB, &full_t[s], kx, base + p.F);
+                    } else {
+                        tma_load_2d(bdst, &tmB, &full_t[s], kx, ti.expert * p.N + ti.n0);
+                    }
+                    ++issued;
+                    if (++s == C::TSTAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // Teardown: every copy issued must have landed before the CTA exits.
+            const long pending = issued < C::TSTAGES ? issued : C::TSTAGES;
+            for (long i = 0; i < pending; ++i) {
+                // stage of the i-th most recent issue and the parity of its fill
+                long idx = issued - 1 - i;
+                const int ss = (int)(idx % C::TSTAGES);
+                const uint32_t pp = (uint32_t)((idx / C::TSTAGES) & 1);
+                if (!mbar_try_wait(&full_t[ss], pp)) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(&full_t[ss], pp)) {
+                        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                            atomicCAS(p.err, 0u, DEV_TIMEOUT_DRAIN);
+                            break;
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int ts = 0, cs = 0, buf = 0;
+            uint32_t tph = 0, cph = 0, bph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < kblocks && ok; ++kb) {
+                    if (C::A_DIRECT && !mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t* cst = cstage + cs * C::CSTAGE_BYTES;
+                    const uint32_t a_base =
+                        C::A_DIRECT ? smem_u32(tstage + ts * C::TSTAGE_BYTES) : smem_u32(cst);
+                    const uint32_t b_base = smem_u32(cst + C::A_CONV_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+                        const int kg = kb * C::BK + kk * C::UMMA_K;
+                        const int gk = C::GROUP_K ? C::GROUP_K : p.K;
+                        const bool first = (kg % gk) == 0;
+                        const bool last = ((kg + C::UMMA_K) % gk) == 0;
+                        if (first) {
+                            if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        tc_mma_f16(tmem_base + (uint32_t)(buf * C::BN), smem_desc_sw128(a_base + kk * 32),
+                                   smem_desc_sw128(b_base + kk * 32), C::IDESC, first ? 0u : 1u);
+                        if (last) {
+                            tc_commit(&acc_full[buf]);
+                            if (++buf == C::NBUF) {
+                                buf = 0;
+                                bph ^= 1u;
+                            }
+                        }
+                    }
+                    if (!ok) break;
+                    tc_commit(&empty_c[cs]);
+                    if (C::A_DIRECT) tc_commit(&empty_t[ts]);
+                    if (++ts == C::TSTAGES) {
+                        ts = 0;
+                        tph ^= 1u;
+                    }
+                    if (++cs == C::CSTAGES) {
+                        cs = 0;
+                        cph ^= 1u;
+                    }
+                }
+            }
+            // Teardown: wait until every MMA issued has completed before TMEM is freed.
+            tc_commit(drain_bar);
+            if (!mbar_try_wait(drain_bar, 0)) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(drain_bar, 0)) {
+                    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                        atomicCAS(p.err, 0u, DEV_TIMEOUT_DRAIN);
+                        break;
+                    }
+                }
+            }
+        }
+    } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                         // TMEM lane quarter of this warp
+        const int half = (warp - C::EPI_BASE) >> 2;     // column half (fold epilogue only)
+        const int row = q * 32 + lane;                  // accumulator row = TMEM lane
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+        int buf = 0;
+        uint32_t bph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const TileInfo ti = decode_tile<C>(p, t);
+            const bool valid = row < ti.rows;
+            const long grow = (long)ti.row0 + row;
+            if constexpr (!C::FOLD) {
+                if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN);
+                if constexpr (C::EPI == Epi::STORE) {
+                    const float s2 = p.scale2_dense;
+#pragma unroll 1
+                    for (int c = 0; c < C::BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(acc + c * 32, r);
+                        tmem_ld_wait();
+                        const int col = ti.n0 + c * 32;
+                        if (valid && col < p.N) {
+                            if (p.ydt == 0) {
+                                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + grow * p.ldy + col);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    dst[j] = make_float4(__uint_as_float(r[4 * j]) * s2, __uint_as_float(r[4 * j + 1]) * s2,
+                                                         __uint_as_float(r[4 * j + 2]) * s2,
+                                                         __uint_as_float(r[4 * j + 3]) * s2);
+                            } else {
+                                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    uint32_t w[4];
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]) * s2,
+                                                                                 __uint_as_float(r[8 * j + 2 * i + 1]) * s2);
+                                        w[i] = *reinterpret_cast<uint32_t*>(&b);
+                                    }
+                                    dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+                                }
+                            }
+                        }
+                    }
+                } else {   // SWIGLU_Q81: columns [0, BN/2) gate, [BN/2, BN) up
+                    const float s2 = p.scale2[ti.expert];
+#pragma unroll 1
+                    for (int c = 0; c < C::BN / 64; ++c) {
+                        uint32_t g[32], u[32];
+                        tmem_ld32(acc + c * 32, g);
+                        tmem_ld32(acc + C::BN / 2 + c * 32, u);
+                        tmem_ld_wait();
+                        if (valid) {
+                            float h[32];
+                            float amax = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const float gv = __uint_as_float(g[j]) * s2;
+                                const float uv = __uint_as_float(u[j]) * s2;
+                                h[j] = gv / (1.0f + expf(-gv)) * uv;
+                                amax = fmaxf(amax, fabsf(h[j]));
+                            }
+                            uint32_t packed[8];
+                            int sum = 0;
+                            float d = 0.f;
+                            if (amax > 0.f) {
+                                d = amax / 127.0f;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    uint32_t w = 0;
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        float v = roundf(h[4 * j + i] / d);
+                                        v = fminf(fmaxf(v, -127.f), 127.f);
+                                        const int qv = (int)v;
+                                        sum += qv;
+                                        w |= ((uint32_t)(qv & 0xFF)) << (8 * i);
+                                    }
+                                    packed[j] = w;
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) packed[j] = 0;
+                            }
+                            const int col = ti.n0 + c * 32;
+                            uint4* hq = reinterpret_cast<uint4*>(p.Hq + grow * p.F + col);
+                            hq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            hq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                            const long bidx = grow * (p.F / 32) + col / 32;
+                            p.Hd[bidx] = __float2half_rn(d);
+                            p.Hs[bidx] = __float2half_rn(d * (float)sum);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                if (++buf == C::NBUF) {
+                    buf = 0;
+                    bph ^= 1u;
+                }
+            } else {
+                // fold: one accumulator per K group, folded into registers with its scale
+                const int groups = p.K / C::GROUP_K;
+                float sum[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) sum[j] = 0.f;
+                // IQ4: this warp's own copy of the block scales it needs, staged
+                // without any cross-warp barrier: dW [KG][64 columns], dH [KG][32 rows].
+                __half* dWs = reinterpret_cast<__half*>(epi_smem) + (warp - C::EPI_BASE) * (C::KG_MAX * 96);
+                __half* dHs = dWs + C::KG_MAX * 64;
+                if constexpr (C::EPI == Epi::FOLD_IQ4) {
+                    __syncwarp();   // the previous tile's reads of this warp are done
+                    const long wcol0 = (long)ti.expert * p.N + ti.n0 + half * 64;
+                    for (int i = lane; i < 64 * groups; i += 32) {
+                        const int n = i / groups, g = i - n * groups;
+                        dWs[g * 64 + n] = p.dW[(wcol0 + n) * groups + g];
+                    }
+                    for (int i = lane; i < 32 * groups; i += 32) {
+                        const int r = i / groups, g = i - r * groups;
+                        const int trow = q * 32 + r;
+                        dHs[g * 32 + r] =
+                            (trow < ti.rows) ? p.dH[((long)ti.row0 + trow) * groups + g] : __float2half(0.f);
+                    }
+                    __syncwarp();
+                }
+                for (int g = 0; g < groups; ++g) {
+                    if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t r0[32], r1[32];
+                    const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + half * 64);
+                    tmem_ld32(acc, r0);
+                    tmem_ld32(acc + 32, r1);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                    if (++buf == C::NBUF) {
+                        buf = 0;
+                        bph ^= 1u;
+                    }
+                    if constexpr (C::EPI == Epi::FOLD_FP8) {
+                        const float s = p.blk_scale[(long)(ti.n0 / 128) * groups + g];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            sum[j] = fmaf(s, __uint_as_float(r0[j]), sum[j]);
+                            sum[32 + j] = fmaf(s, __uint_as_float(r1[j]), sum[32 + j]);
+                        }
+                    } else {
+                        const float dh = __half2float(dHs[g * 32 + lane]);
+                        const __half* dw = dWs + g * 64;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            sum[j] = fmaf(__uint_as_float(r0[j]) * __half2float(dw[j]), dh, sum[j]);
+                            sum[32 + j] = fmaf(__uint_as_float(r1[j]) * __half2float(dw[32 + j]), dh, sum[32 + j]);
+                        }
+                    }
+                }
+                if (!ok) break;
+                if (valid) {
+                    const int col = ti.n0 + half * 64;
+                    if constexpr (C::EPI == Epi::FOLD_FP8) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                __nv_bfloat162 b = __floats2bfloat162_rn(sum[8 * j + 2 * i], sum[8 * j + 2 * i + 1]);
+                                w[i] = *reinterpret_cast<uint32_t*>(&b);
+                            }
+                            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + grow * p.ldy + col);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            dst[j] = make_float4(sum[4 * j], sum[4 * j + 1], sum[4 * j + 2], sum[4 * j + 3]);
+                    }
+                }
+            }
+        }
+    } else if (warp >= C::CONV_BASE) {
+        // ------------------------------------------------------------ converters
+        const int ct = threadIdx.x - C::CONV_BASE * 32;
+        constexpr int CT = C::CONV_WARPS * 32;
+        int ts = 0, cs = 0;
+        uint32_t tph = 0, cph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const TileInfo ti = decode_tile<C>(p, t);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
+                    !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t traw = smem_u32(tstage + ts * C::TSTAGE_BYTES);
+                const uint32_t braw = traw + C::A_RAW_BYTES;
+                const uint32_t cbase = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+                const uint32_t bconv = cbase + C::A_CONV_BYTES;
+                for (int r = ct; r < C::BN; r += CT) {
+                    if constexpr (C::B == BMode::W4) {
+                        // 64 e2m1 codes (32 bytes, 32-byte-swizzled rows) + 4 scale bytes
+                        const int sw = (r >> 2) & 1;
+                        const uint4 c0 = lds128(braw + r * 32 + ((0 ^ sw) << 4));
+                        const uint4 c1 = lds128(braw + r * 32 + ((1 ^ sw) << 4));
+                        long wrow;
+                        bool in_range;
+                        if constexpr (C::EPI == Epi::SWIGLU_Q81) {
+                            const int hr = (r < C::BN / 2) ? (ti.n0 + r) : (p.F + ti.n0 + r - C::BN / 2);
+                            wrow = (long)ti.expert * 2 * p.F + hr;
+                            in_range = true;
+                        } else {
+                            wrow = (long)ti.n0 + r;
+                            in_range = wrow < p.N;
+                        }
+                        const uint32_t sbytes =
+                            in_range ? __ldg(reinterpret_cast<const uint32_t*>(p.w_scale + wrow * (p.K / 16) + kb * 4)) : 0u;
+                        uint32_t sc[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) sc[i] = w4_scale_bf16x2(sbytes >> (8 * i));
+                        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            uint32_t h[4], o[4];
+                            cvt_e2m1x8_f16x2(words[w], h);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                o[i] = bf16x2_mul(bitselect(h[i] >> 3, h[i], kF16ToBf16Mask), sc[w >> 1]);
+                            sts128(bconv + sw128_off(r, w), o[0], o[1], o[2], o[3]);
+                        }
+                    } else if constexpr (C::B == BMode::FP8) {
+                        // 64 E4M3 bytes (64-byte-swizzled rows)
+                        const int sw = (r >> 1) & 3;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v = lds128(braw + r * 64 + ((c ^ sw) << 4));
+                            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t o[8];
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                uint32_t h[2];
+                                cvt_e4m3x4_f16x2(words[w], h);
+                                o[2 * w] = bf16x2_mul(bitselect(h[0] >> 3, h[0], kF16ToBf16Mask), kBf16x2_2p112);
+                                o[2 * w + 1] = bf16x2_mul(bitselect(h[1] >> 3, h[1], kF16ToBf16Mask), kBf16x2_2p112);
+                            }
+                            sts128(bconv + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
+                            sts128(bconv + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
+                        }
+                    } else {
+                        // 64 IQ4_NL indices (32 bytes, 32-byte-swizzled rows) -> exact f16 codebook values
+                        const int sw = (r >> 2) & 1;
+                        const uint4 c0 = lds128(braw + r * 32 + ((0 ^ sw) << 4));
+                        const uint4 c1 = lds128(braw + r * 32 + ((1 ^ sw) << 4));
+                        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            const uint32_t x = words[w];
+                            const uint32_t x4 = x << 4;
+                            const uint32_t xh = x >> 16;
+                            // elements 0..3 (low 16 bits) and 4..7 (high 16 bits)
+                            const uint32_t lo_a = prmt(kIq4T0, kIq4T1, x);
+                            const uint32_t hi_a = prmt(kIq4T2, kIq4T3, x & 0x7777u);
+                            const uint32_t m_a = prmt(x4, x, 0xD9C8u);
+                            const uint32_t v_a = bitselect(lo_a, hi_a, m_a);
+                            const uint32_t lo_b = prmt(kIq4T0, kIq4T1, xh);
+                            const uint32_t hi_b = prmt(kIq4T2, kIq4T3, xh & 0x7777u);
+                            const uint32_t m_b = prmt(x4, x, 0xFBEAu);
+                            const uint32_t v_b = bitselect(lo_b, hi_b, m_b);
+                            const uint32_t o0 = f16x2_sub(prmt(v_a, 0x64646464u, 0x5140u), kF16x2_1152);
+                            const uint32_t o1 = f16x2_sub(prmt(v_a, 0x64646464u, 0x5342u), kF16x2_1152);
+                            const uint32_t o2 = f16x2_sub(prmt(v_b, 0x64646464u, 0x5140u), kF16x2_1152);
+                            const uint32_t o3 = f16x2_sub(prmt(v_b, 0x64646464u, 0x5342u), kF16x2_1152);
+                            sts128(bconv + sw128_off(r, w), o0, o1, o2, o3);
+                        }
+                    }
+                }
+                if constexpr (!C::A_DIRECT) {
+                    // int8 activations (64-byte-swizzled rows of 64 codes) -> exact f16
+                    for (int r = ct; r < C::BM; r += CT) {
+                        const int sw = (r >> 1) & 3;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v = lds128(traw + r * 64 + ((c ^ sw) << 4));
+                            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t o[8];
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const uint32_t x = words[w] ^ 0x80808080u;
+                                o[2 * w] = f16x2_sub(prmt(x, 0x64646464u, 0x5140u), kF16x2_1152);
+                                o[2 * w + 1] = f16x2_sub(prmt(x, 0x64646464u, 0x5342u), kF16x2_1152);
+                            }
+                            sts128(cbase + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
+                            sts128(cbase + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&full_c[cs]);
+                    if constexpr (!C::A_DIRECT) mbar_arrive(&empty_t[ts]);
+                }
+                if (++ts == C::TSTAGES) {
+                    ts = 0;
+                    tph ^= 1u;
+                }
+                if (++cs == C::CSTAGES) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace qmm

@@ -1,0 +1,73 @@
+// Internal declarations shared by the library's translation units (not installed).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace qmm {
+
+// Parameters of one launch of the block-quantised GEMM kernel family.
+struct GemmParams {
+    int M, N, K;            // dense: output rows, columns; all: reduction length
+    int F;                  // gate/up: rows of each half (gate, up) per expert
+    int m_tiles, n_tiles;   // dense: tile grid; grouped: n_tiles per row-tile entry
+    int n_step;             // output columns advanced per column tile
+    const int4* tiles;      // grouped: {expert, first row, rows, 0} per 128-row entry
+    const int* num_entries; // grouped: device count of valid entries
+    int max_entries;        // grouped: capacity of `tiles`
+    const uint8_t* w_scale; // W4: E4M3 scale bytes, one per 16 K per weight row
+    const float* scale2;    // gate/up: fp32 scale2 per expert
+    float scale2_dense;     // dense W4: fp32 scale2
+    const float* blk_scale; // FP8: [N/128][K/128] block scales
+    const __half* dH;       // down: q8_1 block scales of H, [rows][K/32]
+    const __half* dW;       // down: IQ4_NL block scales, [E][N][K/32]
+    void* Y;                // output (fp32 or bf16)
+    int ydt;                // 0: fp32, 1: bf16
+    long ldy;               // output row pitch in elements
+    int8_t* Hq;             // gate/up: q8_1 codes of H [rows][F]
+    __half* Hd;             // gate/up: q8_1 d per 32-block [rows][F/32]
+    __half* Hs;             // gate/up: q8_1 s per 32-block [rows][F/32]
+    uint32_t* err;          // device error word
+};
+
+// Launchers (return a cudaError_t from the launch).  Each takes two encoded
+// tensor maps: tmA for the activation operand, tmB for the raw weight codes.
+cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                               cudaStream_t s);
+cudaError_t launch_w4_gate_up_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                                     cudaStream_t s);
+cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                              cudaStream_t s);
+cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                            cudaStream_t s);
+
+// Dynamic shared memory each GEMM launcher needs (checked against the device limit).
+int smem_w4a16_dense();
+int smem_w4_gate_up_swiglu();
+int smem_fp8_blk128();
+int smem_iq4_down();
+
+// Routing and data-movement kernels (route.cu).
+struct RouteBufs {
+    int32_t* ids;         // [T][k]
+    float* w;             // [T][k]
+    int32_t* counts;      // [E]
+    int32_t* offsets;     // [E+1]
+    int32_t* src;         // [T*k]
+    int32_t* row;         // [T][k]
+    int32_t* chunk_hist;  // [chunks][E]  (scratch)
+    int4* tiles;          // [max_entries] (optional)
+    int32_t* num_entries; // [1]            (optional)
+    int max_entries;
+};
+constexpr int kRouteChunk = 256;   // tokens per grouping chunk
+cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBufs& b, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t* X, const int32_t* src, int rows, int D, uint16_t* Xp, cudaStream_t s);
+cudaError_t launch_combine(const float* Yslot, const int32_t* row, const float* w, int T, int k, int D, float* Y,
+                           cudaStream_t s);
+
+// Device error words of the translation units, read and cleared by qmm_check_status.
+uint32_t* gemm_error_word();   // device address
+}  // namespace qmm

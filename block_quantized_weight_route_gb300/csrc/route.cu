@@ -1,0 +1,296 @@
+// Routed-MoE data movement: top-k routing with renormalised weights, per-expert
+// grouping (histogram, prefix scan, stable permutation), the 128-row tile list
+// the grouped GEMMs walk, the row gather of X, and the weighted combine.
+//
+// Routing follows "AMD_HIP.md", RDNA4 speed switches (router_top10: top-k ids
+// and renormalised weights); grouping tokens per expert for grouped GEMMs over
+// a 64/128-row M tile follows "perf: strix-hip BF16 GEMMs via hipBLASLt"
+// (routed-MoE prefill twins, per-expert pointer tables and max_m_tiles).
+//
+// Grouping is deterministic: the pairs (t, j) of expert e take rows
+// offsets[e] + 0, 1, ... in ascending token order (a token picks an expert at
+// most once), computed with per-chunk counts and bit masks, never with atomic
+// slot claims.
+#include <cfloat>
+#include <climits>
+
+#include "qmm_internal.h"
+
+namespace qmm {
+
+constexpr int kMaxK = 16;
+
+// One warp per token.  Lane l holds logits l, l+32, ...; k rounds of a warp
+// arg-max (ties to the lower expert index) pick the experts in descending order.
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ ids, float* __restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+        float v[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = (e < E) ? __ldg(logits + (long)t * E + e) : -FLT_MAX;
+        }
+        uint32_t taken = 0;
+        float vals[kMaxK];
+        int sel[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) {
+                float bv = -FLT_MAX;
+                int bi = -1;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < E && !((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
+                        bv = v[i];
+                        bi = e;
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                    if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+                        bv = ov;
+                        bi = oi;
+                    }
+                }
+                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+                vals[j] = bv;
+                sel[j] = bi;
+            }
+        }
+        // w_j = exp(l_j - l_max) / sum_i exp(l_i - l_max) over the k chosen experts
+        float ex[kMaxK];
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) {
+                ex[j] = expf(vals[j] - vals[0]);
+                den += ex[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k && lane == j) {
+                ids[(long)t * k + j] = sel[j];
+                w[(long)t * k + j] = ex[j] / den;
+            }
+        }
+    }
+}
+
+// Per chunk of kRouteChunk tokens: how many of its pairs chose each expert.
+__global__ void __launch_bounds__(256) route_hist_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
+                                                         int32_t* __restrict__ chunk_hist) {
+    extern __shared__ int32_t hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const long p0 = (long)blockIdx.x * kRouteChunk * k;
+    const long p1 = min((long)T * k, p0 + (long)kRouteChunk * k);
+    for (long p = p0 + threadIdx.x; p < p1; p += blockDim.x) atomicAdd(&hist[ids[p]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[(long)blockIdx.x * E + e] = hist[e];
+}
+
+// Exclusive block-wide scan of one int per thread (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* total) {
+    __shared__ int warp_sums[32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = warp_sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        warp_sums[lane] = s;   // inclusive
+    }
+    __syncthreads();
+    const int base = wid ? warp_sums[wid - 1] : 0;
+    *total = warp_sums[31];
+    __syncthreads();
+    return base + x - v;
+}
+
+// One CTA of 1024 threads (E <= 1024): per-expert counts and the exclusive
+// per-chunk bases (in place in chunk_hist), offsets, and the 128-row tile list.
+__global__ void __launch_bounds__(1024) route_scan_kernel(int chunks, int E, int32_t* __restrict__ chunk_hist,
+                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                          int4* __restrict__ tiles, int32_t* __restrict__ num_entries,
+                                                          int max_entries) {
+    const int e = threadIdx.x;
+    int cnt = 0;
+    if (e < E) {
+        for (int c = 0; c < chunks; ++c) {
+            const int h = chunk_hist[(long)c * E + e];
+            chunk_hist[(long)c * E + e] = cnt;
+            cnt += h;
+        }
+        counts[e] = cnt;
+    }
+    int total;
+    const int off = block_exclusive_scan(e < E ? cnt : 0, &total);
+    if (e < E) offsets[e] = off;
+    if (e == 0) offsets[E] = total;
+    if (tiles) {
+        const int mt = (e < E) ? (cnt + 127) / 128 : 0;
+        int ntiles;
+        const int tbase = block_exclusive_scan(mt, &ntiles);
+        for (int i = 0; i < mt; ++i) {
+            const int idx = tbase + i;
+            if (idx < max_entries) tiles[idx] = make_int4(e, off + 128 * i, min(128, cnt - 128 * i), 0);
+        }
+        if (e == 0) *num_entries = min(ntiles, max_entries);
+    }
+}
+
+// One CTA per chunk (blockDim == kRouteChunk, one token per thread): the rank of
+// a pair among its expert's pairs inside the chunk is the number of earlier
+// tokens of the chunk whose bit is set in that expert's mask.
+__global__ void __launch_bounds__(kRouteChunk) route_permute_kernel(const int32_t* __restrict__ ids, int T, int E,
+                                                                    int k, const int32_t* __restrict__ chunk_base,
+                                                                    const int32_t* __restrict__ offsets,
+                                                                    int32_t* __restrict__ src,
+                                                                    int32_t* __restrict__ row) {
+    constexpr int WORDS = kRouteChunk / 32;
+    extern __shared__ uint32_t masks[];   // [E][WORDS]
+    for (int i = threadIdx.x; i < E * WORDS; i += blockDim.x) masks[i] = 0;
+    __syncthreads();
+    const int tl = threadIdx.x;
+    const long t = (long)blockIdx.x * kRouteChunk + tl;
+    const bool live = t < T;
+    int my[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+        if (j < k && live) {
+            my[j] = ids[t * k + j];
+            atomicOr(&masks[my[j] * WORDS + (tl >> 5)], 1u << (tl & 31));
+        }
+    }
+    __syncthreads();
+    if (live) {
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) {
+                const int e = my[j];
+                const uint32_t* m = masks + e * WORDS;
+                int rank = __popc(m[tl >> 5] & ((1u << (tl & 31)) - 1u));
+                for (int wd = 0; wd < (tl >> 5); ++wd) rank += __popc(m[wd]);
+                const int r = offsets[e] + chunk_base[(long)blockIdx.x * E + e] + rank;
+                row[t * k + j] = r;
+                src[r] = (int32_t)t;
+            }
+        }
+    }
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBufs& b, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int warps_needed = T;
+    const int grid_topk = (warps_needed + 7) / 8;
+    const int epl = (E + 31) / 32;
+    switch (epl) {
+#define QMM_TOPK_CASE(N)                                                                    \
+    case N:                                                                                 \
+        route_topk_kernel<N><<<grid_topk, 256, 0, s>>>(logits, T, E, k, b.ids, b.w);       \
+        break;
+        QMM_TOPK_CASE(1) QMM_TOPK_CASE(2) QMM_TOPK_CASE(3) QMM_TOPK_CASE(4) QMM_TOPK_CASE(5) QMM_TOPK_CASE(6)
+        QMM_TOPK_CASE(7) QMM_TOPK_CASE(8) QMM_TOPK_CASE(9) QMM_TOPK_CASE(10) QMM_TOPK_CASE(11) QMM_TOPK_CASE(12)
+        QMM_TOPK_CASE(13) QMM_TOPK_CASE(14) QMM_TOPK_CASE(15) QMM_TOPK_CASE(16)
+#undef QMM_TOPK_CASE
+        default:
+            return cudaErrorInvalidValue;
+    }
+    const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
+    route_hist_kernel<<<chunks, 256, E * sizeof(int32_t), s>>>(b.ids, T, E, k, b.chunk_hist);
+    route_scan_kernel<<<1, 1024, 0, s>>>(chunks, E, b.chunk_hist, b.counts, b.offsets, b.tiles, b.num_entries,
+                                         b.max_entries);
+    const size_t msmem = (size_t)E * (kRouteChunk / 32) * sizeof(uint32_t);
+    route_permute_kernel<<<chunks, kRouteChunk, msmem, s>>>(b.ids, T, E, k, b.chunk_hist, b.offsets, b.src, b.row);
+    return cudaGetLastError();
+}
+
+// X_perm[r, :] = X[src[r], :], one warp per row, 16-byte vectors (D % 8 == 0).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ X, const int32_t* __restrict__ src,
+                                                          int rows, int vec_per_row, uint4* __restrict__ Xp) {
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+        const uint4* in = X + (long)src[r] * vec_per_row;
+        uint4* out = Xp + (long)r * vec_per_row;
+        for (int i = lane; i < vec_per_row; i += 32) out[i] = __ldg(in + i);
+    }
+}
+
+cudaError_t launch_gather_rows(const uint16_t* X, const int32_t* src, int rows, int D, uint16_t* Xp, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    int sms = 148;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = min((rows + 7) / 8, sms * 8);
+    gather_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(X), src, rows, D / 8,
+                                           reinterpret_cast<uint4*>(Xp));
+    return cudaGetLastError();
+}
+
+// Y[t, :] = sum_j w[t, j] * Yslot[row[t, j], :], j ascending; one warp per token.
+__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ Yslot, const int32_t* __restrict__ row,
+                                                      const float* __restrict__ w, int T, int k, int vec_per_row,
+                                                      float4* __restrict__ Y) {
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+        int rr[kMaxK];
+        float ww[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) {
+                rr[j] = __ldg(row + (long)t * k + j);
+                ww[j] = __ldg(w + (long)t * k + j);
+            }
+        }
+        for (int i = lane; i < vec_per_row; i += 32) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                if (j < k) {
+                    const float4 v = __ldg(Yslot + (long)rr[j] * vec_per_row + i);
+                    acc.x = fmaf(ww[j], v.x, acc.x);
+                    acc.y = fmaf(ww[j], v.y, acc.y);
+                    acc.z = fmaf(ww[j], v.z, acc.z);
+                    acc.w = fmaf(ww[j], v.w, acc.w);
+                }
+            }
+            Y[(long)t * vec_per_row + i] = acc;
+        }
+    }
+}
+
+cudaError_t launch_combine(const float* Yslot, const int32_t* row, const float* w, int T, int k, int D, float* Y,
+                           cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    int sms = 148;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = min((T + 7) / 8, sms * 8);
+    combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(Yslot), row, w, T, k, D / 4,
+                                        reinterpret_cast<float4*>(Y));
+    return cudaGetLastError();
+}
+
+}  // namespace qmm

@@ -1,0 +1,158 @@
+/*
+ * qmm.h -- C ABI of the block-quantised prefill GEMM and routed-MoE expert-stage
+ * library for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    never allocates, frees or keeps a pointer past the call.  Buffers must be
+ *    16-byte aligned.  All matrices are row-major with K (the reduction
+ *    dimension) fastest for weights.
+ *  - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
+ *  - 4-bit codes are packed two per byte: element 2j of a row is the low nibble
+ *    of byte j, element 2j+1 the high nibble.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream).  Calls are asynchronous and never synchronise the host.
+ *  - Argument checks happen before anything is enqueued; a failed check returns
+ *    QMM_ERR_INVALID_ARG / QMM_ERR_UNSUPPORTED_SHAPE / QMM_ERR_WORKSPACE and
+ *    enqueues nothing.  Launch failures return QMM_ERR_CUDA.  qmm_last_error()
+ *    gives a message for the calling thread's last failure.
+ *  - Kernel-side waits are bounded; a wait that runs out records a code in a
+ *    device error word, and qmm_check_status() (which synchronises `stream`)
+ *    returns QMM_ERR_TIMEOUT for it.
+ *  - The library runs only on compute capability 10.3 (GB300); any other device
+ *    gives QMM_ERR_UNSUPPORTED_DEVICE.  There is no fallback path.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_INVALID_ARG = 1,
+    QMM_ERR_UNSUPPORTED_SHAPE = 2,
+    QMM_ERR_UNSUPPORTED_DEVICE = 3,
+    QMM_ERR_WORKSPACE = 4,
+    QMM_ERR_CUDA = 5,
+    QMM_ERR_TIMEOUT = 6
+} qmm_status;
+
+typedef enum { QMM_F32 = 0, QMM_BF16 = 1 } qmm_dtype;
+
+/* Message describing the calling thread's most recent failed call ("" if none). */
+const char *qmm_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device: QMM_OK, QMM_ERR_TIMEOUT (a kernel wait ran out; the code is
+ * in the message), or QMM_ERR_CUDA if the synchronisation itself failed. */
+qmm_status qmm_check_status(cudaStream_t stream);
+
+/*
+ * qmm_w4a16 -- dense prefill product with 4-bit weights.
+ *   Y[m,n] = scale2 * sum_k X[m,k] * e2m1(Wc[n,k]) * e4m3(Ws[n, k/16])
+ * Format: "perf: strix-hip BF16 GEMMs via hipBLASLt", commit "f16a twins for the
+ * dense M128 and routed-MoE kernels" (e2m1 codes, one E4M3 scale per 16 K, an
+ * fp32 per-tensor scale2 applied once in the epilogue; e2m1 x E4M3 is exact).
+ *   X   [M][K]    bf16 activations
+ *   Wc  [N][K/2]  packed e2m1 codes (bit 3 sign, bits 0-2 index {0,.5,1,1.5,2,3,4,6})
+ *   Ws  [N][K/16] OCP E4M3 scale bytes
+ *   Y   [M][N]    fp32 (ydt = QMM_F32) or bf16 rounded to nearest even (QMM_BF16)
+ * fp32 accumulation.  Shapes: M >= 1, K % 64 == 0, N % 32 == 0.
+ */
+qmm_status qmm_w4a16(const uint16_t *X, int M, int K, int N, const uint8_t *Wc, const uint8_t *Ws, float scale2,
+                     void *Y, qmm_dtype ydt, cudaStream_t stream);
+
+/*
+ * qmm_fp8_blk128 -- dense prefill product with FP8 weights and 128x128 block scales.
+ *   Y[m,n] = sum_kb S[n/128][kb] * sum_{k in block kb} X[m,k] * e4m3(W[n,k])
+ * Each 128-K block is summed unscaled and folded once with its fp32 scale:
+ * "perf: strix-hip BF16 GEMMs via hipBLASLt", FP8 block-scaling twin commit.
+ *   X [M][K] bf16;  W [N][K] OCP E4M3 bytes;  S [N/128][K/128] fp32;  Y [M][N] bf16 (RNE).
+ * fp32 accumulation.  Shapes: M >= 1, K % 128 == 0, N % 128 == 0.
+ */
+qmm_status qmm_fp8_blk128(const uint16_t *X, int M, int K, int N, const uint8_t *W, const float *S, uint16_t *Y,
+                          cudaStream_t stream);
+
+/*
+ * moe_route_permute -- top-k routing and per-expert grouping of T tokens.
+ * For each token t: ids[t][0..k) are the k largest logits (descending; a tie
+ * goes to the lower expert index) and w[t][j] = exp(l_j - l_max) / sum over the
+ * k chosen of exp(l_i - l_max), which equals softmax followed by renormalising
+ * the chosen weights ("AMD_HIP.md", RDNA4 speed switches, router_top10).
+ * Grouping: counts[e] = pairs (t,j) that chose e; offsets = exclusive prefix sum
+ * of counts (offsets[E] = T*k); the pairs of expert e take rows offsets[e],
+ * offsets[e]+1, ... in ascending token order; row[t][j] is the row of pair
+ * (t,j) and src[row] its token.  Integer outputs are deterministic.
+ *   logits [T][E] fp32; ids [T][k] int32; w [T][k] fp32; counts [E] int32;
+ *   offsets [E+1] int32; src [T*k] int32; row [T][k] int32.
+ *   ws: device scratch of at least moe_route_workspace_size(T, E, k) bytes.
+ * Shapes: T >= 0, 1 <= k <= 16, k <= E <= 512.
+ */
+size_t moe_route_workspace_size(int T, int E, int k);
+qmm_status moe_route_permute(const float *logits, int T, int E, int k, int32_t *ids, float *w, int32_t *counts,
+                             int32_t *offsets, int32_t *src, int32_t *row, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/*
+ * moe_expert_stage_w4_iq4 -- the routed expert stage of a prompt.
+ * "Run Edge0-145B Q3_K on AMD HIP (Linux, gfx1100)", commit 4cb5224: gate/up,
+ * SwiGLU, H rounded to q8_1, down over IQ4_NL, for every expert's tokens; with
+ * this library's gate/up format (W4 as in qmm_w4a16, per-expert scale2):
+ *   route + group as moe_route_permute;
+ *   for each routed row r (token t, expert e):
+ *     g[n] = scale2[e] * X[t] . Wgu[e][n],  u[n] = scale2[e] * X[t] . Wgu[e][F+n]
+ *     h = silu(g) * u;   H = q8_1(h) per 32 columns:
+ *       d = max|h|/127, q = round-half-away(h/d) in [-127,127], s = d * sum(q)
+ *     y_r[n] = sum_b d_H[b] * d_W[e][n][b] * sum_{k in b} q[k] * CB[idx[e][n][k]]
+ *       (CB = IQ4_NL codebook {-127,-104,-83,-65,-49,-35,-22,-10,1,13,25,38,53,69,89,113})
+ *   Y[t] = sum_j w[t][j] * y_{row[t][j]}     (j ascending)
+ *   X [T][D] bf16; logits [T][E] fp32;
+ *   Wgu_c [E][2F][D/2] packed e2m1 (rows 0..F-1 gate, F..2F-1 up); Wgu_s [E][2F][D/16] E4M3;
+ *   gu_scale2 [E] fp32; Wd_idx [E][D][F/2] packed IQ4_NL indices; Wd_s [E][D][F/32] fp16;
+ *   Y [T][D] fp32.
+ *   ws: device scratch of at least moe_expert_stage_workspace_size(...) bytes;
+ *   its regions (routing outputs, permuted X, H codes/scales, per-row down
+ *   outputs) are listed by moe_expert_stage_workspace_layout().
+ * Shapes: D % 128 == 0, F % 128 == 0, F <= 1024, 1 <= k <= 16, k <= E <= 512, T >= 0.
+ */
+size_t moe_expert_stage_workspace_size(int T, int D, int F, int E, int k);
+qmm_status moe_expert_stage_w4_iq4(const uint16_t *X, const float *logits, int T, int D, int F, int E, int k,
+                                   const uint8_t *Wgu_c, const uint8_t *Wgu_s, const float *gu_scale2,
+                                   const uint8_t *Wd_idx, const uint16_t *Wd_s, float *Y, void *ws, size_t ws_bytes,
+                                   cudaStream_t stream);
+
+/* Byte offsets, inside the expert-stage workspace, of its regions (for callers
+ * that inspect intermediate results).  Writes QMM_WS_FIELDS offsets in this order:
+ *   0 ids [T*k] i32     1 w [T*k] f32       2 counts [E] i32    3 offsets [E+1] i32
+ *   4 src [T*k] i32     5 row [T*k] i32     6 chunk counts      7 tile list
+ *   8 tile count        9 X_perm [T*k][D] bf16   10 Hq [T*k][F] int8
+ *  11 Hd [T*k][F/32] fp16   12 Hs [T*k][F/32] fp16   13 Yslot [T*k][D] fp32
+ *  14 total size */
+#define QMM_WS_FIELDS 15
+qmm_status moe_expert_stage_workspace_layout(int T, int D, int F, int E, int k, size_t *offsets_out);
+
+/*
+ * Phase timing of the expert stage (for benchmarks).  With profiling on, each
+ * moe_expert_stage_w4_iq4 call records CUDA events on its stream between its
+ * phases: 0 routing (top-k, counts, scan, permutation), 1 row gather of X,
+ * 2 gate/up + SwiGLU + q8_1, 3 down, 4 combine.  qmm_profile_read() waits for
+ * the last profiled call's events and writes its QMM_PROFILE_PHASES phase times
+ * in milliseconds.  Events belong to the current device and are created on the
+ * first profiled call; profiling is off by default.
+ */
+#define QMM_PROFILE_PHASES 5
+qmm_status qmm_profile_enable(int on);
+qmm_status qmm_profile_read(float *ms_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMM_H */

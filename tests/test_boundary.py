@@ -1,0 +1,94 @@
+"""The C-ABI library builds, loads and exports every entry point declared in
+include/*.h; host-side argument checks and workspace arithmetic (no GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from block_quantized_weight_route_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    path = qbuild.build_library()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(", src, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"qmm_w4a16", "qmm_fp8_blk128", "moe_route_permute", "moe_expert_stage_w4_iq4"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_library_has_no_oracle_dependency():
+    """The product library must not link or embed anything from oracle/."""
+    data = open(qbuild.build_library(), "rb").read()
+    assert b"orc_" not in data and b"liboracle" not in data
+
+
+def _status(fn, *args):
+    return fn(*args)
+
+
+def test_argument_checks_return_before_any_device_work(L):
+    P = ctypes.c_void_p
+    L.qmm_w4a16.restype = ctypes.c_int
+    L.qmm_w4a16.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_float, P, ctypes.c_int, P]
+    # null pointers
+    assert L.qmm_w4a16(None, 64, 512, 512, None, None, 1.0, None, 0, None) == 1
+    # misaligned
+    assert L.qmm_w4a16(P(16), 64, 512, 512, P(17), P(32), 1.0, P(48), 0, None) == 1
+    # shapes: K not a multiple of 64, N not a multiple of 32
+    assert L.qmm_w4a16(P(256), 64, 100, 512, P(256), P(256), 1.0, P(256), 0, None) == 2
+    assert L.qmm_w4a16(P(256), 64, 512, 500, P(256), P(256), 1.0, P(256), 0, None) == 2
+    L.qmm_fp8_blk128.restype = ctypes.c_int
+    L.qmm_fp8_blk128.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P]
+    assert L.qmm_fp8_blk128(P(256), 64, 200, 256, P(256), P(256), P(256), None) == 2
+    L.qmm_last_error.restype = ctypes.c_char_p
+    assert b"qmm_fp8_blk128" in L.qmm_last_error()
+    L.moe_route_permute.restype = ctypes.c_int
+    L.moe_route_permute.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int] + [P] * 7 + [ctypes.c_size_t, P]
+    # k > 16, E > 512
+    assert L.moe_route_permute(P(256), 10, 64, 17, *([P(256)] * 7), 1 << 20, None) == 2
+    assert L.moe_route_permute(P(256), 10, 1024, 8, *([P(256)] * 7), 1 << 20, None) == 2
+    # workspace too small
+    L.moe_route_workspace_size.restype = ctypes.c_size_t
+    need = L.moe_route_workspace_size(1000, 128, 8)
+    assert need >= 4 * 128 * 4
+    assert L.moe_route_permute(P(256), 1000, 128, 8, *([P(256)] * 7), need - 1, None) == 4
+
+
+def test_expert_stage_workspace_layout_is_consistent(L):
+    from block_quantized_weight_route_gb300 import QMM_WS_FIELDS
+    L.moe_expert_stage_workspace_size.restype = ctypes.c_size_t
+    L.moe_expert_stage_workspace_layout.restype = ctypes.c_int
+    for (T, D, F, E, k) in [(5268, 2048, 768, 128, 8), (21504, 2560, 1024, 256, 8), (1, 128, 128, 2, 1)]:
+        arr = (ctypes.c_size_t * QMM_WS_FIELDS)()
+        assert L.moe_expert_stage_workspace_layout(T, D, F, E, k, arr) == 0
+        off = list(arr)
+        assert off[0] == 0 and all(o % 256 == 0 for o in off)
+        assert all(b > a for a, b in zip(off, off[1:]))
+        assert off[-1] == L.moe_expert_stage_workspace_size(T, D, F, E, k)
+        P = T * k
+        # the large regions have at least their nominal sizes
+        assert off[10] - off[9] >= P * D * 2          # X_perm
+        assert off[11] - off[10] >= P * F             # Hq
+        assert off[14] - off[13] >= P * D * 4         # Yslot
+    arr = (ctypes.c_size_t * QMM_WS_FIELDS)()
+    assert L.moe_expert_stage_workspace_layout(10, 100, 128, 8, 2, arr) == 2     # D % 128
+    assert L.moe_expert_stage_workspace_layout(10, 128, 2048, 8, 2, arr) == 2    # F > 1024

@@ -1,0 +1,232 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on seeded
+synthetic inputs: element by element on small cases that span several tiles
+and ragged tails, sampled outputs at the full workload sizes, and edge cases.
+
+Tolerances (written here, from the problem statement): integer / index work
+bit-exact; dense GEMMs max|gpu - oracle| <= 2e-3 * max|oracle| against the
+unrounded fp64 oracle; the full expert stage <= 1e-2 * max|oracle|; q8_1 codes
+of H >= 99.9% equal and the rest off by at most 1.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+GEMM_TOL = 2e-3
+STAGE_TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def qlib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import block_quantized_weight_route_gb300 as q
+    q.build_library()
+    return q
+
+
+def dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.cuda()
+
+
+def bf16_dev(bits):
+    return dev(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def bf16_to_np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def rel_err(got, ref):
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-300))
+
+
+# ---------------------------------------------------------------- dense W4A16
+
+def test_w4a16_unit_scales_integer_inputs_are_exact(qlib):
+    """Scales 1.0, scale2 1, small-integer X: every partial sum is a multiple of
+    1/2 below 2^24, so the fp32 result must equal the oracle exactly."""
+    rng = np.random.default_rng(1)
+    M, K, N = 150, 256, 288
+    Xi = rng.integers(-20, 21, size=(M, K)).astype(np.float32)
+    X = torch.from_numpy(Xi).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    Wc = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    Ws = np.full((N, K // 16), 0x38, np.uint8)
+    Y = qlib.qmm_w4a16(bf16_dev(X), dev(Wc), dev(Ws), 1.0).cpu().numpy()
+    ref = oracle.w4a16(X, Wc, Ws, 1.0)
+    assert np.array_equal(Y.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("M,K,N", [(64, 512, 512), (1, 64, 32), (129, 192, 96), (300, 1024, 544)])
+def test_w4a16_matches_oracle(qlib, M, K, N):
+    g = wl.gen_w4a16(M, K, N, 1.0 / 64, seed=M + K + N)
+    Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"])).cpu().numpy()
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"])
+    assert rel_err(Y, ref) <= 1e-5          # fp32 accumulation of exact products
+    assert rel_err(Y, ref) <= GEMM_TOL
+
+
+def test_w4a16_tiny_workload_fp32_out(qlib):
+    w = wl.WORKLOADS["w4a16_m64_k512_n512"]
+    g = wl.generate(w)
+    Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"])).cpu().numpy()
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"])
+    assert rel_err(Y, ref) <= GEMM_TOL
+
+
+def test_w4a16_bf16_out_rounding(qlib):
+    g = wl.gen_w4a16(200, 512, 256, 1.0 / 256, seed=77)
+    Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"]), out_dtype=torch.bfloat16)
+    Yf = bf16_to_np(Y)
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"])
+    # round-to-nearest from fp32: at most half a bf16 ulp (2^-9 relative) plus accumulation error
+    assert np.all(np.abs(Yf - ref) <= np.abs(ref) * 2 ** -8 + 1e-6 * np.max(np.abs(ref)))
+    assert rel_err(Yf, ref) <= GEMM_TOL
+
+
+def test_w4a16_full_size_sampled(qlib):
+    w = wl.WORKLOADS["w4a16_m2048_k5120_n17408"]
+    g = wl.generate(w)
+    Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"]), out_dtype=torch.bfloat16)
+    rows = np.array([0, 1, 127, 128, 1023, 1500, 2046, 2047])
+    cols = np.concatenate([np.arange(0, 17408, 97), [17407, 17406, 255, 256]])
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"], rows=rows, cols=cols)
+    got = bf16_to_np(Y)[np.ix_(rows, cols)]
+    assert rel_err(got, ref) <= GEMM_TOL
+
+
+# ---------------------------------------------------------------- dense FP8 block-128
+
+@pytest.mark.parametrize("M,K,N", [(130, 384, 256), (1, 128, 128), (257, 640, 384)])
+def test_fp8_blk128_matches_oracle(qlib, M, K, N):
+    g = wl.gen_fp8_blk128(M, K, N, seed=M * 3 + N)
+    Y = qlib.qmm_fp8_blk128(bf16_dev(g["X"]), dev(g["W"]), dev(g["S"]))
+    ref = oracle.fp8_blk128(g["X"], g["W"], g["S"])
+    assert rel_err(bf16_to_np(Y), ref) <= GEMM_TOL
+
+
+def test_fp8_blk128_full_size_sampled(qlib):
+    w = wl.WORKLOADS["fp8blk128_m2048_k5120_n5120"]
+    g = wl.generate(w)
+    Y = qlib.qmm_fp8_blk128(bf16_dev(g["X"]), dev(g["W"]), dev(g["S"]))
+    rows = np.array([0, 5, 127, 128, 1000, 2047])
+    cols = np.concatenate([np.arange(0, 5120, 41), [5119]])
+    ref = oracle.fp8_blk128(g["X"], g["W"], g["S"], rows=rows, cols=cols)
+    assert rel_err(bf16_to_np(Y)[np.ix_(rows, cols)], ref) <= GEMM_TOL
+
+
+# ---------------------------------------------------------------- routing
+
+def check_route(qlib, logits, k):
+    r = oracle.route(logits, k)
+    out = qlib.moe_route_permute(dev(logits), k)
+    for key in ("ids", "counts", "offsets", "src", "row"):
+        got = out[key].cpu().numpy().reshape(r[key].shape)
+        assert np.array_equal(got, r[key]), key
+    w = out["w"].cpu().numpy()
+    assert np.max(np.abs(w - r["w"])) <= 2 ** -21
+    return r
+
+
+@pytest.mark.parametrize("name", ["moe_t5268_d2048_f768_e128_k8", "moe_t21504_d2560_f1024_e256_k8_zipf"])
+def test_route_full_size_bit_exact(qlib, name):
+    w = wl.WORKLOADS[name]
+    logits = wl.gen_moe(w.T, 128, 128, w.E, w.k, 1.0, w.zipf_s, seed=w.seed)["logits"]
+    check_route(qlib, logits, w.k)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 8), (257, 32, 4), (1000, 512, 16), (513, 3, 1), (100, 64, 2)])
+def test_route_edge_shapes(qlib, T, E, k):
+    rng = np.random.default_rng(T + E + k)
+    check_route(qlib, (2 * rng.standard_normal((T, E))).astype(np.float32), k)
+
+
+def test_route_ties_and_skew(qlib):
+    T, E, k = 700, 64, 8
+    logits = np.zeros((T, E), np.float32)          # every token ties everywhere: experts 0..7
+    r = check_route(qlib, logits, k)
+    assert np.all(r["ids"] == np.arange(8)[None, :])
+    logits = np.round(np.random.default_rng(0).standard_normal((T, E)) * 2).astype(np.float32)   # many ties
+    check_route(qlib, logits, k)
+
+
+def test_route_empty(qlib):
+    out = qlib.moe_route_permute(torch.empty((0, 16), dtype=torch.float32, device="cuda"), 4)
+    assert out["counts"].sum().item() == 0 and out["offsets"].cpu().tolist() == [0] * 17
+
+
+# ---------------------------------------------------------------- expert stage
+
+def run_stage(qlib, g, k):
+    T, D = g["X"].shape
+    E = g["logits"].shape[1]
+    F = g["Wgu_c"].shape[1] // 2
+    size = qlib.moe_expert_stage_workspace_size(T, D, F, E, k)
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
+    Y = qlib.moe_expert_stage_w4_iq4(bf16_dev(g["X"]), dev(g["logits"]), dev(g["Wgu_c"]), dev(g["Wgu_s"]),
+                                     dev(g["gu_scale2"]), dev(g["Wd_idx"]), dev(g["Wd_s"].view(np.int16)), k, ws=ws)
+    torch.cuda.synchronize()
+    qlib.qmm_check_status()
+    lay = qlib.moe_expert_stage_workspace_layout(T, D, F, E, k)
+    P = T * k
+    view = lambda name, dt, shape: qlib.workspace_view(ws, lay, name, dt, shape).cpu().numpy()  # noqa: E731
+    return dict(Y=Y.cpu().numpy(), Hq=view("Hq", torch.int8, (P, F)), Hd=view("Hd", torch.int16, (P, F // 32)),
+                Yslot=view("Yslot", torch.float32, (P, D)), row=view("row", torch.int32, (T, k)),
+                src=view("src", torch.int32, (P,)), offsets=view("offsets", torch.int32, (E + 1,)))
+
+
+def check_stage(qlib, g, k, tokens=None):
+    gpu = run_stage(qlib, g, k)
+    st = oracle.moe_expert_stage(g["X"], g["logits"], g["Wgu_c"], g["Wgu_s"], g["gu_scale2"], g["Wd_idx"],
+                                 g["Wd_s"], k, tokens=tokens)
+    r = st["route"]
+    assert np.array_equal(gpu["row"], r["row"]) and np.array_equal(gpu["src"], r["src"])
+    assert np.array_equal(gpu["offsets"], r["offsets"])
+    rows = st["pair_rows"]
+    # q8_1 codes of H: >= 99.9% equal, the rest off by one
+    dq = gpu["Hq"][rows].astype(int) - st["Hq"].astype(int)
+    assert np.max(np.abs(dq)) <= 1
+    assert np.mean(dq == 0) >= 0.999
+    # the down product, recomputed by the oracle from the GPU's own H, is tight
+    ys = oracle.moe_down_iq4(gpu["Hq"][rows], gpu["Hd"][rows].view(np.uint16), r["offsets"], rows,
+                             g["Wd_idx"], g["Wd_s"])
+    assert rel_err(gpu["Yslot"][rows], ys) <= 1e-5
+    # the whole stage
+    toks = st["tokens"]
+    assert rel_err(gpu["Y"][toks], st["Y"]) <= STAGE_TOL
+    return gpu, st
+
+
+def test_expert_stage_small_full(qlib):
+    g = wl.gen_moe(300, 256, 256, 8, 2, 1.0 / 128, 0.0, seed=12)
+    check_stage(qlib, g, 2)
+
+
+def test_expert_stage_ragged_groups(qlib):
+    # skewed popularity: one expert takes most tokens (several 128-row tiles), others a handful
+    g = wl.gen_moe(333, 128, 128, 16, 4, 1.0 / 128, 2.0, seed=13)
+    check_stage(qlib, g, 4)
+
+
+def test_expert_stage_k_equals_e(qlib):
+    g = wl.gen_moe(65, 128, 256, 4, 4, 1.0 / 128, 0.0, seed=14)
+    check_stage(qlib, g, 4)
+
+
+def test_expert_stage_t5268_sampled(qlib):
+    w = wl.WORKLOADS["moe_t5268_d2048_f768_e128_k8"]
+    g = wl.generate(w)
+    check_stage(qlib, g, w.k, tokens=np.array([0, 1, 77, 2600, 5266, 5267]))
+
+
+def test_expert_stage_t21504_zipf_sampled(qlib):
+    w = wl.WORKLOADS["moe_t21504_d2560_f1024_e256_k8_zipf"]
+    g = wl.generate(w)
+    check_stage(qlib, g, w.k, tokens=np.array([0, 9999, 21503]))
