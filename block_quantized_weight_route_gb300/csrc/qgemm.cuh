@@ -115,10 +115,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
 // bf16 value 2^112 in both halves: f16 bits >> 3 read as bf16 are the f16 value
 // times 2^-112 (exponent bias 15 vs 127), so this factor restores it exactly.
 constexpr uint32_t kBf16x2_2p112 = 0x77807780u;
-// Select mask for the f16 -> bf16 shift: bits 15/31 keep the sign from the f16
-// word, bits 12/28 take the (always zero) low mantissa bit of the f16 word to
-// clear the sign bits that the shift moved there.
-constexpr uint32_t kF16ToBf16Mask = 0x90009000u;
+// f16x2 -> bf16x2 bit patterns whose values are the f16 values times 2^-112,
+// valid when the low 3 mantissa bits of both halves are zero (true for every
+// e2m1 and E4M3 value).  The shift by 3 lines the 5-bit f16 exponent up with
+// the low bits of the bf16 exponent and leaves each sign bit 3 places too low
+// (bits 12 / 28, with zeros above); adding 7 times that bit moves it up to bit
+// 15 / 31 by carry.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_2m112(uint32_t h) {
+    const uint32_t a = h >> 3;
+    return a + (a & 0x10001000u) * 7u;
+}
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a), y = *reinterpret_cast<__nv_bfloat162*>(&b);
@@ -567,7 +573,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             cvt_e2m1x8_f16x2(words[w], h);
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
-                                o[i] = bf16x2_mul(bitselect(h[i] >> 3, h[i], kF16ToBf16Mask), sc[w >> 1]);
+                                o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[i]), sc[w >> 1]);
                             sts128(bconv + sw128_off(r, w), o[0], o[1], o[2], o[3]);
                         }
                     } else if constexpr (C::B == BMode::FP8) {
@@ -582,8 +588,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             for (int w = 0; w < 4; ++w) {
                                 uint32_t h[2];
                                 cvt_e4m3x4_f16x2(words[w], h);
-                                o[2 * w] = bf16x2_mul(bitselect(h[0] >> 3, h[0], kF16ToBf16Mask), kBf16x2_2p112);
-                                o[2 * w + 1] = bf16x2_mul(bitselect(h[1] >> 3, h[1], kF16ToBf16Mask), kBf16x2_2p112);
+                                o[2 * w] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[0]), kBf16x2_2p112);
+                                o[2 * w + 1] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[1]), kBf16x2_2p112);
                             }
                             sts128(bconv + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
                             sts128(bconv + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);

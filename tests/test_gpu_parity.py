@@ -48,6 +48,19 @@ def rel_err(got, ref):
     return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-300))
 
 
+def check_bf16_output(got, ref, tol=GEMM_TOL):
+    """bf16 outputs against the unrounded fp64 oracle.  The stated bound
+    (tol * max|oracle|) covers the arithmetic; the final round-to-nearest-even
+    into bf16 adds up to half an ulp of the element (up to 2^-8 of it just
+    above a power of two), which is allowed on top.  Both sides must also agree
+    on that rounding: >= 99.9% of outputs equal the oracle rounded to bf16."""
+    a = np.abs(ref)
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 8)
+    assert np.all(np.abs(got - ref) <= tol * np.max(a) + half_ulp)
+    rounded = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    assert np.mean(got == rounded) >= 0.999
+
+
 # ---------------------------------------------------------------- dense W4A16
 
 def test_w4a16_unit_scales_integer_inputs_are_exact(qlib):
@@ -84,11 +97,8 @@ def test_w4a16_tiny_workload_fp32_out(qlib):
 def test_w4a16_bf16_out_rounding(qlib):
     g = wl.gen_w4a16(200, 512, 256, 1.0 / 256, seed=77)
     Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"]), out_dtype=torch.bfloat16)
-    Yf = bf16_to_np(Y)
     ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"])
-    # round-to-nearest from fp32: at most half a bf16 ulp (2^-9 relative) plus accumulation error
-    assert np.all(np.abs(Yf - ref) <= np.abs(ref) * 2 ** -8 + 1e-6 * np.max(np.abs(ref)))
-    assert rel_err(Yf, ref) <= GEMM_TOL
+    check_bf16_output(bf16_to_np(Y), ref)
 
 
 def test_w4a16_full_size_sampled(qlib):
@@ -98,8 +108,7 @@ def test_w4a16_full_size_sampled(qlib):
     rows = np.array([0, 1, 127, 128, 1023, 1500, 2046, 2047])
     cols = np.concatenate([np.arange(0, 17408, 97), [17407, 17406, 255, 256]])
     ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"], rows=rows, cols=cols)
-    got = bf16_to_np(Y)[np.ix_(rows, cols)]
-    assert rel_err(got, ref) <= GEMM_TOL
+    check_bf16_output(bf16_to_np(Y)[np.ix_(rows, cols)], ref)
 
 
 # ---------------------------------------------------------------- dense FP8 block-128
@@ -109,7 +118,7 @@ def test_fp8_blk128_matches_oracle(qlib, M, K, N):
     g = wl.gen_fp8_blk128(M, K, N, seed=M * 3 + N)
     Y = qlib.qmm_fp8_blk128(bf16_dev(g["X"]), dev(g["W"]), dev(g["S"]))
     ref = oracle.fp8_blk128(g["X"], g["W"], g["S"])
-    assert rel_err(bf16_to_np(Y), ref) <= GEMM_TOL
+    check_bf16_output(bf16_to_np(Y), ref)
 
 
 def test_fp8_blk128_full_size_sampled(qlib):
@@ -119,7 +128,7 @@ def test_fp8_blk128_full_size_sampled(qlib):
     rows = np.array([0, 5, 127, 128, 1000, 2047])
     cols = np.concatenate([np.arange(0, 5120, 41), [5119]])
     ref = oracle.fp8_blk128(g["X"], g["W"], g["S"], rows=rows, cols=cols)
-    assert rel_err(bf16_to_np(Y)[np.ix_(rows, cols)], ref) <= GEMM_TOL
+    check_bf16_output(bf16_to_np(Y)[np.ix_(rows, cols)], ref)
 
 
 # ---------------------------------------------------------------- routing
