@@ -79,7 +79,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -364,15 +364,57 @@ def bench_dense(q, torch, device, args, peaks, peak_src):
     return out
 
 
+def run_case(args):
+    """Run one op `--steps` times after `--warmup` runs (no JSON line): a small,
+    fixed command for profiler captures of a single kernel family."""
+    import torch
+    import block_quantized_weight_route_gb300 as q
+    q.build_library()
+    dev = torch.device("cuda", 0)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    if args.case == "stage":
+        w = wl.WORKLOADS[STAGE]
+        g = wl.generate(w)
+        X, L = d(g["X"].view(np.int16)), d(g["logits"])
+        args_ = (d(g["Wgu_c"]), d(g["Wgu_s"]), d(g["gu_scale2"]), d(g["Wd_idx"]), d(g["Wd_s"].view(np.int16)))
+        ws = torch.empty(q.moe_expert_stage_workspace_size(w.T, w.D, w.F, w.E, w.k), dtype=torch.uint8, device=dev)
+        call = lambda: q.moe_expert_stage_w4_iq4(X, L, *args_, w.k, ws=ws)  # noqa: E731
+    elif args.case == "w4a16":
+        w = wl.WORKLOADS[GEMM_W4]
+        g = wl.generate(w)
+        X, Wc, Ws = d(g["X"].view(np.int16)), d(g["Wc"]), d(g["Ws"])
+        call = lambda: q.qmm_w4a16(X, Wc, Ws, float(g["scale2"]), out_dtype=torch.bfloat16)  # noqa: E731
+    else:
+        w = wl.WORKLOADS[GEMM_FP8]
+        g = wl.generate(w)
+        X, W, S = d(g["X"].view(np.int16)), d(g["W"]), d(g["S"])
+        call = lambda: q.qmm_fp8_blk128(X, W, S)  # noqa: E731
+    for _ in range(args.warmup_case):
+        call()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        call()
+    torch.cuda.synchronize()
+    q.qmm_check_status()
+    print(f"case {args.case}: {args.steps} runs, {1e3 * (time.perf_counter() - t0) / args.steps:.3f} ms/run (wall)")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--no-gemm", action="store_true", help="skip the dense GEMM measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["stage", "w4a16", "fp8"], default=None,
+                    help="run one op only (for profiler captures); prints no JSON line")
+    ap.add_argument("--warmup-case", type=int, default=1, help="untimed runs before --steps in --case mode")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = setup_dist(args.gpus)
