@@ -147,6 +147,7 @@ void stage_layout(int T, int D, int F, int E, int k, size_t* off) {
         P * F,                                      // Hq
         P * (F / 32) * 2,                           // Hd
         P * (F / 32) * 2,                           // Hs
+        (size_t)max_tile_entries(T, E, k) * (F / 32) * 128 * 4,   // Hd32: fp32 d per tile entry
         P * D * 4,                                  // Yslot
     };
     size_t o = 0;
@@ -359,7 +360,8 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     int8_t* Hq = static_cast<int8_t*>(at(10));
     __half* Hd = static_cast<__half*>(at(11));
     __half* Hs = static_cast<__half*>(at(12));
-    float* Yslot = static_cast<float*>(at(13));
+    float* Hd32 = static_cast<float*>(at(13));
+    float* Yslot = static_cast<float*>(at(14));
 
     // gate/up + SwiGLU + q8_1
     CUtensorMap ta, tb;
@@ -382,18 +384,19 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     g.Hq = Hq;
     g.Hd = Hd;
     g.Hs = Hs;
+    g.Hd32 = Hd32;
     g.err = d->err;
     e = launch_w4_gate_up_swiglu(ta, tb, g, d->sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "expert stage: gate/up launch");
     if ((e = mark(d, 3, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
-    // down (IQ4_NL x q8_1)
+    // down (IQ4_NL weights on the MMA's M side, q8_1 H codes on its N side)
     CUtensorMap ta2, tb2;
-    if ((st = make_tmap(&ta2, Hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, F, P, F, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) !=
-        QMM_OK)
-        return st;
-    if ((st = make_tmap(&tb2, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
+    if ((st = make_tmap(&ta2, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
                         CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+        return st;
+    if ((st = make_tmap(&tb2, Hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, F, P, F, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+        QMM_OK)
         return st;
     GemmParams q{};
     q.N = D;
@@ -403,7 +406,7 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     q.tiles = rb.tiles;
     q.num_entries = rb.num_entries;
     q.max_entries = max_entries;
-    q.dH = Hd;
+    q.dH32 = Hd32;
     q.dW = reinterpret_cast<const __half*>(Wd_s);
     q.Y = Yslot;
     q.ydt = 0;

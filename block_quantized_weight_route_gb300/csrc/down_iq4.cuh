@@ -1,0 +1,387 @@
+// Routed-MoE down product on sm_103a: q8_1 H times IQ4_NL weights, per expert.
+//
+//   y[t, n] = sum_b d_H[t, b] * d_W[e, n, b] * I[t, n, b]
+//   I[t, n, b] = sum_{k in block b} q[t, k] * codebook[idx[e, n, k]]      (exact)
+//
+// ("Run Edge0-145B Q3_K on AMD HIP (Linux, gfx1100)", commit 4cb5224: the
+// down product reads IQ4_NL weights against H rounded to q8_1.)
+//
+// Both operands are small integers, exact in f16, and a 32-element block sum
+// stays below 2^24, so one f16 tcgen05.mma pair per 32-K block gives I exactly
+// in fp32.  Every block gets its own TMEM accumulator (a ring of 4), which the
+// epilogue folds with d_H * d_W in fp32.
+//
+// Orientation: the MMA's M side is 128 weight rows (output dims n), its N side
+// 128 routed tokens of one expert.  Each epilogue thread owns one output dim,
+// so its d_W values live in registers; d_H varies along the columns and is read
+// from a shared-memory copy of the tile's fp32 d values (one 1-D bulk copy per
+// tile from the per-tile-entry layout the gate/up epilogue writes).
+//
+//   warp 0: TMA producer (IQ4 codes + int8 H codes per K block, d_H per tile)
+//   warp 1: TMEM owner and MMA issuer
+//   warps 4..11: epilogue (2 per TMEM lane quarter, 64 token columns each)
+//   warps 12..15: converters (one weight row and one token row per thread)
+#pragma once
+#include "qgemm.cuh"
+
+namespace qmm {
+
+struct DownCfg {
+    static constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16, GROUP_K = 32;
+    static constexpr int EPI_WARPS = 8, CONV_WARPS = 4, EPI_BASE = 4, CONV_BASE = 12;
+    static constexpr int THREADS = 32 * (4 + EPI_WARPS + CONV_WARPS);
+    static constexpr int TSTAGES = 4, CSTAGES = 3, SSTAGES = 2, NBUF = 4;
+    static constexpr int KG_MAX = 32;                         // K <= 1024
+    static constexpr int A_RAW_BYTES = BM * 32;               // IQ4 codes: 64 indices per row
+    static constexpr int B_RAW_BYTES = BN * 64;               // int8 H codes
+    static constexpr int TSTAGE_BYTES = A_RAW_BYTES + B_RAW_BYTES;
+    static constexpr int A_CONV_BYTES = BM * BK * 2, B_CONV_BYTES = BN * BK * 2;
+    static constexpr int CSTAGE_BYTES = A_CONV_BYTES + B_CONV_BYTES;
+    static constexpr int SSTAGE_BYTES = KG_MAX * BN * 4;      // d_H of one tile, [group][token] fp32
+    static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, false);
+    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * SSTAGES + 2 * NBUF + 1;
+    static constexpr int SMEM_BYTES = 1024 + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES +
+                                      SSTAGES * SSTAGE_BYTES + BAR_COUNT * 8 + 64;
+    static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0 && SSTAGE_BYTES % 1024 == 0, "align");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Wait (bounded) for the completion of the `issued` most recent fills of a ring.
+__device__ __forceinline__ void drain_ring(uint64_t* full, long issued, int stages, uint32_t* err) {
+    const long pending = issued < stages ? issued : stages;
+    for (long i = 0; i < pending; ++i) {
+        const long idx = issued - 1 - i;
+        const int s = (int)(idx % stages);
+        const uint32_t par = (uint32_t)((idx / stages) & 1);
+        if (mbar_try_wait(&full[s], par)) continue;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full[s], par)) {
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                atomicCAS(err, 0u, DEV_TIMEOUT_DRAIN);
+                break;
+            }
+        }
+    }
+}
+
+// p.K = F (reduction), p.N = D (weight rows per expert), p.n_tiles = D / 128,
+// p.tiles / num_entries / max_entries: the 128-token tile list of the routing,
+// p.dW: IQ4_NL scales [E][D][F/32] fp16, p.dH32: d_H fp32 [entry][F/32][128],
+// p.Y: Yslot [T*k][D] fp32 (p.ldy = D).
+// tmA: IQ4 codes as [E*D][F/2] bytes, box {32, 128}, 32-byte swizzle.
+// tmB: H codes as [T*k][F] bytes, box {64, 128}, 64-byte swizzle.
+__global__ void __launch_bounds__(DownCfg::THREADS, 1)
+    down_iq4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+    using C = DownCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* tstage = smem;
+    uint8_t* cstage = tstage + C::TSTAGES * C::TSTAGE_BYTES;
+    uint8_t* sstage = cstage + C::CSTAGES * C::CSTAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sstage + C::SSTAGES * C::SSTAGE_BYTES);
+    uint64_t* full_t = bars;
+    uint64_t* empty_t = full_t + C::TSTAGES;
+    uint64_t* full_c = empty_t + C::TSTAGES;
+    uint64_t* empty_c = full_c + C::CSTAGES;
+    uint64_t* full_s = empty_c + C::CSTAGES;
+    uint64_t* empty_s = full_s + C::SSTAGES;
+    uint64_t* acc_full = empty_s + C::SSTAGES;
+    uint64_t* acc_empty = acc_full + C::NBUF;
+    uint64_t* drain_bar = acc_empty + C::NBUF;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::TSTAGES; ++i) {
+            mbar_init(&full_t[i], 1);
+            mbar_init(&empty_t[i], C::CONV_WARPS);
+        }
+        for (int i = 0; i < C::CSTAGES; ++i) {
+            mbar_init(&full_c[i], C::CONV_WARPS);
+            mbar_init(&empty_c[i], 1);
+        }
+        for (int i = 0; i < C::SSTAGES; ++i) {
+            mbar_init(&full_s[i], 1);
+            mbar_init(&empty_s[i], C::EPI_WARPS);
+        }
+        for (int i = 0; i < C::NBUF; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], C::EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int kblocks = p.K / C::BK;
+    const int groups = p.K / C::GROUP_K;
+    const int entries = min(*p.num_entries, p.max_entries);
+    const int num_tiles = entries * p.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0, ss = 0;
+            uint32_t ph = 0, sph = 0;
+            long issued = 0, s_issued = 0;
+            bool ok = true;
+            const uint32_t sbytes = (uint32_t)(groups * C::BN * 4);
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const int entry = t / p.n_tiles;
+                const int n0 = (t - entry * p.n_tiles) * C::BM;
+                const int4 g = p.tiles[entry];
+                // this tile's d_H values
+                if (!mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) break;
+                mbar_arrive_expect_tx(&full_s[ss], sbytes);
+                bulk_load(sstage + ss * C::SSTAGE_BYTES, p.dH32 + (long)entry * groups * C::BN, sbytes, &full_s[ss]);
+                ++s_issued;
+                if (++ss == C::SSTAGES) {
+                    ss = 0;
+                    sph ^= 1u;
+                }
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                    mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                    tma_load_2d(st, &tmA, &full_t[s], kb * 32, g.x * p.N + n0);
+                    tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
+                    ++issued;
+                    if (++s == C::TSTAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            drain_ring(full_t, issued, C::TSTAGES, p.err);
+            drain_ring(full_s, s_issued, C::SSTAGES, p.err);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int cs = 0, buf = 0;
+            uint32_t cph = 0, bph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < kblocks && ok; ++kb) {
+                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+                    const uint32_t b_base = a_base + C::A_CONV_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+                        const bool first = (kk & 1) == 0, last = (kk & 1) == 1;
+                        if (first) {
+                            if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        tc_mma_f16(tmem_base + (uint32_t)(buf * C::BN), smem_desc_sw128(a_base + kk * 32),
+                                   smem_desc_sw128(b_base + kk * 32), C::IDESC, first ? 0u : 1u);
+                        if (last) {
+                            tc_commit(&acc_full[buf]);
+                            if (++buf == C::NBUF) {
+                                buf = 0;
+                                bph ^= 1u;
+                            }
+                        }
+                    }
+                    if (!ok) break;
+                    tc_commit(&empty_c[cs]);
+                    if (++cs == C::CSTAGES) {
+                        cs = 0;
+                        cph ^= 1u;
+                    }
+                }
+            }
+            tc_commit(drain_bar);
+            if (!mbar_try_wait(drain_bar, 0)) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(drain_bar, 0)) {
+                    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                        atomicCAS(p.err, 0u, DEV_TIMEOUT_DRAIN);
+                        break;
+                    }
+                }
+            }
+        }
+    } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int half = (warp - C::EPI_BASE) >> 2;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+        int buf = 0, ss = 0;
+        uint32_t bph = 0, sph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const int entry = t / p.n_tiles;
+            const int n0 = (t - entry * p.n_tiles) * C::BM;
+            const int4 g4 = p.tiles[entry];
+            const int n = n0 + q * 32 + lane;                   // this thread's output dim
+            // d_W[e, n, 0..groups) as half2 pairs (groups <= 32, 16-byte vector loads)
+            uint32_t dwh[C::KG_MAX / 2];
+            const __half* dw_row = p.dW + ((long)g4.x * p.N + n) * groups;
+            if ((groups & 7) == 0) {            // rows are whole 16-byte vectors
+                const uint4* dwp = reinterpret_cast<const uint4*>(dw_row);
+#pragma unroll
+                for (int i = 0; i < C::KG_MAX / 8; ++i) {
+                    if (i * 8 < groups) {
+                        const uint4 v = __ldg(dwp + i);
+                        dwh[4 * i] = v.x;
+                        dwh[4 * i + 1] = v.y;
+                        dwh[4 * i + 2] = v.z;
+                        dwh[4 * i + 3] = v.w;
+                    } else {
+                        dwh[4 * i] = dwh[4 * i + 1] = dwh[4 * i + 2] = dwh[4 * i + 3] = 0u;
+                    }
+                }
+            } else {
+                const unsigned short* dws = reinterpret_cast<const unsigned short*>(dw_row);
+#pragma unroll
+                for (int i = 0; i < C::KG_MAX / 2; ++i) {
+                    const uint32_t lo = (2 * i < groups) ? __ldg(dws + 2 * i) : 0u;
+                    const uint32_t hi = (2 * i + 1 < groups) ? __ldg(dws + 2 * i + 1) : 0u;
+                    dwh[i] = lo | (hi << 16);
+                }
+            }
+            if (!mbar_wait(&full_s[ss], sph, abort_flag, p.err, DEV_TIMEOUT_ACC)) break;
+            const uint32_t dh_base = smem_u32(sstage + ss * C::SSTAGE_BYTES) + half * 64 * 4;
+            uint64_t y[32];                                       // 64 token columns as f32 pairs
+#pragma unroll
+            for (int j = 0; j < 32; ++j) y[j] = 0ull;
+            for (int g = 0; g < groups; ++g) {
+                if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t pair = dwh[g >> 1];
+                const float dwf = __half2float(__ushort_as_half((unsigned short)((g & 1) ? (pair >> 16) : (pair & 0xFFFFu))));
+                const uint64_t dw2 = f32x2_pack(dwf, dwf);
+                const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + half * 64);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(acc + c * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 dh = lds128(dh_base + (uint32_t)((g * C::BN + c * 32 + 4 * j) * 4));
+                        const uint64_t i01 = f32x2_pack(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]));
+                        const uint64_t i23 = f32x2_pack(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        const uint64_t d01 = f32x2_pack(__uint_as_float(dh.x), __uint_as_float(dh.y));
+                        const uint64_t d23 = f32x2_pack(__uint_as_float(dh.z), __uint_as_float(dh.w));
+                        y[c * 16 + 2 * j] = f32x2_fma(f32x2_mul(i01, d01), dw2, y[c * 16 + 2 * j]);
+                        y[c * 16 + 2 * j + 1] = f32x2_fma(f32x2_mul(i23, d23), dw2, y[c * 16 + 2 * j + 1]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                if (++buf == C::NBUF) {
+                    buf = 0;
+                    bph ^= 1u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_s[ss]);
+            if (++ss == C::SSTAGES) {
+                ss = 0;
+                sph ^= 1u;
+            }
+            if (!ok) break;
+            // Yslot[row, n] for this warp's 64 token columns; lanes write consecutive n
+            float* out = static_cast<float*>(p.Y) + (long)g4.y * p.ldy + n;
+            const int tok0 = half * 64;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                float lo, hi;
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(y[j]));
+                if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = lo;
+                if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = hi;
+            }
+        }
+    } else if (warp >= C::CONV_BASE) {
+        // ------------------------------------------------------------ converters
+        const int ct = threadIdx.x - C::CONV_BASE * 32;
+        int ts = 0, cs = 0;
+        uint32_t tph = 0, cph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
+                    !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t traw = smem_u32(tstage + ts * C::TSTAGE_BYTES);
+                const uint32_t cbase = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+                convert_iq4_row(traw, cbase, ct);
+                convert_i8_row(traw + C::A_RAW_BYTES, cbase + C::A_CONV_BYTES, ct);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&full_c[cs]);
+                    mbar_arrive(&empty_t[ts]);
+                }
+                if (++ts == C::TSTAGES) {
+                    ts = 0;
+                    tph ^= 1u;
+                }
+                if (++cs == C::CSTAGES) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace qmm

@@ -5,7 +5,7 @@
 
 namespace qmm {
 
-using CfgFp8 = GemmCfg<AMode::BF16_TMA, BMode::FP8, Epi::FOLD_FP8, 128, 4, 8, 4, 4, false>;
+using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 4, 8, 4, 4, false>;
 
 int smem_fp8_blk128() { return CfgFp8::SMEM_BYTES; }
 

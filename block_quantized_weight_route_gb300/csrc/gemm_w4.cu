@@ -6,9 +6,9 @@
 namespace qmm {
 
 // Dense: 128 x 256 tiles, 8 converter warps (one weight row per thread), 4 epilogue warps.
-using CfgW4Dense = GemmCfg<AMode::BF16_TMA, BMode::W4, Epi::STORE, 256, 8, 4, 4, 3, false>;
+using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 256, 8, 4, 4, 3, false>;
 // Gate/up: 128 token rows x (128 gate + 128 up) weight rows per tile.
-using CfgW4GateUp = GemmCfg<AMode::BF16_TMA, BMode::W4, Epi::SWIGLU_Q81, 256, 8, 4, 4, 3, true>;
+using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 256, 8, 4, 4, 3, true>;
 
 int smem_w4a16_dense() { return CfgW4Dense::SMEM_BYTES; }
 int smem_w4_gate_up_swiglu() { return CfgW4GateUp::SMEM_BYTES; }

@@ -17,10 +17,11 @@
 //    twins").  e2m1 x E4M3 is exact in bf16, so the dequantised operand is exact.
 //  - FP8 with one fp32 scale per 128x128 block: each 128-K block is accumulated
 //    unscaled and folded once with its scale (same page, FP8 block-scaling twin).
-//  - IQ4_NL x q8_1: one exact integer dot per 32-K block (both operands are small
-//    integers, exact in f16, block sums < 2^24 exact in fp32), folded with the
-//    two fp16 block scales ("Run Edge0-145B Q3_K on AMD HIP (Linux, gfx1100)",
-//    commit 4cb5224: gate/up, SwiGLU, q8_1 H, IQ4_NL down).
+//  - routed-MoE gate/up: per expert, X rows of the expert's tokens times its W4
+//    gate and up rows; the epilogue applies SwiGLU and rounds H to q8_1 blocks
+//    of 32 ("Run Edge0-145B Q3_K on AMD HIP (Linux, gfx1100)", commit 4cb5224).
+// The IQ4_NL down product has its own kernel (down_iq4.cuh) built from the
+// same pieces.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -30,14 +31,11 @@
 
 namespace qmm {
 
-enum class AMode { BF16_TMA, I8_CONV };
-enum class BMode { W4, FP8, IQ4 };
-enum class Epi { STORE, SWIGLU_Q81, FOLD_FP8, FOLD_IQ4 };
+enum class BMode { W4, FP8 };
+enum class Epi { STORE, SWIGLU_Q81, FOLD_FP8 };
 
-template <AMode A_, BMode B_, Epi E_, int BN_, int CONV_WARPS_, int EPI_WARPS_, int TSTAGES_, int CSTAGES_,
-          bool GROUPED_>
+template <BMode B_, Epi E_, int BN_, int CONV_WARPS_, int EPI_WARPS_, int TSTAGES_, int CSTAGES_, bool GROUPED_>
 struct GemmCfg {
-    static constexpr AMode A = A_;
     static constexpr BMode B = B_;
     static constexpr Epi EPI = E_;
     static constexpr bool GROUPED = GROUPED_;
@@ -46,36 +44,30 @@ struct GemmCfg {
     static constexpr int EPI_BASE = 4, CONV_BASE = 4 + EPI_WARPS_;
     static constexpr int THREADS = 32 * (4 + EPI_WARPS_ + CONV_WARPS_);
     static constexpr int TSTAGES = TSTAGES_, CSTAGES = CSTAGES_;
-    static constexpr bool A_DIRECT = (A_ == AMode::BF16_TMA);
-    // raw (TMA) stage
-    static constexpr int A_RAW_BYTES = BM * BK * (A_DIRECT ? 2 : 1);
+    // raw (TMA) stage: bf16 activation tile (read by the MMA in place) + weight codes
+    static constexpr int A_RAW_BYTES = BM * BK * 2;
     static constexpr int B_ROW_BYTES = (B_ == BMode::FP8) ? 64 : 32;   // bytes of codes per weight row per k-block
     static constexpr int B_RAW_BYTES = BN * B_ROW_BYTES;
     static constexpr int TSTAGE_BYTES = A_RAW_BYTES + B_RAW_BYTES;
-    // converted stage
-    static constexpr int A_CONV_BYTES = A_DIRECT ? 0 : BM * BK * 2;
-    static constexpr int B_CONV_BYTES = BN * BK * 2;
-    static constexpr int CSTAGE_BYTES = A_CONV_BYTES + B_CONV_BYTES;
-    // accumulation groups
-    static constexpr bool FOLD = (E_ == Epi::FOLD_FP8 || E_ == Epi::FOLD_IQ4);
-    static constexpr int GROUP_K = (E_ == Epi::FOLD_FP8) ? 128 : (E_ == Epi::FOLD_IQ4 ? 32 : 0);   // 0: whole K
+    // converted stage: the bf16 weight tile
+    static constexpr int CSTAGE_BYTES = BN * BK * 2;
+    // accumulation groups: the whole K, or one per 128-K block (FP8 fold)
+    static constexpr bool FOLD = (E_ == Epi::FOLD_FP8);
+    static constexpr int GROUP_K = FOLD ? 128 : 0;   // 0: whole K
     static constexpr int NBUF = 512 / BN;
-    static constexpr bool BF16_OPERANDS = (B_ != BMode::IQ4);
-    static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, BF16_OPERANDS);
-    // epilogue staging for the IQ4 fold, per epilogue warp: dW [KG][64] and dH [KG][32] fp16
-    static constexpr int KG_MAX = 32;   // K / 32 groups at most (K <= 1024)
-    static constexpr int EPI_SMEM = (E_ == Epi::FOLD_IQ4) ? EPI_WARPS_ * KG_MAX * 96 * 2 : 0;
+    static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, true);
     static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * NBUF + 1;
     static constexpr int SMEM_BYTES =
-        1024 /*align slack*/ + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES + EPI_SMEM + BAR_COUNT * 8 + 64;
+        1024 /*align slack*/ + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES + BAR_COUNT * 8 + 64;
     static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
     static_assert(!FOLD || EPI_WARPS == 8, "fold epilogue splits columns over two warpgroups");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
+    static_assert(BN == CONV_WARPS * 32, "one weight row per converter thread");
 };
 
 struct TileInfo {
-    int expert, row0, rows, n0;
+    int expert, row0, rows, n0, entry;
 };
 
 template <class C>
@@ -88,12 +80,14 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
         ti.row0 = g.y;
         ti.rows = g.z;
         ti.n0 = nt * p.n_step;
+        ti.entry = entry;
     } else {
         const int mt = t % p.m_tiles, nt = t / p.m_tiles;
         ti.expert = 0;
         ti.row0 = mt * C::BM;
         ti.rows = min(C::BM, p.M - ti.row0);
         ti.n0 = nt * p.n_step;
+        ti.entry = mt;
     }
     return ti;
 }
@@ -155,6 +149,99 @@ constexpr uint32_t kIq4T3 = 0xF1D9C5B5u;   //   53   69   89  113
 // f16 bits 0x64XX are 1024 + XX; subtracting 1152 leaves XX - 128.
 constexpr uint32_t kF16x2_1152 = 0x64806480u;
 
+// ---------------------------------------------------------------------------
+// Row converters: one thread turns one row of raw codes for a 64-wide K block
+// into 64 exact 16-bit operand values, written as 8 chunks of 16 bytes into a
+// 128-byte-swizzled K-major tile.
+
+// W4: 64 e2m1 codes (32 bytes, 32-byte-swizzled rows) and 4 E4M3 scale bytes.
+__device__ __forceinline__ void convert_w4_row(uint32_t raw_tile, uint32_t dst_tile, int r, uint32_t sbytes) {
+    const int sw = (r >> 2) & 1;
+    const uint4 c0 = lds128(raw_tile + r * 32 + ((0 ^ sw) << 4));
+    const uint4 c1 = lds128(raw_tile + r * 32 + ((1 ^ sw) << 4));
+    uint32_t sc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] = w4_scale_bf16x2(sbytes >> (8 * i));
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        uint32_t h[4], o[4];
+        cvt_e2m1x8_f16x2(words[w], h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[i]), sc[w >> 1]);
+        sts128(dst_tile + sw128_off(r, w), o[0], o[1], o[2], o[3]);
+    }
+}
+
+// FP8: 64 E4M3 bytes (64-byte-swizzled rows) -> exact bf16.
+__device__ __forceinline__ void convert_fp8_row(uint32_t raw_tile, uint32_t dst_tile, int r) {
+    const int sw = (r >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 v = lds128(raw_tile + r * 64 + ((c ^ sw) << 4));
+        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t h[2];
+            cvt_e4m3x4_f16x2(words[w], h);
+            o[2 * w] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[0]), kBf16x2_2p112);
+            o[2 * w + 1] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[1]), kBf16x2_2p112);
+        }
+        sts128(dst_tile + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
+        sts128(dst_tile + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
+    }
+}
+
+// IQ4_NL: 64 4-bit indices (32 bytes, 32-byte-swizzled rows) -> exact f16 codebook values.
+__device__ __forceinline__ void convert_iq4_row(uint32_t raw_tile, uint32_t dst_tile, int r) {
+    const int sw = (r >> 2) & 1;
+    const uint4 c0 = lds128(raw_tile + r * 32 + ((0 ^ sw) << 4));
+    const uint4 c1 = lds128(raw_tile + r * 32 + ((1 ^ sw) << 4));
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t x = words[w];
+        const uint32_t x4 = x << 4;
+        const uint32_t xh = x >> 16;
+        // elements 0..3 (low 16 bits) and 4..7 (high 16 bits): codebook byte from
+        // entries 0-7 or 8-15 chosen by bit 3 of each index
+        const uint32_t v_a = bitselect(prmt(kIq4T0, kIq4T1, x), prmt(kIq4T2, kIq4T3, x & 0x7777u), prmt(x4, x, 0xD9C8u));
+        const uint32_t v_b =
+            bitselect(prmt(kIq4T0, kIq4T1, xh), prmt(kIq4T2, kIq4T3, xh & 0x7777u), prmt(x4, x, 0xFBEAu));
+        const uint32_t o0 = f16x2_sub(prmt(v_a, 0x64646464u, 0x5140u), kF16x2_1152);
+        const uint32_t o1 = f16x2_sub(prmt(v_a, 0x64646464u, 0x5342u), kF16x2_1152);
+        const uint32_t o2 = f16x2_sub(prmt(v_b, 0x64646464u, 0x5140u), kF16x2_1152);
+        const uint32_t o3 = f16x2_sub(prmt(v_b, 0x64646464u, 0x5342u), kF16x2_1152);
+        sts128(dst_tile + sw128_off(r, w), o0, o1, o2, o3);
+    }
+}
+
+// int8: 64 codes (64-byte-swizzled rows) -> exact f16.
+__device__ __forceinline__ void convert_i8_row(uint32_t raw_tile, uint32_t dst_tile, int r) {
+    const int sw = (r >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 v = lds128(raw_tile + r * 64 + ((c ^ sw) << 4));
+        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t x = words[w] ^ 0x80808080u;
+            o[2 * w] = f16x2_sub(prmt(x, 0x64646464u, 0x5140u), kF16x2_1152);
+            o[2 * w + 1] = f16x2_sub(prmt(x, 0x64646464u, 0x5342u), kF16x2_1152);
+        }
+        sts128(dst_tile + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
+        sts128(dst_tile + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
+    }
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
@@ -162,8 +249,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tstage = smem;
     uint8_t* cstage = tstage + C::TSTAGES * C::TSTAGE_BYTES;
-    uint8_t* epi_smem = cstage + C::CSTAGES * C::CSTAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + C::EPI_SMEM);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cstage + C::CSTAGES * C::CSTAGE_BYTES);
     uint64_t* full_t = bars;
     uint64_t* empty_t = full_t + C::TSTAGES;
     uint64_t* full_c = empty_t + C::TSTAGES;
@@ -179,7 +265,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::TSTAGES; ++i) {
             mbar_init(&full_t[i], 1);
-            mbar_init(&empty_t[i], C::A_DIRECT ? 1 : C::CONV_WARPS);
+            mbar_init(&empty_t[i], 1);   // released by the MMA's commit (it read the activation tile)
         }
         for (int i = 0; i < C::CSTAGES; ++i) {
             mbar_init(&full_c[i], C::CONV_WARPS);
@@ -272,7 +358,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
-                    if (C::A_DIRECT && !mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL)) {
+                    if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL)) {
                         ok = false;
                         break;
                     }
@@ -281,10 +367,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    uint8_t* cst = cstage + cs * C::CSTAGE_BYTES;
-                    const uint32_t a_base =
-                        C::A_DIRECT ? smem_u32(tstage + ts * C::TSTAGE_BYTES) : smem_u32(cst);
-                    const uint32_t b_base = smem_u32(cst + C::A_CONV_BYTES);
+                    const uint32_t a_base = smem_u32(tstage + ts * C::TSTAGE_BYTES);
+                    const uint32_t b_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
                         const int kg = kb * C::BK + kk * C::UMMA_K;
@@ -310,7 +394,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                     if (!ok) break;
                     tc_commit(&empty_c[cs]);
-                    if (C::A_DIRECT) tc_commit(&empty_t[ts]);
+                    tc_commit(&empty_t[ts]);
                     if (++ts == C::TSTAGES) {
                         ts = 0;
                         tph ^= 1u;
@@ -430,8 +514,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             hq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                             hq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                             const long bidx = grow * (p.F / 32) + col / 32;
-                            p.Hd[bidx] = __float2half_rn(d);
+                            const __half d16 = __float2half_rn(d);
+                            p.Hd[bidx] = d16;
                             p.Hs[bidx] = __float2half_rn(d * (float)sum);
+                            // the value the down product uses, fp32, per tile entry [entry][F/32][128 rows]
+                            p.Hd32[((long)ti.entry * (p.F / 32) + col / 32) * C::BM + row] = __half2float(d16);
                         }
                     }
                 }
@@ -443,41 +530,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     bph ^= 1u;
                 }
             } else {
-                // fold: one accumulator per K group, folded into registers with its scale
+                // FP8 fold: one accumulator per 128-K block, folded into registers with its scale
                 const int groups = p.K / C::GROUP_K;
                 float sum[64];
 #pragma unroll
                 for (int j = 0; j < 64; ++j) sum[j] = 0.f;
-                // IQ4: this warp's own copy of the block scales it needs, staged
-                // without any cross-warp barrier: dW [KG][64 columns], dH [KG][32 rows].
-                __half* dWs = reinterpret_cast<__half*>(epi_smem) + (warp - C::EPI_BASE) * (C::KG_MAX * 96);
-                __half* dHs = dWs + C::KG_MAX * 64;
-                if constexpr (C::EPI == Epi::FOLD_IQ4) {
-                    __syncwarp();   // the previous tile's reads of this warp are done
-                    const long wcol0 = (long)ti.expert * p.N + ti.n0 + half * 64;
-                    for (int i = lane; i < 64 * groups; i += 32) {
-                        const int n = i / groups, g = i - n * groups;
-                        dWs[g * 64 + n] = p.dW[(wcol0 + n) * groups + g];
-                    }
-                    for (int i = lane; i < 32 * groups; i += 32) {
-                        const int r = i / groups, g = i - r * groups;
-                        const int trow = q * 32 + r;
-                        dHs[g * 32 + r] =
-                            (trow < ti.rows) ? p.dH[((long)ti.row0 + trow) * groups + g] : __float2half(0.f);
-                    }
-                    __syncwarp();
-                }
                 for (int g = 0; g < groups; ++g) {
                     if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t r0[32], r1[32];
+                    const float s = __ldg(p.blk_scale + (long)(ti.n0 / 128) * groups + g);
                     const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + half * 64);
-                    tmem_ld32(acc, r0);
-                    tmem_ld32(acc + 32, r1);
-                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(acc + c * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sum[c * 32 + j] = fmaf(s, __uint_as_float(r[j]), sum[c * 32 + j]);
+                    }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -485,169 +558,90 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         buf = 0;
                         bph ^= 1u;
                     }
-                    if constexpr (C::EPI == Epi::FOLD_FP8) {
-                        const float s = p.blk_scale[(long)(ti.n0 / 128) * groups + g];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            sum[j] = fmaf(s, __uint_as_float(r0[j]), sum[j]);
-                            sum[32 + j] = fmaf(s, __uint_as_float(r1[j]), sum[32 + j]);
-                        }
-                    } else {
-                        const float dh = __half2float(dHs[g * 32 + lane]);
-                        const __half* dw = dWs + g * 64;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            sum[j] = fmaf(__uint_as_float(r0[j]) * __half2float(dw[j]), dh, sum[j]);
-                            sum[32 + j] = fmaf(__uint_as_float(r1[j]) * __half2float(dw[32 + j]), dh, sum[32 + j]);
-                        }
-                    }
                 }
                 if (!ok) break;
                 if (valid) {
                     const int col = ti.n0 + half * 64;
-                    if constexpr (C::EPI == Epi::FOLD_FP8) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            uint32_t w[4];
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t w[4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                __nv_bfloat162 b = __floats2bfloat162_rn(sum[8 * j + 2 * i], sum[8 * j + 2 * i + 1]);
-                                w[i] = *reinterpret_cast<uint32_t*>(&b);
-                            }
-                            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat162 b = __floats2bfloat162_rn(sum[8 * j + 2 * i], sum[8 * j + 2 * i + 1]);
+                            w[i] = *reinterpret_cast<uint32_t*>(&b);
                         }
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + grow * p.ldy + col);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            dst[j] = make_float4(sum[4 * j], sum[4 * j + 1], sum[4 * j + 2], sum[4 * j + 3]);
+                        dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
         }
     } else if (warp >= C::CONV_BASE) {
         // ------------------------------------------------------------ converters
-        const int ct = threadIdx.x - C::CONV_BASE * 32;
-        constexpr int CT = C::CONV_WARPS * 32;
+        const int ct = threadIdx.x - C::CONV_BASE * 32;   // this thread's weight row in every tile
         int ts = 0, cs = 0;
         uint32_t tph = 0, cph = 0;
         bool ok = true;
+        // W4 scales: 16-byte loads covering 4 K blocks, one chunk ahead (K % 256 == 0),
+        // else one 4-byte load per K block.
+        const bool vec_scales = (p.K % 256) == 0;
+        const int kchunks = kblocks / 4;
+        auto scale_row = [&](const TileInfo& tt, bool& in_range) -> long {
+            if constexpr (C::EPI == Epi::SWIGLU_Q81) {
+                const int hr = (ct < C::BN / 2) ? (tt.n0 + ct) : (p.F + tt.n0 + ct - C::BN / 2);
+                in_range = true;
+                return (long)tt.expert * 2 * p.F + hr;
+            } else {
+                in_range = (long)tt.n0 + ct < p.N;
+                return (long)tt.n0 + ct;
+            }
+        };
+        auto load_chunk = [&](int t, int ch) -> uint4 {
+            if (t >= num_tiles) return make_uint4(0, 0, 0, 0);
+            const TileInfo tt = decode_tile<C>(p, t);
+            bool in_range;
+            const long wrow = scale_row(tt, in_range);
+            return in_range ? ldg_nc_v4(p.w_scale + wrow * (p.K / 16) + ch * 16) : make_uint4(0, 0, 0, 0);
+        };
+        uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = make_uint4(0, 0, 0, 0);
+        if constexpr (C::B == BMode::W4) {
+            if (vec_scales) sc_next = load_chunk(blockIdx.x, 0);
+        }
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             const TileInfo ti = decode_tile<C>(p, t);
             for (int kb = 0; kb < kblocks; ++kb) {
+                uint32_t sbytes = 0;
+                if constexpr (C::B == BMode::W4) {
+                    if (vec_scales) {
+                        if ((kb & 3) == 0) {
+                            sc_cur = sc_next;
+                            const int ch = (kb >> 2) + 1;
+                            sc_next = (ch < kchunks) ? load_chunk(t, ch) : load_chunk(t + gridDim.x, 0);
+                        }
+                        const int j = kb & 3;
+                        sbytes = j == 0 ? sc_cur.x : (j == 1 ? sc_cur.y : (j == 2 ? sc_cur.z : sc_cur.w));
+                    } else {
+                        bool in_range;
+                        const long wrow = scale_row(ti, in_range);
+                        sbytes = in_range ? __ldg(reinterpret_cast<const uint32_t*>(p.w_scale + wrow * (p.K / 16) + kb * 4))
+                                          : 0u;
+                    }
+                }
                 if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
                     !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY)) {
                     ok = false;
                     break;
                 }
-                const uint32_t traw = smem_u32(tstage + ts * C::TSTAGE_BYTES);
-                const uint32_t braw = traw + C::A_RAW_BYTES;
-                const uint32_t cbase = smem_u32(cstage + cs * C::CSTAGE_BYTES);
-                const uint32_t bconv = cbase + C::A_CONV_BYTES;
-                for (int r = ct; r < C::BN; r += CT) {
-                    if constexpr (C::B == BMode::W4) {
-                        // 64 e2m1 codes (32 bytes, 32-byte-swizzled rows) + 4 scale bytes
-                        const int sw = (r >> 2) & 1;
-                        const uint4 c0 = lds128(braw + r * 32 + ((0 ^ sw) << 4));
-                        const uint4 c1 = lds128(braw + r * 32 + ((1 ^ sw) << 4));
-                        long wrow;
-                        bool in_range;
-                        if constexpr (C::EPI == Epi::SWIGLU_Q81) {
-                            const int hr = (r < C::BN / 2) ? (ti.n0 + r) : (p.F + ti.n0 + r - C::BN / 2);
-                            wrow = (long)ti.expert * 2 * p.F + hr;
-                            in_range = true;
-                        } else {
-                            wrow = (long)ti.n0 + r;
-                            in_range = wrow < p.N;
-                        }
-                        const uint32_t sbytes =
-                            in_range ? __ldg(reinterpret_cast<const uint32_t*>(p.w_scale + wrow * (p.K / 16) + kb * 4)) : 0u;
-                        uint32_t sc[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) sc[i] = w4_scale_bf16x2(sbytes >> (8 * i));
-                        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                        for (int w = 0; w < 8; ++w) {
-                            uint32_t h[4], o[4];
-                            cvt_e2m1x8_f16x2(words[w], h);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[i]), sc[w >> 1]);
-                            sts128(bconv + sw128_off(r, w), o[0], o[1], o[2], o[3]);
-                        }
-                    } else if constexpr (C::B == BMode::FP8) {
-                        // 64 E4M3 bytes (64-byte-swizzled rows)
-                        const int sw = (r >> 1) & 3;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 v = lds128(braw + r * 64 + ((c ^ sw) << 4));
-                            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-                            uint32_t o[8];
-#pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                uint32_t h[2];
-                                cvt_e4m3x4_f16x2(words[w], h);
-                                o[2 * w] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[0]), kBf16x2_2p112);
-                                o[2 * w + 1] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[1]), kBf16x2_2p112);
-                            }
-                            sts128(bconv + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
-                            sts128(bconv + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
-                        }
-                    } else {
-                        // 64 IQ4_NL indices (32 bytes, 32-byte-swizzled rows) -> exact f16 codebook values
-                        const int sw = (r >> 2) & 1;
-                        const uint4 c0 = lds128(braw + r * 32 + ((0 ^ sw) << 4));
-                        const uint4 c1 = lds128(braw + r * 32 + ((1 ^ sw) << 4));
-                        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                        for (int w = 0; w < 8; ++w) {
-                            const uint32_t x = words[w];
-                            const uint32_t x4 = x << 4;
-                            const uint32_t xh = x >> 16;
-                            // elements 0..3 (low 16 bits) and 4..7 (high 16 bits)
-                            const uint32_t lo_a = prmt(kIq4T0, kIq4T1, x);
-                            const uint32_t hi_a = prmt(kIq4T2, kIq4T3, x & 0x7777u);
-                            const uint32_t m_a = prmt(x4, x, 0xD9C8u);
-                            const uint32_t v_a = bitselect(lo_a, hi_a, m_a);
-                            const uint32_t lo_b = prmt(kIq4T0, kIq4T1, xh);
-                            const uint32_t hi_b = prmt(kIq4T2, kIq4T3, xh & 0x7777u);
-                            const uint32_t m_b = prmt(x4, x, 0xFBEAu);
-                            const uint32_t v_b = bitselect(lo_b, hi_b, m_b);
-                            const uint32_t o0 = f16x2_sub(prmt(v_a, 0x64646464u, 0x5140u), kF16x2_1152);
-                            const uint32_t o1 = f16x2_sub(prmt(v_a, 0x64646464u, 0x5342u), kF16x2_1152);
-                            const uint32_t o2 = f16x2_sub(prmt(v_b, 0x64646464u, 0x5140u), kF16x2_1152);
-                            const uint32_t o3 = f16x2_sub(prmt(v_b, 0x64646464u, 0x5342u), kF16x2_1152);
-                            sts128(bconv + sw128_off(r, w), o0, o1, o2, o3);
-                        }
-                    }
-                }
-                if constexpr (!C::A_DIRECT) {
-                    // int8 activations (64-byte-swizzled rows of 64 codes) -> exact f16
-                    for (int r = ct; r < C::BM; r += CT) {
-                        const int sw = (r >> 1) & 3;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 v = lds128(traw + r * 64 + ((c ^ sw) << 4));
-                            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-                            uint32_t o[8];
-#pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                const uint32_t x = words[w] ^ 0x80808080u;
-                                o[2 * w] = f16x2_sub(prmt(x, 0x64646464u, 0x5140u), kF16x2_1152);
-                                o[2 * w + 1] = f16x2_sub(prmt(x, 0x64646464u, 0x5342u), kF16x2_1152);
-                            }
-                            sts128(cbase + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
-                            sts128(cbase + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
-                        }
-                    }
+                const uint32_t braw = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
+                const uint32_t bconv = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+                if constexpr (C::B == BMode::W4) {
+                    convert_w4_row(braw, bconv, ct, sbytes);
+                } else {
+                    convert_fp8_row(braw, bconv, ct);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&full_c[cs]);
-                    if constexpr (!C::A_DIRECT) mbar_arrive(&empty_t[ts]);
-                }
+                if (lane == 0) mbar_arrive(&full_c[cs]);
                 if (++ts == C::TSTAGES) {
                     ts = 0;
                     tph ^= 1u;

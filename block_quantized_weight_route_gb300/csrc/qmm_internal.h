@@ -21,7 +21,7 @@ struct GemmParams {
     const float* scale2;    // gate/up: fp32 scale2 per expert
     float scale2_dense;     // dense W4: fp32 scale2
     const float* blk_scale; // FP8: [N/128][K/128] block scales
-    const __half* dH;       // down: q8_1 block scales of H, [rows][K/32]
+    const float* dH32;      // down: fp32 d of H per 128-row tile entry, [entry][K/32][128]
     const __half* dW;       // down: IQ4_NL block scales, [E][N][K/32]
     void* Y;                // output (fp32 or bf16)
     int ydt;                // 0: fp32, 1: bf16
@@ -29,6 +29,7 @@ struct GemmParams {
     int8_t* Hq;             // gate/up: q8_1 codes of H [rows][F]
     __half* Hd;             // gate/up: q8_1 d per 32-block [rows][F/32]
     __half* Hs;             // gate/up: q8_1 s per 32-block [rows][F/32]
+    float* Hd32;            // gate/up: fp32 value of the fp16 d, [entry][F/32][128 rows]
     uint32_t* err;          // device error word
 };
 

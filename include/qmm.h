@@ -134,9 +134,10 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t *X, const float *logits, int T
  *   0 ids [T*k] i32     1 w [T*k] f32       2 counts [E] i32    3 offsets [E+1] i32
  *   4 src [T*k] i32     5 row [T*k] i32     6 chunk counts      7 tile list
  *   8 tile count        9 X_perm [T*k][D] bf16   10 Hq [T*k][F] int8
- *  11 Hd [T*k][F/32] fp16   12 Hs [T*k][F/32] fp16   13 Yslot [T*k][D] fp32
- *  14 total size */
-#define QMM_WS_FIELDS 15
+ *  11 Hd [T*k][F/32] fp16   12 Hs [T*k][F/32] fp16
+ *  13 d of H as fp32 per 128-row tile (internal)   14 Yslot [T*k][D] fp32
+ *  15 total size */
+#define QMM_WS_FIELDS 16
 qmm_status moe_expert_stage_workspace_layout(int T, int D, int F, int E, int k, size_t *offsets_out);
 
 /*

@@ -88,7 +88,7 @@ def test_expert_stage_workspace_layout_is_consistent(L):
         # the large regions have at least their nominal sizes
         assert off[10] - off[9] >= P * D * 2          # X_perm
         assert off[11] - off[10] >= P * F             # Hq
-        assert off[14] - off[13] >= P * D * 4         # Yslot
+        assert off[15] - off[14] >= P * D * 4         # Yslot
     arr = (ctypes.c_size_t * QMM_WS_FIELDS)()
     assert L.moe_expert_stage_workspace_layout(10, 100, 128, 8, 2, arr) == 2     # D % 128
     assert L.moe_expert_stage_workspace_layout(10, 128, 2048, 8, 2, arr) == 2    # F > 1024
