@@ -20,7 +20,8 @@
 //   warp 0: TMA producer (IQ4 codes + int8 H codes per K block, d_H per tile)
 //   warp 1: TMEM owner and MMA issuer
 //   warps 4..11: epilogue (2 per TMEM lane quarter, 64 token columns each)
-//   warps 12..15: converters (one weight row and one token row per thread)
+//   warps 2, 3, 12, 14: converters (one weight row and one token row per thread),
+//   kept off the MMA issuer's sub-partition (warp id % 4 == 1)
 #pragma once
 #include "qgemm.cuh"
 
@@ -28,8 +29,14 @@ namespace qmm {
 
 struct DownCfg {
     static constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16, GROUP_K = 32;
-    static constexpr int EPI_WARPS = 8, CONV_WARPS = 4, EPI_BASE = 4, CONV_BASE = 12;
-    static constexpr int THREADS = 32 * (4 + EPI_WARPS + CONV_WARPS);
+    // 16 warps: producer 0, MMA 1, epilogue 4..11, converters 2, 3, 12, 14 (none
+    // shares sub-partition 1 with the MMA issuer), 5 and 9 only fold, 13 and 15 idle.
+    static constexpr int EPI_WARPS = 8, CONV_WARPS = 4, EPI_BASE = 4;
+    static constexpr int THREADS = 512;
+    __device__ static int conv_slot(int warp) {
+        constexpr unsigned long long tab = 0x403000000002100ull;   // slot + 1 per warp, one nibble each
+        return (int)((tab >> (4 * warp)) & 15u) - 1;
+    }
     static constexpr int TSTAGES = 4, CSTAGES = 3, SSTAGES = 2, NBUF = 4;
     static constexpr int KG_MAX = 32;                         // K <= 1024
     static constexpr int A_RAW_BYTES = BM * 32;               // IQ4 codes: 64 indices per row
@@ -68,24 +75,6 @@ __device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c
     uint64_t r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
-}
-
-// Wait (bounded) for the completion of the `issued` most recent fills of a ring.
-__device__ __forceinline__ void drain_ring(uint64_t* full, long issued, int stages, uint32_t* err) {
-    const long pending = issued < stages ? issued : stages;
-    for (long i = 0; i < pending; ++i) {
-        const long idx = issued - 1 - i;
-        const int s = (int)(idx % stages);
-        const uint32_t par = (uint32_t)((idx / stages) & 1);
-        if (mbar_try_wait(&full[s], par)) continue;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&full[s], par)) {
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-                atomicCAS(err, 0u, DEV_TIMEOUT_DRAIN);
-                break;
-            }
-        }
-    }
 }
 
 // p.K = F (reduction), p.N = D (weight rows per expert), p.n_tiles = D / 128,
@@ -154,7 +143,7 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        {
             int s = 0, ss = 0;
             uint32_t ph = 0, sph = 0;
             long issued = 0, s_issued = 0;
@@ -165,23 +154,32 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
                 const int n0 = (t - entry * p.n_tiles) * C::BM;
                 const int4 g = p.tiles[entry];
                 // this tile's d_H values
-                if (!mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) break;
-                mbar_arrive_expect_tx(&full_s[ss], sbytes);
-                bulk_load(sstage + ss * C::SSTAGE_BYTES, p.dH32 + (long)entry * groups * C::BN, sbytes, &full_s[ss]);
+                const bool sfree = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                if (__any_sync(0xffffffffu, !sfree)) break;
+                if (elect_one_sync()) {
+                    mbar_arrive_expect_tx(&full_s[ss], sbytes);
+                    bulk_load(sstage + ss * C::SSTAGE_BYTES, p.dH32 + (long)entry * groups * C::BN, sbytes,
+                              &full_s[ss]);
+                }
+                __syncwarp();
                 ++s_issued;
                 if (++ss == C::SSTAGES) {
                     ss = 0;
                     sph ^= 1u;
                 }
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) {
+                    const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                    if (__any_sync(0xffffffffu, !got)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
-                    tma_load_2d(st, &tmA, &full_t[s], kb * 32, g.x * p.N + n0);
-                    tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
+                    if (elect_one_sync()) {
+                        uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                        mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                        tma_load_2d(st, &tmA, &full_t[s], kb * 32, g.x * p.N + n0);
+                        tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
+                    }
+                    __syncwarp();
                     ++issued;
                     if (++s == C::TSTAGES) {
                         s = 0;
@@ -189,38 +187,49 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
                     }
                 }
             }
-            drain_ring(full_t, issued, C::TSTAGES, p.err);
-            drain_ring(full_s, s_issued, C::SSTAGES, p.err);
+            if (lane == 0) {
+                drain_ring(full_t, issued, C::TSTAGES, p.err);
+                drain_ring(full_s, s_issued, C::SSTAGES, p.err);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {
             int cs = 0, buf = 0;
             uint32_t cph = 0, bph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
-                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                    const bool got = mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
+                    if (__any_sync(0xffffffffu, !got)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    // (no tcgen05 fence here: the operands are ordered by the mbarrier and the
+                    // writers' proxy fence; a tcgen05 fence per K block would drain the MMA pipe)
                     const uint32_t a_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
                     const uint32_t b_base = a_base + C::A_CONV_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
                         const bool first = (kk & 1) == 0, last = (kk & 1) == 1;
                         if (first) {
-                            if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                            const bool free = mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err,
+                                                        DEV_TIMEOUT_ACC_EMPTY);
+                            if (__any_sync(0xffffffffu, !free)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
                         }
-                        tc_mma_f16(tmem_base + (uint32_t)(buf * C::BN), smem_desc_sw128(a_base + kk * 32),
-                                   smem_desc_sw128(b_base + kk * 32), C::IDESC, first ? 0u : 1u);
+                        const uint64_t adesc = smem_desc_sw128(a_base + kk * 32);
+                        const uint64_t bdesc = smem_desc_sw128(b_base + kk * 32);
+                        const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::BN);
+                        if (elect_one_sync()) {
+                            tc_mma_f16(dtmem, adesc, bdesc, C::IDESC, first ? 0u : 1u);
+                            if (last) tc_commit(&acc_full[buf]);
+                        }
+                        __syncwarp();
                         if (last) {
-                            tc_commit(&acc_full[buf]);
                             if (++buf == C::NBUF) {
                                 buf = 0;
                                 bph ^= 1u;
@@ -228,23 +237,17 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
                         }
                     }
                     if (!ok) break;
-                    tc_commit(&empty_c[cs]);
+                    if (elect_one_sync()) tc_commit(&empty_c[cs]);
+                    __syncwarp();
                     if (++cs == C::CSTAGES) {
                         cs = 0;
                         cph ^= 1u;
                     }
                 }
             }
-            tc_commit(drain_bar);
-            if (!mbar_try_wait(drain_bar, 0)) {
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(drain_bar, 0)) {
-                    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-                        atomicCAS(p.err, 0u, DEV_TIMEOUT_DRAIN);
-                        break;
-                    }
-                }
-            }
+            if (elect_one_sync()) tc_commit(drain_bar);
+            __syncwarp();
+            if (lane == 0) drain_ring(drain_bar, 1, 1, p.err);
         }
     } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
@@ -342,9 +345,9 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
                 if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = hi;
             }
         }
-    } else if (warp >= C::CONV_BASE) {
+    } else if (C::conv_slot(warp) >= 0) {
         // ------------------------------------------------------------ converters
-        const int ct = threadIdx.x - C::CONV_BASE * 32;
+        const int ct = C::conv_slot(warp) * 32 + lane;
         int ts = 0, cs = 0;
         uint32_t tph = 0, cph = 0;
         bool ok = true;

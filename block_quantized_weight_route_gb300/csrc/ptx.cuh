@@ -68,12 +68,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for phase `parity` of `bar` to complete.  Returns false (after setting
 // *err to `code` if no error was recorded yet, and raising the CTA-wide abort
 // flag) when the wait times out or another role of the CTA has aborted.
+// The fast path polls try_wait (which itself suspends the thread for a short,
+// hardware-defined time) before touching the wall clock: reading %globaltimer
+// is slow, so it is consulted only every 256 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err, uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
@@ -212,6 +218,19 @@ __device__ __forceinline__ void cvt_e4m3x4_f16x2(uint32_t q, uint32_t (&h)[2]) {
         "cvt.rn.f16x2.e4m3x2 %1, s1;\n\t}"
         : "=r"(h[0]), "=r"(h[1])
         : "r"(q));
+}
+
+// True in exactly one lane of the (fully converged) warp.  Issue roles run their
+// loops on the whole warp so that descriptors and coordinates stay warp-uniform,
+// and let this one lane issue the TMA / tcgen05 instructions.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t"
+        "elect.sync _|P1, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P1;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

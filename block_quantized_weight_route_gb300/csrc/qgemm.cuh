@@ -1,11 +1,12 @@
 // Warp-specialised block-quantised GEMM for sm_103a (one CTA per SM, persistent).
 //
 //   warp 0        : TMA producer (activations tile + raw quantised weight tile)
-//   warp 1        : TMEM owner and MMA issuer (one thread issues tcgen05.mma)
-//   warps 2..3    : idle
+//   warp 1        : TMEM owner and MMA issuer (one elected thread issues tcgen05.mma)
 //   epilogue warps: read fp32 accumulators from TMEM, scale / fold / quantise, store
-//   converter warps: turn raw weight codes (and int8 activations) into the exact
-//                    16-bit operand tiles the tensor core reads, in shared memory
+//                   (12..15, or 4..11 for the two-warpgroup fold epilogue)
+//   converter warps: turn raw weight codes into the exact 16-bit operand tiles
+//                    the tensor core reads, in shared memory; none of them runs on
+//                    the MMA issuer's sub-partition (warp id % 4 == 1)
 //
 // Tile: 128 rows (tokens) x BN columns (weight rows), K step 64.  The MMA is
 // tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16), fp32 accumulation in
@@ -41,8 +42,11 @@ struct GemmCfg {
     static constexpr bool GROUPED = GROUPED_;
     static constexpr int BM = 128, BN = BN_, BK = 64, UMMA_K = 16;
     static constexpr int CONV_WARPS = CONV_WARPS_, EPI_WARPS = EPI_WARPS_;
-    static constexpr int EPI_BASE = 4, CONV_BASE = 4 + EPI_WARPS_;
-    static constexpr int THREADS = 32 * (4 + EPI_WARPS_ + CONV_WARPS_);
+    // 16 warps.  Warp w runs on SM sub-partition w % 4; the MMA issuer (warp 1)
+    // must not share its sub-partition with ALU-heavy converter warps, or its
+    // mbarrier waits are starved and the tensor pipe idles.
+    static constexpr int EPI_BASE = (EPI_WARPS_ == 4) ? 12 : 4;
+    static constexpr int THREADS = 512;
     static constexpr int TSTAGES = TSTAGES_, CSTAGES = CSTAGES_;
     // raw (TMA) stage: bf16 activation tile (read by the MMA in place) + weight codes
     static constexpr int A_RAW_BYTES = BM * BK * 2;
@@ -64,6 +68,15 @@ struct GemmCfg {
     static_assert(!FOLD || EPI_WARPS == 8, "fold epilogue splits columns over two warpgroups");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
     static_assert(BN == CONV_WARPS * 32, "one weight row per converter thread");
+    static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4), "warp layout");
+    // converter slot of a warp, -1 if it is not a converter:
+    //   4 epilogue warps (12..15): converters on warps 2,3,4,6,7,8,10,11
+    //   8 epilogue warps (4..11):  converters on warps 2,3,12,14
+    __device__ static int conv_slot(int warp) {
+        // slot + 1 per warp, one nibble each (0: not a converter)
+        constexpr unsigned long long tab = (EPI_WARPS == 4) ? 0x870654032100ull : 0x403000000002100ull;
+        return (int)((tab >> (4 * warp)) & 15u) - 1;
+    }
 };
 
 struct TileInfo {
@@ -236,6 +249,24 @@ __device__ __forceinline__ void convert_i8_row(uint32_t raw_tile, uint32_t dst_t
     }
 }
 
+// Wait (bounded) for the completion of the `issued` most recent fills of a ring.
+__device__ __forceinline__ void drain_ring(uint64_t* full, long issued, int stages, uint32_t* err) {
+    const long pending = issued < stages ? issued : stages;
+    for (long i = 0; i < pending; ++i) {
+        const long idx = issued - 1 - i;
+        const int s = (int)(idx % stages);
+        const uint32_t par = (uint32_t)((idx / stages) & 1);
+        if (mbar_try_wait(&full[s], par)) continue;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full[s], par)) {
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                atomicCAS(err, 0u, DEV_TIMEOUT_DRAIN);
+                break;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
@@ -300,7 +331,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        {
             int s = 0;
             uint32_t ph = 0;
             long issued = 0;
@@ -308,23 +339,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile<C>(p, t);
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) {
+                    const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                    if (__any_sync(0xffffffffu, !got)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
-                    tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
-                    uint8_t* bdst = st + C::A_RAW_BYTES;
-                    const int kx = kb * C::B_ROW_BYTES;
-                    if constexpr (C::EPI == Epi::SWIGLU_Q81) {
-                        // gate rows e*2F + n0 .. +BN/2, up rows e*2F + F + n0 .. +BN/2
-                        const int base = ti.expert * 2 * p.F + ti.n0;
-                        tma_load_2d(bdst, &tmB, &full_t[s], kx, base);
-                        tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, &tmB, &full_t[s], kx, base + p.F);
-                    } else {
-                        tma_load_2d(bdst, &tmB, &full_t[s], kx, ti.expert * p.N + ti.n0);
+                    if (elect_one_sync()) {
+                        uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                        mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                        tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
+                        uint8_t* bdst = st + C::A_RAW_BYTES;
+                        const int kx = kb * C::B_ROW_BYTES;
+                        if constexpr (C::EPI == Epi::SWIGLU_Q81) {
+                            // gate rows e*2F + n0 .. +BN/2, up rows e*2F + F + n0 .. +BN/2
+                            const int base = ti.expert * 2 * p.F + ti.n0;
+                            tma_load_2d(bdst, &tmB, &full_t[s], kx, base);
+                            tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, &tmB, &full_t[s], kx, base + p.F);
+                        } else {
+                            tma_load_2d(bdst, &tmB, &full_t[s], kx, ti.expert * p.N + ti.n0);
+                        }
                     }
+                    __syncwarp();
                     ++issued;
                     if (++s == C::TSTAGES) {
                         s = 0;
@@ -333,40 +368,24 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             // Teardown: every copy issued must have landed before the CTA exits.
-            const long pending = issued < C::TSTAGES ? issued : C::TSTAGES;
-            for (long i = 0; i < pending; ++i) {
-                // stage of the i-th most recent issue and the parity of its fill
-                long idx = issued - 1 - i;
-                const int ss = (int)(idx % C::TSTAGES);
-                const uint32_t pp = (uint32_t)((idx / C::TSTAGES) & 1);
-                if (!mbar_try_wait(&full_t[ss], pp)) {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(&full_t[ss], pp)) {
-                        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-                            atomicCAS(p.err, 0u, DEV_TIMEOUT_DRAIN);
-                            break;
-                        }
-                    }
-                }
-            }
+            if (lane == 0) drain_ring(full_t, issued, C::TSTAGES, p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {
             int ts = 0, cs = 0, buf = 0;
             uint32_t tph = 0, cph = 0, bph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
-                    if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL)) {
+                    bool got = mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL);
+                    got = got && mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
+                    if (__any_sync(0xffffffffu, !got)) {
                         ok = false;
                         break;
                     }
-                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                    // (no tcgen05 fence here: the operands are ordered by the mbarrier and the
+                    // writers' proxy fence; a tcgen05 fence per K block would drain the MMA pipe)
                     const uint32_t a_base = smem_u32(tstage + ts * C::TSTAGE_BYTES);
                     const uint32_t b_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
 #pragma unroll
@@ -376,16 +395,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         const bool first = (kg % gk) == 0;
                         const bool last = ((kg + C::UMMA_K) % gk) == 0;
                         if (first) {
-                            if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                            const bool free = mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err,
+                                                        DEV_TIMEOUT_ACC_EMPTY);
+                            if (__any_sync(0xffffffffu, !free)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
                         }
-                        tc_mma_f16(tmem_base + (uint32_t)(buf * C::BN), smem_desc_sw128(a_base + kk * 32),
-                                   smem_desc_sw128(b_base + kk * 32), C::IDESC, first ? 0u : 1u);
+                        const uint64_t adesc = smem_desc_sw128(a_base + kk * 32);
+                        const uint64_t bdesc = smem_desc_sw128(b_base + kk * 32);
+                        const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::BN);
+                        if (elect_one_sync()) {
+                            tc_mma_f16(dtmem, adesc, bdesc, C::IDESC, first ? 0u : 1u);
+                            if (last) tc_commit(&acc_full[buf]);
+                        }
+                        __syncwarp();
                         if (last) {
-                            tc_commit(&acc_full[buf]);
                             if (++buf == C::NBUF) {
                                 buf = 0;
                                 bph ^= 1u;
@@ -393,8 +419,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         }
                     }
                     if (!ok) break;
-                    tc_commit(&empty_c[cs]);
-                    tc_commit(&empty_t[ts]);
+                    if (elect_one_sync()) {
+                        tc_commit(&empty_c[cs]);
+                        tc_commit(&empty_t[ts]);
+                    }
+                    __syncwarp();
                     if (++ts == C::TSTAGES) {
                         ts = 0;
                         tph ^= 1u;
@@ -406,16 +435,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             // Teardown: wait until every MMA issued has completed before TMEM is freed.
-            tc_commit(drain_bar);
-            if (!mbar_try_wait(drain_bar, 0)) {
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(drain_bar, 0)) {
-                    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-                        atomicCAS(p.err, 0u, DEV_TIMEOUT_DRAIN);
-                        break;
-                    }
-                }
-            }
+            if (elect_one_sync()) tc_commit(drain_bar);
+            __syncwarp();
+            if (lane == 0) drain_ring(drain_bar, 1, 1, p.err);
         }
     } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
@@ -576,9 +598,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
         }
-    } else if (warp >= C::CONV_BASE) {
+    } else if (C::conv_slot(warp) >= 0) {
         // ------------------------------------------------------------ converters
-        const int ct = threadIdx.x - C::CONV_BASE * 32;   // this thread's weight row in every tile
+        const int ct = C::conv_slot(warp) * 32 + lane;   // this thread's weight row in every tile
         int ts = 0, cs = 0;
         uint32_t tph = 0, cph = 0;
         bool ok = true;
