@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.moe_expert_stage_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.moe_expert_stage_workspace_layout.restype = i32
         L.moe_expert_stage_workspace_layout.argtypes = [i32, i32, i32, i32, i32, P]
+        L.moe_route_permute_noalloc.restype = i32
+        L.moe_route_permute_noalloc.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, P]
         L.qmm_profile_enable.restype = i32
         L.qmm_profile_enable.argtypes = [i32]
         L.qmm_profile_read.restype = i32

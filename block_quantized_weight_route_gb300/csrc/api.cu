@@ -159,6 +159,9 @@ void stage_layout(int T, int D, int F, int E, int k, size_t* off) {
 }
 
 }  // namespace
+
+void set_last_error(const char* msg) { t_last_error = msg; }
+
 }  // namespace qmm
 
 using namespace qmm;

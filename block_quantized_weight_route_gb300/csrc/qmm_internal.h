@@ -69,6 +69,6 @@ cudaError_t launch_gather_rows(const uint16_t* X, const int32_t* src, int rows, 
 cudaError_t launch_combine(const float* Yslot, const int32_t* row, const float* w, int T, int k, int D, float* Y,
                            cudaStream_t s);
 
-// Device error words of the translation units, read and cleared by qmm_check_status.
-uint32_t* gemm_error_word();   // device address
+// Set the calling thread's message returned by qmm_last_error().
+void set_last_error(const char* msg);
 }  // namespace qmm

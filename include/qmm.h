@@ -141,6 +141,32 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t *X, const float *logits, int T
 qmm_status moe_expert_stage_workspace_layout(int T, int D, int F, int E, int k, size_t *offsets_out);
 
 /*
+ * moe_route_permute_noalloc -- moe_route_permute for callers that cannot
+ * allocate device memory (no counterpart on the pages: a library convenience).
+ * Same inputs, outputs, results and shape rules as moe_route_permute, without
+ * the ws / ws_bytes arguments.  Such callers are, for example, code running in
+ * a CUDA stream capture under the global capture mode (where cudaMalloc is not
+ * allowed), plug-ins of another runtime that owns all device memory, and
+ * latency-critical loops where cudaMalloc / cudaFree would synchronise.
+ * The per-chunk counting scratch lives instead in a fixed device array inside
+ * this library: QMM_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that loads the
+ * library, kept until the process exits.  The limit: ceil(T / 256) * E counters
+ * of 4 bytes must fit in it (with E = 512, T <= 131072; with E = 256,
+ * T <= 262144; with E = 128, T <= 524288); larger shapes return
+ * QMM_ERR_UNSUPPORTED_SHAPE with the sizes in qmm_last_error().
+ * The first call on a device looks up the array's device address (a host-side
+ * set-up step, no allocation); make that first call before any stream capture.
+ * The function itself calls no cudaMalloc, cudaFree or allocating routine.
+ * Every call shares the one array: calls whose work overlaps on the GPU (on
+ * different streams, or in different host threads) race on it, so serialise
+ * them.  Every counter is written before it is read, so nothing needs clearing.
+ */
+#define QMM_NOALLOC_SCRATCH_BYTES (1u << 20)
+qmm_status moe_route_permute_noalloc(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                                     int32_t *counts, int32_t *offsets, int32_t *src, int32_t *row,
+                                     cudaStream_t stream);
+
+/*
  * Phase timing of the expert stage (for benchmarks).  With profiling on, each
  * moe_expert_stage_w4_iq4 call records CUDA events on its stream between its
  * phases: 0 routing (top-k, counts, scan, permutation), 1 row gather of X,
