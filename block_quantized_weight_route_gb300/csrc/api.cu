@@ -198,8 +198,10 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     DeviceState* d = nullptr;
     qmm_status st = device_state(&d);
     if (st != QMM_OK) return st;
+    const int n_tiles = (N + 255) / 256;
+    const int cn = cluster_for(n_tiles);
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 128,
+    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 128 / cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
     if ((st = make_tmap(&tb, Wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, 32, 256,
@@ -210,7 +212,7 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     p.N = N;
     p.K = K;
     p.m_tiles = (M + 127) / 128;
-    p.n_tiles = (N + 255) / 256;
+    p.n_tiles = n_tiles;
     p.n_step = 256;
     p.w_scale = Ws;
     p.scale2_dense = scale2;
@@ -218,8 +220,7 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     p.ydt = (ydt == QMM_BF16) ? 1 : 0;
     p.ldy = N;
     p.err = d->err;
-    const int tiles = p.m_tiles * p.n_tiles;
-    cudaError_t e = launch_w4a16_dense(ta, tb, p, tiles < d->sms ? tiles : d->sms, stream);
+    cudaError_t e = launch_w4a16_dense(ta, tb, p, cn, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_w4a16 launch");
     return QMM_OK;
 }
@@ -235,8 +236,9 @@ qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t*
     DeviceState* d = nullptr;
     qmm_status st = device_state(&d);
     if (st != QMM_OK) return st;
+    const int cn = cluster_for(N / 128);
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 128,
+    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 128 / cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
     if ((st = make_tmap(&tb, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) != QMM_OK)
@@ -253,8 +255,7 @@ qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t*
     p.ydt = 1;
     p.ldy = N;
     p.err = d->err;
-    const int tiles = p.m_tiles * p.n_tiles;
-    cudaError_t e = launch_fp8_blk128(ta, tb, p, tiles < d->sms ? tiles : d->sms, stream);
+    cudaError_t e = launch_fp8_blk128(ta, tb, p, cn, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_fp8_blk128 launch");
     return QMM_OK;
 }
@@ -367,8 +368,9 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     float* Yslot = static_cast<float*>(at(14));
 
     // gate/up + SwiGLU + q8_1
+    const int gu_cn = cluster_for(F / 128);
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, 128,
+    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, 128 / gu_cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
     if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, 128,
@@ -389,7 +391,7 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     g.Hs = Hs;
     g.Hd32 = Hd32;
     g.err = d->err;
-    e = launch_w4_gate_up_swiglu(ta, tb, g, d->sms, stream);
+    e = launch_w4_gate_up_swiglu(ta, tb, g, gu_cn, stream);
     if (e != cudaSuccess) return cuda_fail(e, "expert stage: gate/up launch");
     if ((e = mark(d, 3, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 

@@ -5,18 +5,17 @@
 
 namespace qmm {
 
-using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 4, 8, 4, 4, false>;
+template <int CN>
+using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 4, 8, 4, 4, false, CN>;
 
-int smem_fp8_blk128() { return CfgFp8::SMEM_BYTES; }
-
-cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                               cudaStream_t s) {
-    static_assert(CfgFp8::SMEM_BYTES <= 232448, "shared memory");
-    cudaError_t e =
-        cudaFuncSetAttribute(qgemm_kernel<CfgFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgFp8::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    qgemm_kernel<CfgFp8><<<grid, CfgFp8::THREADS, CfgFp8::SMEM_BYTES, s>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    const int items = p.m_tiles * (p.n_tiles / cn);
+    switch (cn) {
+        case 4: return launch_qgemm<CfgFp8<4>>(tmA, tmB, p, items, s);
+        case 2: return launch_qgemm<CfgFp8<2>>(tmA, tmB, p, items, s);
+        default: return launch_qgemm<CfgFp8<1>>(tmA, tmB, p, items, s);
+    }
 }
 
 }  // namespace qmm

@@ -6,31 +6,31 @@
 namespace qmm {
 
 // Dense: 128 x 256 tiles, 8 converter warps (one weight row per thread), 4 epilogue warps.
-using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 256, 8, 4, 4, 3, false>;
+template <int CN>
+using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 256, 8, 4, 4, 3, false, CN>;
 // Gate/up: 128 token rows x (128 gate + 128 up) weight rows per tile.
-using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 256, 8, 4, 4, 3, true>;
+template <int CN>
+using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 256, 8, 4, 4, 3, true, CN>;
 
-int smem_w4a16_dense() { return CfgW4Dense::SMEM_BYTES; }
-int smem_w4_gate_up_swiglu() { return CfgW4GateUp::SMEM_BYTES; }
+int cluster_for(int n_tiles) { return (n_tiles % 4 == 0) ? 4 : ((n_tiles % 2 == 0) ? 2 : 1); }
 
-template <class C>
-static cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
-                          cudaStream_t s) {
-    static_assert(C::SMEM_BYTES <= 232448, "shared memory");
-    cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    qgemm_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(tmA, tmB, p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                cudaStream_t s) {
-    return launch<CfgW4Dense>(tmA, tmB, p, grid, s);
+    const int items = p.m_tiles * (p.n_tiles / cn);
+    switch (cn) {
+        case 4: return launch_qgemm<CfgW4Dense<4>>(tmA, tmB, p, items, s);
+        case 2: return launch_qgemm<CfgW4Dense<2>>(tmA, tmB, p, items, s);
+        default: return launch_qgemm<CfgW4Dense<1>>(tmA, tmB, p, items, s);
+    }
 }
 
-cudaError_t launch_w4_gate_up_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+cudaError_t launch_w4_gate_up_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                      cudaStream_t s) {
-    return launch<CfgW4GateUp>(tmA, tmB, p, grid, s);
+    switch (cn) {
+        case 4: return launch_qgemm<CfgW4GateUp<4>>(tmA, tmB, p, 0, s);
+        case 2: return launch_qgemm<CfgW4GateUp<2>>(tmA, tmB, p, 0, s);
+        default: return launch_qgemm<CfgW4GateUp<1>>(tmA, tmB, p, 0, s);
+    }
 }
 
 }  // namespace qmm

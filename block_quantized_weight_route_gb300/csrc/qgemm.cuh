@@ -35,9 +35,15 @@ namespace qmm {
 enum class BMode { W4, FP8 };
 enum class Epi { STORE, SWIGLU_Q81, FOLD_FP8 };
 
-template <BMode B_, Epi E_, int BN_, int CONV_WARPS_, int EPI_WARPS_, int TSTAGES_, int CSTAGES_, bool GROUPED_>
+template <BMode B_, Epi E_, int BN_, int CONV_WARPS_, int EPI_WARPS_, int TSTAGES_, int CSTAGES_, bool GROUPED_,
+          int CLUSTER_N_ = 1>
 struct GemmCfg {
     static constexpr BMode B = B_;
+    // CTAs of a cluster work on the same activation rows and consecutive column
+    // tiles; each loads 1/CLUSTER_N of the activation tile and multicasts it to
+    // all, so the activations cross L2 once per cluster instead of once per CTA.
+    static constexpr int CLUSTER_N = CLUSTER_N_;
+    static constexpr int A_SLICE_ROWS = 128 / CLUSTER_N_;
     static constexpr Epi EPI = E_;
     static constexpr bool GROUPED = GROUPED_;
     static constexpr int BM = 128, BN = BN_, BK = 64, UMMA_K = 16;
@@ -58,6 +64,7 @@ struct GemmCfg {
     // accumulation groups: the whole K, or one per 128-K block (FP8 fold)
     static constexpr bool FOLD = (E_ == Epi::FOLD_FP8);
     static constexpr int GROUP_K = FOLD ? 128 : 0;   // 0: whole K
+    static_assert(GROUP_K == 0 || GROUP_K == 2 * BK, "fold groups span two K blocks");
     static constexpr int NBUF = 512 / BN;
     static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, true);
     static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * NBUF + 1;
@@ -68,6 +75,7 @@ struct GemmCfg {
     static_assert(!FOLD || EPI_WARPS == 8, "fold epilogue splits columns over two warpgroups");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
     static_assert(BN == CONV_WARPS * 32, "one weight row per converter thread");
+    static_assert(CLUSTER_N == 1 || CLUSTER_N == 2 || CLUSTER_N == 4, "cluster size");
     static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4), "warp layout");
     // converter slot of a warp, -1 if it is not a converter:
     //   4 epilogue warps (12..15): converters on warps 2,3,4,6,7,8,10,11
@@ -83,11 +91,15 @@ struct TileInfo {
     int expert, row0, rows, n0, entry;
 };
 
+// Work item g of a cluster: one block of activation rows and CLUSTER_N
+// consecutive column tiles; CTA `crank` of the cluster takes column tile
+// ng * CLUSTER_N + crank.  (p.n_tiles is a multiple of CLUSTER_N.)
 template <class C>
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int g, int crank) {
     TileInfo ti;
+    const int n_groups = p.n_tiles / C::CLUSTER_N;
     if constexpr (C::GROUPED) {
-        const int entry = t / p.n_tiles, nt = t - entry * p.n_tiles;
+        const int entry = g / n_groups, nt = (g - entry * n_groups) * C::CLUSTER_N + crank;
         const int4 g = p.tiles[entry];
         ti.expert = g.x;
         ti.row0 = g.y;
@@ -95,7 +107,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
         ti.n0 = nt * p.n_step;
         ti.entry = entry;
     } else {
-        const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+        const int mt = g % p.m_tiles, nt = (g / p.m_tiles) * C::CLUSTER_N + crank;
         ti.expert = 0;
         ti.row0 = mt * C::BM;
         ti.rows = min(C::BM, p.M - ti.row0);
@@ -296,7 +308,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::TSTAGES; ++i) {
             mbar_init(&full_t[i], 1);
-            mbar_init(&empty_t[i], 1);   // released by the MMA's commit (it read the activation tile)
+            // released by the MMA commit of every CTA of the cluster (each read the multicast tile)
+            mbar_init(&empty_t[i], C::CLUSTER_N);
         }
         for (int i = 0; i < C::CSTAGES; ++i) {
             mbar_init(&full_c[i], C::CONV_WARPS);
@@ -317,16 +330,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
+    if constexpr (C::CLUSTER_N > 1) cluster_sync();   // peers' barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const int kblocks = p.K / C::BK;
-    int num_tiles;
+    const int crank = (C::CLUSTER_N > 1) ? (int)cluster_ctarank() : 0;
+    const int cid = (C::CLUSTER_N > 1) ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int ncl = (C::CLUSTER_N > 1) ? (int)cluster_count_x() : (int)gridDim.x;
+    int num_tiles;   // work items (one per cluster step)
     if constexpr (C::GROUPED) {
         const int entries = min(*p.num_entries, p.max_entries);
-        num_tiles = entries * p.n_tiles;
+        num_tiles = entries * (p.n_tiles / C::CLUSTER_N);
     } else {
-        num_tiles = p.m_tiles * p.n_tiles;
+        num_tiles = p.m_tiles * (p.n_tiles / C::CLUSTER_N);
     }
 
     if (warp == 0) {
@@ -336,8 +353,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t ph = 0;
             long issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<C>(p, t);
+            for (int t = cid; t < num_tiles && ok; t += ncl) {
+                const TileInfo ti = decode_tile<C>(p, t, crank);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
                     if (__any_sync(0xffffffffu, !got)) {
@@ -347,7 +364,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (elect_one_sync()) {
                         uint8_t* st = tstage + s * C::TSTAGE_BYTES;
                         mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
-                        tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
+                        if constexpr (C::CLUSTER_N > 1) {
+                            // this CTA's slice of the activation tile, written into every CTA of the cluster
+                            tma_load_2d_multicast(st + crank * C::A_SLICE_ROWS * 128, &tmA, &full_t[s], kb * C::BK,
+                                                  ti.row0 + crank * C::A_SLICE_ROWS,
+                                                  (uint16_t)((1u << C::CLUSTER_N) - 1));
+                        } else {
+                            tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
+                        }
                         uint8_t* bdst = st + C::A_RAW_BYTES;
                         const int kx = kb * C::B_ROW_BYTES;
                         if constexpr (C::EPI == Epi::SWIGLU_Q81) {
@@ -376,7 +400,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             int ts = 0, cs = 0, buf = 0;
             uint32_t tph = 0, cph = 0, bph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = cid; t < num_tiles && ok; t += ncl) {
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
                     bool got = mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL);
                     got = got && mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
@@ -390,10 +414,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const uint32_t b_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-                        const int kg = kb * C::BK + kk * C::UMMA_K;
-                        const int gk = C::GROUP_K ? C::GROUP_K : p.K;
-                        const bool first = (kg % gk) == 0;
-                        const bool last = ((kg + C::UMMA_K) % gk) == 0;
+                        // first / last MMA of an accumulation group (the whole K, or one
+                        // 128-K block = two K blocks for the FP8 fold); no divisions here:
+                        // this loop sits between consecutive MMA issues
+                        bool first, last;
+                        if constexpr (C::GROUP_K == 128) {
+                            first = (kk == 0) && ((kb & 1) == 0);
+                            last = (kk == C::BK / C::UMMA_K - 1) && ((kb & 1) == 1);
+                        } else {
+                            first = (kk == 0) && (kb == 0);
+                            last = (kk == C::BK / C::UMMA_K - 1) && (kb == kblocks - 1);
+                        }
                         if (first) {
                             const bool free = mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err,
                                                         DEV_TIMEOUT_ACC_EMPTY);
@@ -421,7 +452,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (!ok) break;
                     if (elect_one_sync()) {
                         tc_commit(&empty_c[cs]);
-                        tc_commit(&empty_t[ts]);
+                        if constexpr (C::CLUSTER_N > 1)
+                            tc_commit_multicast(&empty_t[ts], (uint16_t)((1u << C::CLUSTER_N) - 1));
+                        else
+                            tc_commit(&empty_t[ts]);
                     }
                     __syncwarp();
                     if (++ts == C::TSTAGES) {
@@ -448,8 +482,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int buf = 0;
         uint32_t bph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const TileInfo ti = decode_tile<C>(p, t);
+        for (int t = cid; t < num_tiles && ok; t += ncl) {
+            const TileInfo ti = decode_tile<C>(p, t, crank);
             const bool valid = row < ti.rows;
             const long grow = (long)ti.row0 + row;
             if constexpr (!C::FOLD) {
@@ -620,17 +654,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         };
         auto load_chunk = [&](int t, int ch) -> uint4 {
             if (t >= num_tiles) return make_uint4(0, 0, 0, 0);
-            const TileInfo tt = decode_tile<C>(p, t);
+            const TileInfo tt = decode_tile<C>(p, t, crank);
             bool in_range;
             const long wrow = scale_row(tt, in_range);
             return in_range ? ldg_nc_v4(p.w_scale + wrow * (p.K / 16) + ch * 16) : make_uint4(0, 0, 0, 0);
         };
         uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = make_uint4(0, 0, 0, 0);
         if constexpr (C::B == BMode::W4) {
-            if (vec_scales) sc_next = load_chunk(blockIdx.x, 0);
+            if (vec_scales) sc_next = load_chunk(cid, 0);
         }
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const TileInfo ti = decode_tile<C>(p, t);
+        for (int t = cid; t < num_tiles && ok; t += ncl) {
+            const TileInfo ti = decode_tile<C>(p, t, crank);
             for (int kb = 0; kb < kblocks; ++kb) {
                 uint32_t sbytes = 0;
                 if constexpr (C::B == BMode::W4) {
@@ -638,7 +672,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if ((kb & 3) == 0) {
                             sc_cur = sc_next;
                             const int ch = (kb >> 2) + 1;
-                            sc_next = (ch < kchunks) ? load_chunk(t, ch) : load_chunk(t + gridDim.x, 0);
+                            sc_next = (ch < kchunks) ? load_chunk(t, ch) : load_chunk(t + ncl, 0);
                         }
                         const int j = kb & 3;
                         sbytes = j == 0 ? sc_cur.x : (j == 1 ? sc_cur.y : (j == 2 ? sc_cur.z : sc_cur.w));
@@ -677,10 +711,60 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
 
     __syncthreads();
+    // No CTA leaves while a peer may still multicast into its shared memory or
+    // signal its barriers.
+    if constexpr (C::CLUSTER_N > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launch of a GemmCfg instantiation: cluster launch when CLUSTER_N > 1,
+// persistent grid of (max co-resident clusters, capped by the work) x CLUSTER_N.
+template <class C>
+cudaError_t launch_qgemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_items,
+                         cudaStream_t s) {
+    static_assert(C::SMEM_BYTES <= 232448, "shared memory");
+    cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (C::CLUSTER_N > 1) {
+        e = cudaFuncSetAttribute(qgemm_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        if (e != cudaSuccess) return e;
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static int max_clusters[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C::CLUSTER_N;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters[dev] == 0) {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int n = sms / C::CLUSTER_N;
+        if (C::CLUSTER_N > 1) {
+            cfg.gridDim = dim3(C::CLUSTER_N * n, 1, 1);
+            int q = 0;
+            if (cudaOccupancyMaxActiveClusters(&q, qgemm_kernel<C>, &cfg) == cudaSuccess && q > 0) n = q;
+        }
+        max_clusters[dev] = n;
+    }
+    int clusters = max_clusters[dev];
+    if (max_items > 0 && max_items < clusters) clusters = max_items;
+    cfg.gridDim = dim3(C::CLUSTER_N * clusters, 1, 1);
+    e = cudaLaunchKernelEx(&cfg, qgemm_kernel<C>, tmA, tmB, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace qmm

@@ -34,20 +34,19 @@ struct GemmParams {
 };
 
 // Launchers (return a cudaError_t from the launch).  Each takes two encoded
-// tensor maps: tmA for the activation operand, tmB for the raw weight codes.
-cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+// tensor maps: tmA for the activation operand (box rows 128 / cn: each CTA of a
+// cluster of cn loads that slice and multicasts it), tmB for the raw weight
+// codes; cn must divide p.n_tiles (cluster_for picks it).
+int cluster_for(int n_tiles);
+cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                cudaStream_t s);
-cudaError_t launch_w4_gate_up_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+cudaError_t launch_w4_gate_up_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                      cudaStream_t s);
-cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                               cudaStream_t s);
 cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                             cudaStream_t s);
 
-// Dynamic shared memory each GEMM launcher needs (checked against the device limit).
-int smem_w4a16_dense();
-int smem_w4_gate_up_swiglu();
-int smem_fp8_blk128();
 int smem_iq4_down();
 
 // Routing and data-movement kernels (route.cu).
