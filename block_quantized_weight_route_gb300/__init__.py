@@ -14,9 +14,9 @@ import torch
 
 from .build import LIB, build_library  # noqa: F401
 
-QMM_WS_FIELDS = 16
+QMM_WS_FIELDS = 18
 WS_FIELD_NAMES = ("ids", "w", "counts", "offsets", "src", "row", "chunk_counts", "tiles", "tile_count",
-                  "X_perm", "Hq", "Hd", "Hs", "Hd32", "Yslot", "total")
+                  "tiles256", "tile_count256", "X_perm", "Hq", "Hd", "Hs", "Hd32", "Yslot", "total")
 
 _STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE",
            3: "QMM_ERR_UNSUPPORTED_DEVICE", 4: "QMM_ERR_WORKSPACE", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT"}

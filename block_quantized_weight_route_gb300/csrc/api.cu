@@ -129,6 +129,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int route_chunks(int T) { return (T + kRouteChunk - 1) / kRouteChunk; }
 int max_tile_entries(int T, int E, int k) { return (int)(((long)T * k + 127) / 128) + E; }
+int max_tile_entries256(int T, int E, int k) { return (int)(((long)T * k + 255) / 256) + E; }
 
 // Workspace regions of the expert stage, in the order of the QMM_WS_FIELDS list.
 void stage_layout(int T, int D, int F, int E, int k, size_t* off) {
@@ -141,7 +142,9 @@ void stage_layout(int T, int D, int F, int E, int k, size_t* off) {
         P * 4,                                      // src
         P * 4,                                      // row
         (size_t)route_chunks(T) * E * 4,            // chunk counts
-        (size_t)max_tile_entries(T, E, k) * 16,     // tile list
+        (size_t)max_tile_entries(T, E, k) * 16,     // tile list, 128-row entries
+        16,                                         // tile count
+        (size_t)max_tile_entries256(T, E, k) * 16,  // tile list, 256-row entries
         16,                                         // tile count
         P * D * 2,                                  // X_perm
         P * F,                                      // Hq
@@ -198,22 +201,23 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     DeviceState* d = nullptr;
     qmm_status st = device_state(&d);
     if (st != QMM_OK) return st;
-    const int n_tiles = (N + 255) / 256;
+    // 256 x 128 tiles; clusters of cn CTAs share the activation rows
+    const int n_tiles = (N + 127) / 128;
     const int cn = cluster_for(n_tiles);
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 128 / cn,
+    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 256 / cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
-    if ((st = make_tmap(&tb, Wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, 32, 256,
+    if ((st = make_tmap(&tb, Wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, 32, 128,
                         CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
         return st;
     GemmParams p{};
     p.M = M;
     p.N = N;
     p.K = K;
-    p.m_tiles = (M + 127) / 128;
+    p.m_tiles = (M + 255) / 256;
     p.n_tiles = n_tiles;
-    p.n_step = 256;
+    p.n_step = 128;
     p.w_scale = Ws;
     p.scale2_dense = scale2;
     p.Y = Y;
@@ -349,41 +353,43 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
 
     cudaError_t e;
     if ((e = mark(d, 0, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
+    const int max_entries2 = max_tile_entries256(T, E, k);
     RouteBufs rb{static_cast<int32_t*>(at(0)), static_cast<float*>(at(1)), static_cast<int32_t*>(at(2)),
                  static_cast<int32_t*>(at(3)), static_cast<int32_t*>(at(4)), static_cast<int32_t*>(at(5)),
                  static_cast<int32_t*>(at(6)), static_cast<int4*>(at(7)), static_cast<int32_t*>(at(8)),
-                 max_entries};
+                 max_entries, static_cast<int4*>(at(9)), static_cast<int32_t*>(at(10)), max_entries2};
     e = launch_route(logits, T, E, k, rb, stream);
     if (e != cudaSuccess) return cuda_fail(e, "expert stage: routing");
     if ((e = mark(d, 1, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
-    uint16_t* Xp = static_cast<uint16_t*>(at(9));
+    uint16_t* Xp = static_cast<uint16_t*>(at(11));
     e = launch_gather_rows(X, rb.src, P, D, Xp, stream);
     if (e != cudaSuccess) return cuda_fail(e, "expert stage: gather");
     if ((e = mark(d, 2, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
-    int8_t* Hq = static_cast<int8_t*>(at(10));
-    __half* Hd = static_cast<__half*>(at(11));
-    __half* Hs = static_cast<__half*>(at(12));
-    float* Hd32 = static_cast<float*>(at(13));
-    float* Yslot = static_cast<float*>(at(14));
+    int8_t* Hq = static_cast<int8_t*>(at(12));
+    __half* Hd = static_cast<__half*>(at(13));
+    __half* Hs = static_cast<__half*>(at(14));
+    float* Hd32 = static_cast<float*>(at(15));
+    float* Yslot = static_cast<float*>(at(16));
 
     // gate/up + SwiGLU + q8_1
-    const int gu_cn = cluster_for(F / 128);
+    // 256 token rows x (64 gate + 64 up weight rows) per tile; clusters share the rows
+    const int gu_cn = cluster_for(F / 64);
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, 128 / gu_cn,
+    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, 256 / gu_cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
-    if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, 128,
+    if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, 64,
                         CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
         return st;
     GemmParams g{};
     g.K = D;
     g.F = F;
-    g.n_tiles = F / 128;
-    g.n_step = 128;
-    g.tiles = rb.tiles;
-    g.num_entries = rb.num_entries;
-    g.max_entries = max_entries;
+    g.n_tiles = F / 64;
+    g.n_step = 64;
+    g.tiles = rb.tiles2;
+    g.num_entries = rb.num_entries2;
+    g.max_entries = max_entries2;
     g.w_scale = Wgu_s;
     g.scale2 = gu_scale2;
     g.Hq = Hq;

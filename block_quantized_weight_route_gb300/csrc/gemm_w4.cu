@@ -5,12 +5,13 @@
 
 namespace qmm {
 
-// Dense: 128 x 256 tiles, 8 converter warps (one weight row per thread), 4 epilogue warps.
+// Dense: 256 x 128 tiles (two 128-row sub-tiles share each converted weight
+// tile), 8 converter warps (two per weight row), 4 epilogue warps.
 template <int CN>
-using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 256, 8, 4, 4, 3, false, CN>;
-// Gate/up: 128 token rows x (128 gate + 128 up) weight rows per tile.
+using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 128, 8, 4, 4, 3, false, CN, 2>;
+// Gate/up: 256 token rows x (64 gate + 64 up) weight rows per tile.
 template <int CN>
-using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 256, 8, 4, 4, 3, true, CN>;
+using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, 4, 3, true, CN, 2>;
 
 int cluster_for(int n_tiles) { return (n_tiles % 4 == 0) ? 4 : ((n_tiles % 2 == 0) ? 2 : 1); }
 

@@ -36,17 +36,21 @@ enum class BMode { W4, FP8 };
 enum class Epi { STORE, SWIGLU_Q81, FOLD_FP8 };
 
 template <BMode B_, Epi E_, int BN_, int CONV_WARPS_, int EPI_WARPS_, int TSTAGES_, int CSTAGES_, bool GROUPED_,
-          int CLUSTER_N_ = 1>
+          int CLUSTER_N_ = 1, int MSUB_ = 1>
 struct GemmCfg {
     static constexpr BMode B = B_;
+    // MSUB row blocks of 128 share every converted weight tile: each K step
+    // issues MSUB MMAs (one per 128-row sub-tile) against the same B operand,
+    // which divides the conversion work per FLOP by MSUB.
+    static constexpr int MSUB = MSUB_;
     // CTAs of a cluster work on the same activation rows and consecutive column
     // tiles; each loads 1/CLUSTER_N of the activation tile and multicasts it to
     // all, so the activations cross L2 once per cluster instead of once per CTA.
     static constexpr int CLUSTER_N = CLUSTER_N_;
-    static constexpr int A_SLICE_ROWS = 128 / CLUSTER_N_;
+    static constexpr int A_SLICE_ROWS = 128 * MSUB_ / CLUSTER_N_;
     static constexpr Epi EPI = E_;
     static constexpr bool GROUPED = GROUPED_;
-    static constexpr int BM = 128, BN = BN_, BK = 64, UMMA_K = 16;
+    static constexpr int BM = 128 * MSUB_, BN = BN_, BK = 64, UMMA_K = 16;
     static constexpr int CONV_WARPS = CONV_WARPS_, EPI_WARPS = EPI_WARPS_;
     // 16 warps.  Warp w runs on SM sub-partition w % 4; the MMA issuer (warp 1)
     // must not share its sub-partition with ALU-heavy converter warps, or its
@@ -65,8 +69,9 @@ struct GemmCfg {
     static constexpr bool FOLD = (E_ == Epi::FOLD_FP8);
     static constexpr int GROUP_K = FOLD ? 128 : 0;   // 0: whole K
     static_assert(GROUP_K == 0 || GROUP_K == 2 * BK, "fold groups span two K blocks");
-    static constexpr int NBUF = 512 / BN;
-    static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, true);
+    static constexpr int NBUF = 512 / (BN * MSUB_);
+    static constexpr uint32_t IDESC = idesc_kind_f16(128, BN, true);
+    static constexpr int TPR = CONV_WARPS_ * 32 / BN_;   // converter threads per weight row
     static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * NBUF + 1;
     static constexpr int SMEM_BYTES =
         1024 /*align slack*/ + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES + BAR_COUNT * 8 + 64;
@@ -74,7 +79,11 @@ struct GemmCfg {
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
     static_assert(!FOLD || EPI_WARPS == 8, "fold epilogue splits columns over two warpgroups");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
-    static_assert(BN == CONV_WARPS * 32, "one weight row per converter thread");
+    static_assert(TPR == 1 || (TPR == 2 && B_ == BMode::W4), "one or (W4) two converter threads per weight row");
+    static_assert(CONV_WARPS * 32 == TPR * BN, "converters cover the weight rows");
+    static_assert(MSUB == 1 || MSUB == 2, "row sub-tiles");
+    static_assert(MSUB == 1 || !FOLD, "the fold epilogue uses one row sub-tile");
+    static_assert(NBUF >= 1, "TMEM columns");
     static_assert(CLUSTER_N == 1 || CLUSTER_N == 2 || CLUSTER_N == 4, "cluster size");
     static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4), "warp layout");
     // converter slot of a warp, -1 if it is not a converter:
@@ -100,12 +109,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int g, int 
     const int n_groups = p.n_tiles / C::CLUSTER_N;
     if constexpr (C::GROUPED) {
         const int entry = g / n_groups, nt = (g - entry * n_groups) * C::CLUSTER_N + crank;
-        const int4 g = p.tiles[entry];
-        ti.expert = g.x;
-        ti.row0 = g.y;
-        ti.rows = g.z;
+        const int4 e4 = p.tiles[entry];
+        ti.expert = e4.x;
+        ti.row0 = e4.y;
+        ti.rows = e4.z;
         ti.n0 = nt * p.n_step;
-        ti.entry = entry;
+        // index of the first 128-row routing entry the tile covers (two per tile when MSUB == 2)
+        ti.entry = (C::MSUB == 2) ? e4.w : entry;
     } else {
         const int mt = g % p.m_tiles, nt = (g / p.m_tiles) * C::CLUSTER_N + crank;
         ti.expert = 0;
@@ -195,6 +205,23 @@ __device__ __forceinline__ void convert_w4_row(uint32_t raw_tile, uint32_t dst_t
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[i]), sc[w >> 1]);
         sts128(dst_tile + sw128_off(r, w), o[0], o[1], o[2], o[3]);
+    }
+}
+
+// W4, half a row: the 32 codes of K half h (one 16-byte chunk) and their 2 scales.
+__device__ __forceinline__ void convert_w4_half(uint32_t raw_tile, uint32_t dst_tile, int r, int h, uint32_t sbytes) {
+    const int sw = (r >> 2) & 1;
+    const uint4 c = lds128(raw_tile + r * 32 + ((h ^ sw) << 4));
+    const uint32_t sc0 = w4_scale_bf16x2(sbytes >> (16 * h));
+    const uint32_t sc1 = w4_scale_bf16x2(sbytes >> (16 * h + 8));
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t hh[4], o[4];
+        cvt_e2m1x8_f16x2(words[w], hh);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(hh[i]), (w < 2) ? sc0 : sc1);
+        sts128(dst_tile + sw128_off(r, 4 * h + w), o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -434,11 +461,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             }
                             tc_fence_after();
                         }
-                        const uint64_t adesc = smem_desc_sw128(a_base + kk * 32);
                         const uint64_t bdesc = smem_desc_sw128(b_base + kk * 32);
-                        const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::BN);
+                        const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::MSUB * C::BN);
                         if (elect_one_sync()) {
-                            tc_mma_f16(dtmem, adesc, bdesc, C::IDESC, first ? 0u : 1u);
+#pragma unroll
+                            for (int m = 0; m < C::MSUB; ++m)
+                                tc_mma_f16(dtmem + (uint32_t)(m * C::BN), smem_desc_sw128(a_base + m * 16384 + kk * 32),
+                                           bdesc, C::IDESC, first ? 0u : 1u);
                             if (last) tc_commit(&acc_full[buf]);
                         }
                         __syncwarp();
@@ -484,97 +513,101 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         bool ok = true;
         for (int t = cid; t < num_tiles && ok; t += ncl) {
             const TileInfo ti = decode_tile<C>(p, t, crank);
-            const bool valid = row < ti.rows;
-            const long grow = (long)ti.row0 + row;
             if constexpr (!C::FOLD) {
                 if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN);
-                if constexpr (C::EPI == Epi::STORE) {
-                    const float s2 = p.scale2_dense;
 #pragma unroll 1
-                    for (int c = 0; c < C::BN / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(acc + c * 32, r);
-                        tmem_ld_wait();
-                        const int col = ti.n0 + c * 32;
-                        if (valid && col < p.N) {
-                            if (p.ydt == 0) {
-                                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + grow * p.ldy + col);
-#pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    dst[j] = make_float4(__uint_as_float(r[4 * j]) * s2, __uint_as_float(r[4 * j + 1]) * s2,
-                                                         __uint_as_float(r[4 * j + 2]) * s2,
-                                                         __uint_as_float(r[4 * j + 3]) * s2);
-                            } else {
-                                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    uint32_t w[4];
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i) {
-                                        __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]) * s2,
-                                                                                 __uint_as_float(r[8 * j + 2 * i + 1]) * s2);
-                                        w[i] = *reinterpret_cast<uint32_t*>(&b);
+                for (int m = 0; m < C::MSUB; ++m) {
+                    // row sub-tile m: rows m*128 + lane of this warp's quarter
+                    const bool valid = m * 128 + row < ti.rows;
+                    const long grow = (long)ti.row0 + m * 128 + row;
+                    const uint32_t acc = lane_addr + (uint32_t)(buf * C::MSUB * C::BN + m * C::BN);
+                    if constexpr (C::EPI == Epi::STORE) {
+                        const float s2 = p.scale2_dense;
+    #pragma unroll 1
+                        for (int c = 0; c < C::BN / 32; ++c) {
+                            uint32_t r[32];
+                            tmem_ld32(acc + c * 32, r);
+                            tmem_ld_wait();
+                            const int col = ti.n0 + c * 32;
+                            if (valid && col < p.N) {
+                                if (p.ydt == 0) {
+                                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + grow * p.ldy + col);
+    #pragma unroll
+                                    for (int j = 0; j < 8; ++j)
+                                        dst[j] = make_float4(__uint_as_float(r[4 * j]) * s2, __uint_as_float(r[4 * j + 1]) * s2,
+                                                             __uint_as_float(r[4 * j + 2]) * s2,
+                                                             __uint_as_float(r[4 * j + 3]) * s2);
+                                } else {
+                                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
+    #pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        uint32_t w[4];
+    #pragma unroll
+                                        for (int i = 0; i < 4; ++i) {
+                                            __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]) * s2,
+                                                                                     __uint_as_float(r[8 * j + 2 * i + 1]) * s2);
+                                            w[i] = *reinterpret_cast<uint32_t*>(&b);
+                                        }
+                                        dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
                                     }
-                                    dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
                                 }
                             }
                         }
-                    }
-                } else {   // SWIGLU_Q81: columns [0, BN/2) gate, [BN/2, BN) up
-                    const float s2 = p.scale2[ti.expert];
-#pragma unroll 1
-                    for (int c = 0; c < C::BN / 64; ++c) {
-                        uint32_t g[32], u[32];
-                        tmem_ld32(acc + c * 32, g);
-                        tmem_ld32(acc + C::BN / 2 + c * 32, u);
-                        tmem_ld_wait();
-                        if (valid) {
-                            float h[32];
-                            float amax = 0.f;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const float gv = __uint_as_float(g[j]) * s2;
-                                const float uv = __uint_as_float(u[j]) * s2;
-                                h[j] = gv / (1.0f + expf(-gv)) * uv;
-                                amax = fmaxf(amax, fabsf(h[j]));
-                            }
-                            uint32_t packed[8];
-                            int sum = 0;
-                            float d = 0.f;
-                            if (amax > 0.f) {
-                                d = amax / 127.0f;
-#pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    uint32_t w = 0;
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i) {
-                                        float v = roundf(h[4 * j + i] / d);
-                                        v = fminf(fmaxf(v, -127.f), 127.f);
-                                        const int qv = (int)v;
-                                        sum += qv;
-                                        w |= ((uint32_t)(qv & 0xFF)) << (8 * i);
-                                    }
-                                    packed[j] = w;
+                    } else {   // SWIGLU_Q81: columns [0, BN/2) gate, [BN/2, BN) up
+                        const float s2 = p.scale2[ti.expert];
+    #pragma unroll 1
+                        for (int c = 0; c < C::BN / 64; ++c) {
+                            uint32_t g[32], u[32];
+                            tmem_ld32(acc + c * 32, g);
+                            tmem_ld32(acc + C::BN / 2 + c * 32, u);
+                            tmem_ld_wait();
+                            if (valid) {
+                                float h[32];
+                                float amax = 0.f;
+    #pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    const float gv = __uint_as_float(g[j]) * s2;
+                                    const float uv = __uint_as_float(u[j]) * s2;
+                                    h[j] = gv / (1.0f + expf(-gv)) * uv;
+                                    amax = fmaxf(amax, fabsf(h[j]));
                                 }
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 8; ++j) packed[j] = 0;
+                                uint32_t packed[8];
+                                int sum = 0;
+                                float d = 0.f;
+                                if (amax > 0.f) {
+                                    d = amax / 127.0f;
+    #pragma unroll
+                                    for (int j = 0; j < 8; ++j) {
+                                        uint32_t w = 0;
+    #pragma unroll
+                                        for (int i = 0; i < 4; ++i) {
+                                            float v = roundf(h[4 * j + i] / d);
+                                            v = fminf(fmaxf(v, -127.f), 127.f);
+                                            const int qv = (int)v;
+                                            sum += qv;
+                                            w |= ((uint32_t)(qv & 0xFF)) << (8 * i);
+                                        }
+                                        packed[j] = w;
+                                    }
+                                } else {
+    #pragma unroll
+                                    for (int j = 0; j < 8; ++j) packed[j] = 0;
+                                }
+                                const int col = ti.n0 + c * 32;
+                                uint4* hq = reinterpret_cast<uint4*>(p.Hq + grow * p.F + col);
+                                hq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                                hq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                                const long bidx = grow * (p.F / 32) + col / 32;
+                                const __half d16 = __float2half_rn(d);
+                                p.Hd[bidx] = d16;
+                                p.Hs[bidx] = __float2half_rn(d * (float)sum);
+                                // the value the down product uses, fp32, per tile entry [entry][F/32][128 rows]
+                                p.Hd32[((long)(ti.entry + m) * (p.F / 32) + col / 32) * 128 + row] = __half2float(d16);
                             }
-                            const int col = ti.n0 + c * 32;
-                            uint4* hq = reinterpret_cast<uint4*>(p.Hq + grow * p.F + col);
-                            hq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                            hq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                            const long bidx = grow * (p.F / 32) + col / 32;
-                            const __half d16 = __float2half_rn(d);
-                            p.Hd[bidx] = d16;
-                            p.Hs[bidx] = __float2half_rn(d * (float)sum);
-                            // the value the down product uses, fp32, per tile entry [entry][F/32][128 rows]
-                            p.Hd32[((long)ti.entry * (p.F / 32) + col / 32) * C::BM + row] = __half2float(d16);
                         }
                     }
                 }
@@ -587,6 +620,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             } else {
                 // FP8 fold: one accumulator per 128-K block, folded into registers with its scale
+                const bool valid = row < ti.rows;
+                const long grow = (long)ti.row0 + row;
                 const int groups = p.K / C::GROUP_K;
                 float sum[64];
 #pragma unroll
@@ -634,7 +669,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
     } else if (C::conv_slot(warp) >= 0) {
         // ------------------------------------------------------------ converters
-        const int ct = C::conv_slot(warp) * 32 + lane;   // this thread's weight row in every tile
+        const int ct = C::conv_slot(warp) * 32 + lane;
+        const int crow = ct % C::BN;                      // this thread's weight row in every tile
+        const int chalf = ct / C::BN;                     // and its K half (TPR == 2)
         int ts = 0, cs = 0;
         uint32_t tph = 0, cph = 0;
         bool ok = true;
@@ -644,12 +681,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int kchunks = kblocks / 4;
         auto scale_row = [&](const TileInfo& tt, bool& in_range) -> long {
             if constexpr (C::EPI == Epi::SWIGLU_Q81) {
-                const int hr = (ct < C::BN / 2) ? (tt.n0 + ct) : (p.F + tt.n0 + ct - C::BN / 2);
+                const int hr = (crow < C::BN / 2) ? (tt.n0 + crow) : (p.F + tt.n0 + crow - C::BN / 2);
                 in_range = true;
                 return (long)tt.expert * 2 * p.F + hr;
             } else {
-                in_range = (long)tt.n0 + ct < p.N;
-                return (long)tt.n0 + ct;
+                in_range = (long)tt.n0 + crow < p.N;
+                return (long)tt.n0 + crow;
             }
         };
         auto load_chunk = [&](int t, int ch) -> uint4 {
@@ -691,9 +728,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const uint32_t braw = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
                 const uint32_t bconv = smem_u32(cstage + cs * C::CSTAGE_BYTES);
                 if constexpr (C::B == BMode::W4) {
-                    convert_w4_row(braw, bconv, ct, sbytes);
+                    if constexpr (C::TPR == 2)
+                        convert_w4_half(braw, bconv, crow, chalf, sbytes);
+                    else
+                        convert_w4_row(braw, bconv, crow, sbytes);
                 } else {
-                    convert_fp8_row(braw, bconv, ct);
+                    convert_fp8_row(braw, bconv, crow);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();

@@ -58,9 +58,12 @@ struct RouteBufs {
     int32_t* src;         // [T*k]
     int32_t* row;         // [T][k]
     int32_t* chunk_hist;  // [chunks][E]  (scratch)
-    int4* tiles;          // [max_entries] (optional)
+    int4* tiles;          // [max_entries] 128-row entries (optional)
     int32_t* num_entries; // [1]            (optional)
     int max_entries;
+    int4* tiles2;         // [max_entries2] 256-row entries (optional, needs tiles)
+    int32_t* num_entries2;
+    int max_entries2;
 };
 constexpr int kRouteChunk = 256;   // tokens per grouping chunk
 cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBufs& b, cudaStream_t s);

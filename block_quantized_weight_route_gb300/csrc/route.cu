@@ -126,11 +126,14 @@ __device__ int block_exclusive_scan(int v, int* total) {
 }
 
 // One CTA of 1024 threads (E <= 1024): per-expert counts and the exclusive
-// per-chunk bases (in place in chunk_hist), offsets, and the 128-row tile list.
+// per-chunk bases (in place in chunk_hist), offsets, and the tile lists:
+// 128-row entries {expert, first row, rows, 0} and 256-row entries
+// {expert, first row, rows, index of its first 128-row entry}.
 __global__ void __launch_bounds__(1024) route_scan_kernel(int chunks, int E, int32_t* __restrict__ chunk_hist,
                                                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                           int4* __restrict__ tiles, int32_t* __restrict__ num_entries,
-                                                          int max_entries) {
+                                                          int max_entries, int4* __restrict__ tiles2,
+                                                          int32_t* __restrict__ num_entries2, int max_entries2) {
     const int e = threadIdx.x;
     int cnt = 0;
     if (e < E) {
@@ -154,6 +157,17 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int chunks, int E, int
             if (idx < max_entries) tiles[idx] = make_int4(e, off + 128 * i, min(128, cnt - 128 * i), 0);
         }
         if (e == 0) *num_entries = min(ntiles, max_entries);
+        if (tiles2) {
+            const int mt2 = (e < E) ? (cnt + 255) / 256 : 0;
+            int ntiles2;
+            const int tbase2 = block_exclusive_scan(mt2, &ntiles2);
+            for (int i = 0; i < mt2; ++i) {
+                const int idx = tbase2 + i;
+                if (idx < max_entries2)
+                    tiles2[idx] = make_int4(e, off + 256 * i, min(256, cnt - 256 * i), tbase + 2 * i);
+            }
+            if (e == 0) *num_entries2 = min(ntiles2, max_entries2);
+        }
     }
 }
 
@@ -217,7 +231,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBu
     const int chunks = (T + kRouteChunk - 1) / kRouteChunk;
     route_hist_kernel<<<chunks, 256, E * sizeof(int32_t), s>>>(b.ids, T, E, k, b.chunk_hist);
     route_scan_kernel<<<1, 1024, 0, s>>>(chunks, E, b.chunk_hist, b.counts, b.offsets, b.tiles, b.num_entries,
-                                         b.max_entries);
+                                         b.max_entries, b.tiles2, b.num_entries2, b.max_entries2);
     const size_t msmem = (size_t)E * (kRouteChunk / 32) * sizeof(uint32_t);
     route_permute_kernel<<<chunks, kRouteChunk, msmem, s>>>(b.ids, T, E, k, b.chunk_hist, b.offsets, b.src, b.row);
     return cudaGetLastError();

@@ -86,9 +86,9 @@ def test_expert_stage_workspace_layout_is_consistent(L):
         assert off[-1] == L.moe_expert_stage_workspace_size(T, D, F, E, k)
         P = T * k
         # the large regions have at least their nominal sizes
-        assert off[10] - off[9] >= P * D * 2          # X_perm
-        assert off[11] - off[10] >= P * F             # Hq
-        assert off[15] - off[14] >= P * D * 4         # Yslot
+        assert off[12] - off[11] >= P * D * 2         # X_perm
+        assert off[13] - off[12] >= P * F             # Hq
+        assert off[17] - off[16] >= P * D * 4         # Yslot
     arr = (ctypes.c_size_t * QMM_WS_FIELDS)()
     assert L.moe_expert_stage_workspace_layout(10, 100, 128, 8, 2, arr) == 2     # D % 128
     assert L.moe_expert_stage_workspace_layout(10, 128, 2048, 8, 2, arr) == 2    # F > 1024
