@@ -27,16 +27,21 @@
 
 namespace qmm {
 
-struct DownCfg {
+template <int EPI_WARPS_>
+struct DownCfgT {
     static constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16, GROUP_K = 32;
-    // 16 warps: producer 0, MMA 1, epilogue 4..11, converters 2, 3, 12, 14 (none
-    // shares sub-partition 1 with the MMA issuer), 5 and 9 only fold, 13 and 15 idle.
-    static constexpr int EPI_WARPS = 8, CONV_WARPS = 4, EPI_BASE = 4;
-    static constexpr int THREADS = 512;
+    // Warps: producer 0, MMA 1, epilogue 4 .. 4+EPI_WARPS-1 (EPI_WARPS/4 per TMEM
+    // lane quarter, each folding CPW token columns), converters on warps 2, 3 and
+    // two more after the epilogue on sub-partitions 0 and 2 (none shares
+    // sub-partition 1 with the MMA issuer), the rest idle.
+    static constexpr int EPI_WARPS = EPI_WARPS_, CONV_WARPS = 4, EPI_BASE = 4;
+    static constexpr int CPW = 128 / (EPI_WARPS_ / 4);        // token columns per epilogue warp
+    static constexpr int THREADS = 32 * (EPI_WARPS_ + 8);
     __device__ static int conv_slot(int warp) {
-        constexpr unsigned long long tab = 0x403000000002100ull;   // slot + 1 per warp, one nibble each
-        return (int)((tab >> (4 * warp)) & 15u) - 1;
+        const int w2 = 4 + EPI_WARPS;                          // first warp after the epilogue (sub-partition 0)
+        return warp == 2 ? 0 : (warp == 3 ? 1 : (warp == w2 ? 2 : (warp == w2 + 2 ? 3 : -1)));
     }
+    static_assert(EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue width");
     static constexpr int TSTAGES = 4, CSTAGES = 3, SSTAGES = 2, NBUF = 4;
     static constexpr int KG_MAX = 32;                         // K <= 1024
     static constexpr int A_RAW_BYTES = BM * 32;               // IQ4 codes: 64 indices per row
@@ -52,6 +57,10 @@ struct DownCfg {
     static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0 && SSTAGE_BYTES % 1024 == 0, "align");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
+#ifndef QMM_DOWN_EPI_WARPS
+#define QMM_DOWN_EPI_WARPS 8
+#endif
+using DownCfg = DownCfgT<QMM_DOWN_EPI_WARPS>;
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -83,9 +92,9 @@ __device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c
 // p.Y: Yslot [T*k][D] fp32 (p.ldy = D).
 // tmA: IQ4 codes as [E*D][F/2] bytes, box {32, 128}, 32-byte swizzle.
 // tmB: H codes as [T*k][F] bytes, box {64, 128}, 64-byte swizzle.
-__global__ void __launch_bounds__(DownCfg::THREADS, 1)
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
     down_iq4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
-    using C = DownCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tstage = smem;
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
     } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
-        const int half = (warp - C::EPI_BASE) >> 2;
+        const int cq = (warp - C::EPI_BASE) >> 2;              // this warp's block of CPW token columns
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
         int buf = 0, ss = 0;
         uint32_t bph = 0, sph = 0;
@@ -289,10 +298,10 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
                 }
             }
             if (!mbar_wait(&full_s[ss], sph, abort_flag, p.err, DEV_TIMEOUT_ACC)) break;
-            const uint32_t dh_base = smem_u32(sstage + ss * C::SSTAGE_BYTES) + half * 64 * 4;
-            uint64_t y[32];                                       // 64 token columns as f32 pairs
+            const uint32_t dh_base = smem_u32(sstage + ss * C::SSTAGE_BYTES) + cq * C::CPW * 4;
+            uint64_t y[C::CPW / 2];                               // CPW token columns as f32 pairs
 #pragma unroll
-            for (int j = 0; j < 32; ++j) y[j] = 0ull;
+            for (int j = 0; j < C::CPW / 2; ++j) y[j] = 0ull;
             for (int g = 0; g < groups; ++g) {
                 if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                     ok = false;
@@ -302,9 +311,9 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
                 const uint32_t pair = dwh[g >> 1];
                 const float dwf = __half2float(__ushort_as_half((unsigned short)((g & 1) ? (pair >> 16) : (pair & 0xFFFFu))));
                 const uint64_t dw2 = f32x2_pack(dwf, dwf);
-                const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + half * 64);
+                const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + cq * C::CPW);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < C::CPW / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(acc + c * 32, r);
                     tmem_ld_wait();
@@ -336,9 +345,9 @@ __global__ void __launch_bounds__(DownCfg::THREADS, 1)
             if (!ok) break;
             // Yslot[row, n] for this warp's 64 token columns; lanes write consecutive n
             float* out = static_cast<float*>(p.Y) + (long)g4.y * p.ldy + n;
-            const int tok0 = half * 64;
+            const int tok0 = cq * C::CPW;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < C::CPW / 2; ++j) {
                 float lo, hi;
                 asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(y[j]));
                 if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = lo;

@@ -7,10 +7,10 @@ int smem_iq4_down() { return DownCfg::SMEM_BYTES; }
 
 cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                             cudaStream_t s) {
-    cudaError_t e =
-        cudaFuncSetAttribute(down_iq4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DownCfg::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(down_iq4_kernel<DownCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DownCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    down_iq4_kernel<<<grid, DownCfg::THREADS, DownCfg::SMEM_BYTES, s>>>(tmA, tmB, p);
+    down_iq4_kernel<DownCfg><<<grid, DownCfg::THREADS, DownCfg::SMEM_BYTES, s>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 

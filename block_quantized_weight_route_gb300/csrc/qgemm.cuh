@@ -428,6 +428,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t tph = 0, cph = 0, bph = 0;
             bool ok = true;
             for (int t = cid; t < num_tiles && ok; t += ncl) {
+                // sub-tiles holding at least one live row (a tile of <= 128 rows skips the second)
+                int nsub = C::MSUB;
+                if constexpr (C::MSUB == 2) nsub = (decode_tile<C>(p, t, crank).rows > 128) ? 2 : 1;
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
                     bool got = mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL);
                     got = got && mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
@@ -466,8 +469,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if (elect_one_sync()) {
 #pragma unroll
                             for (int m = 0; m < C::MSUB; ++m)
-                                tc_mma_f16(dtmem + (uint32_t)(m * C::BN), smem_desc_sw128(a_base + m * 16384 + kk * 32),
-                                           bdesc, C::IDESC, first ? 0u : 1u);
+                                if (m < nsub)
+                                    tc_mma_f16(dtmem + (uint32_t)(m * C::BN),
+                                               smem_desc_sw128(a_base + m * 16384 + kk * 32), bdesc, C::IDESC,
+                                               first ? 0u : 1u);
                             if (last) tc_commit(&acc_full[buf]);
                         }
                         __syncwarp();
@@ -521,6 +526,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int m = 0; m < C::MSUB; ++m) {
+                    if (m * 128 >= ti.rows) break;   // the MMA skipped this sub-tile: nothing to read
                     // row sub-tile m: rows m*128 + lane of this warp's quarter
                     const bool valid = m * 128 + row < ti.rows;
                     const long grow = (long)ti.row0 + m * 128 + row;
