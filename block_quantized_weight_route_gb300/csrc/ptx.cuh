@@ -65,22 +65,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware until the phase
+// completes (it is woken when it does) or `hint_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete.  Returns false (after setting
 // *err to `code` if no error was recorded yet, and raising the CTA-wide abort
 // flag) when the wait times out or another role of the CTA has aborted.
-// The fast path polls try_wait (which itself suspends the thread for a short,
-// hardware-defined time) before touching the wall clock: reading %globaltimer
-// is slow, so it is consulted only every 256 polls.
+// After a first poll the thread sleeps in try_wait (woken on completion, or
+// after at most 2 us) rather than spinning: polling warps slow the warps that
+// do the work.  The wall clock (slow to read) is consulted every 64 sleeps.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err, uint32_t code) {
-#pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 256; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
             atomicCAS(err, 0u, code);
