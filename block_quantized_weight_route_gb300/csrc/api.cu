@@ -147,7 +147,7 @@ void stage_layout(int T, int D, int F, int E, int k, size_t* off) {
         (size_t)max_tile_entries256(T, E, k) * 16,  // tile list, 256-row entries
         16,                                         // tile count
         P * D * 2,                                  // X_perm
-        P * F,                                      // Hq
+        P * F * 2,                                  // Hq (f16 codes)
         P * (F / 32) * 2,                           // Hd
         P * (F / 32) * 2,                           // Hs
         (size_t)max_tile_entries(T, E, k) * (F / 32) * 128 * 4,   // Hd32: fp32 d per tile entry
@@ -366,7 +366,7 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     if (e != cudaSuccess) return cuda_fail(e, "expert stage: gather");
     if ((e = mark(d, 2, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
-    int8_t* Hq = static_cast<int8_t*>(at(12));
+    __half* Hq = static_cast<__half*>(at(12));
     __half* Hd = static_cast<__half*>(at(13));
     __half* Hs = static_cast<__half*>(at(14));
     float* Hd32 = static_cast<float*>(at(15));
@@ -406,8 +406,8 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     if ((st = make_tmap(&ta2, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
                         CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
         return st;
-    if ((st = make_tmap(&tb2, Hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, F, P, F, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) !=
-        QMM_OK)
+    if ((st = make_tmap(&tb2, Hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, F, P, (uint64_t)F * 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
     GemmParams q{};
     q.N = D;

@@ -12,55 +12,76 @@
 // epilogue folds with d_H * d_W in fp32.
 //
 // Orientation: the MMA's M side is 128 weight rows (output dims n), its N side
-// 128 routed tokens of one expert.  Each epilogue thread owns one output dim,
-// so its d_W values live in registers; d_H varies along the columns and is read
-// from a shared-memory copy of the tile's fp32 d values (one 1-D bulk copy per
-// tile from the per-tile-entry layout the gate/up epilogue writes).
+// 128 routed tokens of one expert.  Each epilogue thread owns one output dim
+// and reads its d_W per block from shared memory; d_H varies along the columns
+// and is read (broadcast) from a shared-memory copy of the tile's fp32 d values.
+// Both scale tables arrive by 1-D bulk copies once per tile: d_H from the
+// per-tile-entry layout the gate/up epilogue writes, d_W as the tile's 128
+// contiguous rows of [E][D][F/32].
 //
-//   warp 0: TMA producer (IQ4 codes + int8 H codes per K block, d_H per tile)
+// The H codes are stored by the gate/up epilogue as exact f16 integers, so the
+// MMA's token operand comes straight from TMA (128-byte swizzle) with no
+// conversion; only the IQ4 indices are expanded (codebook lookup) to f16.
+//
+//   warp 0: TMA producer (IQ4 codes + f16 H codes per K block, d_H and d_W per tile)
 //   warp 1: TMEM owner and MMA issuer
-//   warps 4..11: epilogue (2 per TMEM lane quarter, 64 token columns each)
-//   warps 2, 3, 12, 14: converters (one weight row and one token row per thread),
-//   kept off the MMA issuer's sub-partition (warp id % 4 == 1)
+//   warps 4 .. 4+EPI_WARPS-1: epilogue (EPI_WARPS/4 per TMEM lane quarter)
+//   warps 2, 3 (and with four converters two more after the epilogue, on
+//   sub-partitions 0 and 2): IQ4 converters; none shares sub-partition 1 with
+//   the MMA issuer
 #pragma once
 #include "qgemm.cuh"
 
 namespace qmm {
 
-template <int EPI_WARPS_>
+template <int EPI_WARPS_, int CONV_WARPS_, int TSTAGES_>
 struct DownCfgT {
     static constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16, GROUP_K = 32;
-    // Warps: producer 0, MMA 1, epilogue 4 .. 4+EPI_WARPS-1 (EPI_WARPS/4 per TMEM
-    // lane quarter, each folding CPW token columns), converters on warps 2, 3 and
-    // two more after the epilogue on sub-partitions 0 and 2 (none shares
-    // sub-partition 1 with the MMA issuer), the rest idle.
-    static constexpr int EPI_WARPS = EPI_WARPS_, CONV_WARPS = 4, EPI_BASE = 4;
+    static constexpr int EPI_WARPS = EPI_WARPS_, CONV_WARPS = CONV_WARPS_, EPI_BASE = 4;
     static constexpr int CPW = 128 / (EPI_WARPS_ / 4);        // token columns per epilogue warp
-    static constexpr int THREADS = 32 * (EPI_WARPS_ + 8);
+    static constexpr int NCH = CPW / 32;                      // 32-column TMEM loads per block
+    static constexpr int W2 = EPI_BASE + EPI_WARPS;           // first warp after the epilogue (sub-partition 0)
+    static constexpr int THREADS = 32 * (CONV_WARPS == 2 ? W2 : W2 + 3);
+    static constexpr int CONV_THREADS = 32 * CONV_WARPS;
     __device__ static int conv_slot(int warp) {
-        const int w2 = 4 + EPI_WARPS;                          // first warp after the epilogue (sub-partition 0)
-        return warp == 2 ? 0 : (warp == 3 ? 1 : (warp == w2 ? 2 : (warp == w2 + 2 ? 3 : -1)));
+        if (warp == 2) return 0;
+        if (warp == 3) return 1;
+        if (CONV_WARPS == 4) {
+            if (warp == W2) return 2;
+            if (warp == W2 + 2) return 3;
+        }
+        return -1;
     }
     static_assert(EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue width");
-    static constexpr int TSTAGES = 4, CSTAGES = 3, SSTAGES = 2, NBUF = 4;
+    static_assert(CONV_WARPS == 2 || CONV_WARPS == 4, "converter count");
+    static constexpr int TSTAGES = TSTAGES_, CSTAGES = 3, SSTAGES = 2, NBUF = 4;
     static constexpr int KG_MAX = 32;                         // K <= 1024
     static constexpr int A_RAW_BYTES = BM * 32;               // IQ4 codes: 64 indices per row
-    static constexpr int B_RAW_BYTES = BN * 64;               // int8 H codes
-    static constexpr int TSTAGE_BYTES = A_RAW_BYTES + B_RAW_BYTES;
-    static constexpr int A_CONV_BYTES = BM * BK * 2, B_CONV_BYTES = BN * BK * 2;
-    static constexpr int CSTAGE_BYTES = A_CONV_BYTES + B_CONV_BYTES;
-    static constexpr int SSTAGE_BYTES = KG_MAX * BN * 4;      // d_H of one tile, [group][token] fp32
+    static constexpr int B_BYTES = BN * BK * 2;               // f16 H codes, 128-byte rows
+    static constexpr int TSTAGE_BYTES = A_RAW_BYTES + B_BYTES;
+    static constexpr int CSTAGE_BYTES = BM * BK * 2;          // expanded IQ4 values
+    static constexpr int DH_BYTES = KG_MAX * BN * 4;          // d_H of one tile, [block][token] fp32
+    static constexpr int DW_BYTES = BM * KG_MAX * 2;          // d_W of one tile, [row][block] fp16
+    static constexpr int SSTAGE_BYTES = DH_BYTES + DW_BYTES;
     static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, false);
     static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * SSTAGES + 2 * NBUF + 1;
     static constexpr int SMEM_BYTES = 1024 + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES +
                                       SSTAGES * SSTAGE_BYTES + BAR_COUNT * 8 + 64;
-    static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0 && SSTAGE_BYTES % 1024 == 0, "align");
+    static_assert(A_RAW_BYTES % 1024 == 0 && TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0 &&
+                      SSTAGE_BYTES % 1024 == 0,
+                  "align");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 #ifndef QMM_DOWN_EPI_WARPS
-#define QMM_DOWN_EPI_WARPS 8
+#define QMM_DOWN_EPI_WARPS 16
 #endif
-using DownCfg = DownCfgT<QMM_DOWN_EPI_WARPS>;
+#ifndef QMM_DOWN_CONV_WARPS
+#define QMM_DOWN_CONV_WARPS 2
+#endif
+#ifndef QMM_DOWN_TSTAGES
+#define QMM_DOWN_TSTAGES 4
+#endif
+using DownCfg = DownCfgT<QMM_DOWN_EPI_WARPS, QMM_DOWN_CONV_WARPS, QMM_DOWN_TSTAGES>;
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -68,6 +89,12 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
                      smem_u32(smem_dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t saddr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr));
+    return v;
 }
 
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
@@ -91,7 +118,7 @@ __device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c
 // p.dW: IQ4_NL scales [E][D][F/32] fp16, p.dH32: d_H fp32 [entry][F/32][128],
 // p.Y: Yslot [T*k][D] fp32 (p.ldy = D).
 // tmA: IQ4 codes as [E*D][F/2] bytes, box {32, 128}, 32-byte swizzle.
-// tmB: H codes as [T*k][F] bytes, box {64, 128}, 64-byte swizzle.
+// tmB: H codes as [T*k][F] f16, box {64, 128}, 128-byte swizzle.
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     down_iq4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
@@ -117,7 +144,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::TSTAGES; ++i) {
             mbar_init(&full_t[i], 1);
-            mbar_init(&empty_t[i], C::CONV_WARPS);
+            // released by the converters (IQ4 codes read) and the MMA commit (H codes read)
+            mbar_init(&empty_t[i], C::CONV_WARPS + 1);
         }
         for (int i = 0; i < C::CSTAGES; ++i) {
             mbar_init(&full_c[i], C::CONV_WARPS);
@@ -157,18 +185,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t ph = 0, sph = 0;
             long issued = 0, s_issued = 0;
             bool ok = true;
-            const uint32_t sbytes = (uint32_t)(groups * C::BN * 4);
+            const uint32_t dh_bytes = (uint32_t)(groups * C::BN * 4);
+            const uint32_t dw_bytes = (uint32_t)(C::BM * groups * 2);
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const int entry = t / p.n_tiles;
                 const int n0 = (t - entry * p.n_tiles) * C::BM;
                 const int4 g = p.tiles[entry];
-                // this tile's d_H values
+                // this tile's d_H and d_W values
                 const bool sfree = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
                 if (__any_sync(0xffffffffu, !sfree)) break;
                 if (elect_one_sync()) {
-                    mbar_arrive_expect_tx(&full_s[ss], sbytes);
-                    bulk_load(sstage + ss * C::SSTAGE_BYTES, p.dH32 + (long)entry * groups * C::BN, sbytes,
-                              &full_s[ss]);
+                    uint8_t* st = sstage + ss * C::SSTAGE_BYTES;
+                    mbar_arrive_expect_tx(&full_s[ss], dh_bytes + dw_bytes);
+                    bulk_load(st, p.dH32 + (long)entry * groups * C::BN, dh_bytes, &full_s[ss]);
+                    bulk_load(st + C::DH_BYTES, p.dW + ((long)g.x * p.N + n0) * groups, dw_bytes, &full_s[ss]);
                 }
                 __syncwarp();
                 ++s_issued;
@@ -204,20 +234,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         {
-            int cs = 0, buf = 0;
-            uint32_t cph = 0, bph = 0;
+            int cs = 0, ts = 0, buf = 0;
+            uint32_t cph = 0, tph = 0, bph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
-                    const bool got = mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
+                    // expanded weights ready (the converters saw the TMA stage complete);
+                    // the H codes of the same stage are waited on directly
+                    const bool got = mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV) &&
+                                     mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL);
                     if (__any_sync(0xffffffffu, !got)) {
                         ok = false;
                         break;
                     }
-                    // (no tcgen05 fence here: the operands are ordered by the mbarrier and the
+                    // (no tcgen05 fence here: the operands are ordered by the mbarriers and the
                     // writers' proxy fence; a tcgen05 fence per K block would drain the MMA pipe)
                     const uint32_t a_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
-                    const uint32_t b_base = a_base + C::A_CONV_BYTES;
+                    const uint32_t b_base = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
                         const bool first = (kk & 1) == 0, last = (kk & 1) == 1;
@@ -246,11 +279,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         }
                     }
                     if (!ok) break;
-                    if (elect_one_sync()) tc_commit(&empty_c[cs]);
+                    if (elect_one_sync()) {
+                        tc_commit(&empty_c[cs]);
+                        tc_commit(&empty_t[ts]);
+                    }
                     __syncwarp();
                     if (++cs == C::CSTAGES) {
                         cs = 0;
                         cph ^= 1u;
+                    }
+                    if (++ts == C::TSTAGES) {
+                        ts = 0;
+                        tph ^= 1u;
                     }
                 }
             }
@@ -262,43 +302,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int cq = (warp - C::EPI_BASE) >> 2;              // this warp's block of CPW token columns
+        const int r = q * 32 + lane;                            // this thread's weight row in the tile
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
         int buf = 0, ss = 0;
         uint32_t bph = 0, sph = 0;
         bool ok = true;
+        int4 g4 = (int)blockIdx.x < num_tiles ? p.tiles[blockIdx.x / p.n_tiles] : make_int4(0, 0, 0, 0);
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             const int entry = t / p.n_tiles;
             const int n0 = (t - entry * p.n_tiles) * C::BM;
-            const int4 g4 = p.tiles[entry];
-            const int n = n0 + q * 32 + lane;                   // this thread's output dim
-            // d_W[e, n, 0..groups) as half2 pairs (groups <= 32, 16-byte vector loads)
-            uint32_t dwh[C::KG_MAX / 2];
-            const __half* dw_row = p.dW + ((long)g4.x * p.N + n) * groups;
-            if ((groups & 7) == 0) {            // rows are whole 16-byte vectors
-                const uint4* dwp = reinterpret_cast<const uint4*>(dw_row);
-#pragma unroll
-                for (int i = 0; i < C::KG_MAX / 8; ++i) {
-                    if (i * 8 < groups) {
-                        const uint4 v = __ldg(dwp + i);
-                        dwh[4 * i] = v.x;
-                        dwh[4 * i + 1] = v.y;
-                        dwh[4 * i + 2] = v.z;
-                        dwh[4 * i + 3] = v.w;
-                    } else {
-                        dwh[4 * i] = dwh[4 * i + 1] = dwh[4 * i + 2] = dwh[4 * i + 3] = 0u;
-                    }
-                }
-            } else {
-                const unsigned short* dws = reinterpret_cast<const unsigned short*>(dw_row);
-#pragma unroll
-                for (int i = 0; i < C::KG_MAX / 2; ++i) {
-                    const uint32_t lo = (2 * i < groups) ? __ldg(dws + 2 * i) : 0u;
-                    const uint32_t hi = (2 * i + 1 < groups) ? __ldg(dws + 2 * i + 1) : 0u;
-                    dwh[i] = lo | (hi << 16);
-                }
-            }
+            const int tn = t + gridDim.x;
+            // the next tile's descriptor, loaded while this tile runs
+            const int4 g4n = tn < num_tiles ? p.tiles[tn / p.n_tiles] : make_int4(0, 0, 0, 0);
             if (!mbar_wait(&full_s[ss], sph, abort_flag, p.err, DEV_TIMEOUT_ACC)) break;
-            const uint32_t dh_base = smem_u32(sstage + ss * C::SSTAGE_BYTES) + cq * C::CPW * 4;
+            const uint32_t sbase = smem_u32(sstage + ss * C::SSTAGE_BYTES);
+            const uint32_t dh_base = sbase + cq * C::CPW * 4;
+            const uint32_t dw_addr = sbase + C::DH_BYTES + (uint32_t)(r * groups * 2);
             uint64_t y[C::CPW / 2];                               // CPW token columns as f32 pairs
 #pragma unroll
             for (int j = 0; j < C::CPW / 2; ++j) y[j] = 0ull;
@@ -308,29 +327,31 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t pair = dwh[g >> 1];
-                const float dwf = __half2float(__ushort_as_half((unsigned short)((g & 1) ? (pair >> 16) : (pair & 0xFFFFu))));
+                const float dwf = __half2float(__ushort_as_half((unsigned short)lds_u16(dw_addr + g * 2)));
                 const uint64_t dw2 = f32x2_pack(dwf, dwf);
                 const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + cq * C::CPW);
 #pragma unroll
-                for (int c = 0; c < C::CPW / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(acc + c * 32, r);
+                for (int c = 0; c < C::NCH; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(acc + c * 32, v);
                     tmem_ld_wait();
+                    if (c == C::NCH - 1) {
+                        // the accumulator is in registers: hand the buffer back before folding
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                    }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const uint4 dh = lds128(dh_base + (uint32_t)((g * C::BN + c * 32 + 4 * j) * 4));
-                        const uint64_t i01 = f32x2_pack(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]));
-                        const uint64_t i23 = f32x2_pack(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        const uint64_t i01 = f32x2_pack(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
+                        const uint64_t i23 = f32x2_pack(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                         const uint64_t d01 = f32x2_pack(__uint_as_float(dh.x), __uint_as_float(dh.y));
                         const uint64_t d23 = f32x2_pack(__uint_as_float(dh.z), __uint_as_float(dh.w));
                         y[c * 16 + 2 * j] = f32x2_fma(f32x2_mul(i01, d01), dw2, y[c * 16 + 2 * j]);
                         y[c * 16 + 2 * j + 1] = f32x2_fma(f32x2_mul(i23, d23), dw2, y[c * 16 + 2 * j + 1]);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[buf]);
                 if (++buf == C::NBUF) {
                     buf = 0;
                     bph ^= 1u;
@@ -343,8 +364,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 sph ^= 1u;
             }
             if (!ok) break;
-            // Yslot[row, n] for this warp's 64 token columns; lanes write consecutive n
-            float* out = static_cast<float*>(p.Y) + (long)g4.y * p.ldy + n;
+            // Yslot[row, n] for this warp's token columns; lanes write consecutive n
+            float* out = static_cast<float*>(p.Y) + (long)g4.y * p.ldy + n0 + r;
             const int tok0 = cq * C::CPW;
 #pragma unroll
             for (int j = 0; j < C::CPW / 2; ++j) {
@@ -353,9 +374,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = lo;
                 if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = hi;
             }
+            g4 = g4n;
         }
     } else if (C::conv_slot(warp) >= 0) {
-        // ------------------------------------------------------------ converters
+        // ------------------------------------------------------------ converters (IQ4 indices -> f16)
         const int ct = C::conv_slot(warp) * 32 + lane;
         int ts = 0, cs = 0;
         uint32_t tph = 0, cph = 0;
@@ -369,8 +391,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 const uint32_t traw = smem_u32(tstage + ts * C::TSTAGE_BYTES);
                 const uint32_t cbase = smem_u32(cstage + cs * C::CSTAGE_BYTES);
-                convert_iq4_row(traw, cbase, ct);
-                convert_i8_row(traw + C::A_RAW_BYTES, cbase + C::A_CONV_BYTES, ct);
+#pragma unroll
+                for (int rr = ct; rr < C::BM; rr += C::CONV_THREADS) convert_iq4_row(traw, cbase, rr);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

@@ -581,32 +581,31 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                     h[j] = gv / (1.0f + expf(-gv)) * uv;
                                     amax = fmaxf(amax, fabsf(h[j]));
                                 }
-                                uint32_t packed[8];
+                                // the codes are stored as exact f16 integers: the down
+                                // product's MMA reads them as its operand without conversion
+                                uint32_t packed[16];
                                 int sum = 0;
                                 float d = 0.f;
                                 if (amax > 0.f) {
                                     d = amax / 127.0f;
     #pragma unroll
-                                    for (int j = 0; j < 8; ++j) {
-                                        uint32_t w = 0;
-    #pragma unroll
-                                        for (int i = 0; i < 4; ++i) {
-                                            float v = roundf(h[4 * j + i] / d);
-                                            v = fminf(fmaxf(v, -127.f), 127.f);
-                                            const int qv = (int)v;
-                                            sum += qv;
-                                            w |= ((uint32_t)(qv & 0xFF)) << (8 * i);
-                                        }
-                                        packed[j] = w;
+                                    for (int j = 0; j < 16; ++j) {
+                                        float v0 = roundf(h[2 * j] / d), v1 = roundf(h[2 * j + 1] / d);
+                                        v0 = fminf(fmaxf(v0, -127.f), 127.f);
+                                        v1 = fminf(fmaxf(v1, -127.f), 127.f);
+                                        sum += (int)v0 + (int)v1;
+                                        const __half2 hv = __floats2half2_rn(v0, v1);
+                                        packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
                                     }
                                 } else {
     #pragma unroll
-                                    for (int j = 0; j < 8; ++j) packed[j] = 0;
+                                    for (int j = 0; j < 16; ++j) packed[j] = 0;
                                 }
                                 const int col = ti.n0 + c * 32;
                                 uint4* hq = reinterpret_cast<uint4*>(p.Hq + grow * p.F + col);
-                                hq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                                hq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    #pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    hq[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
                                 const long bidx = grow * (p.F / 32) + col / 32;
                                 const __half d16 = __float2half_rn(d);
                                 p.Hd[bidx] = d16;

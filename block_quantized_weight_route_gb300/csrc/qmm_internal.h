@@ -26,7 +26,7 @@ struct GemmParams {
     void* Y;                // output (fp32 or bf16)
     int ydt;                // 0: fp32, 1: bf16
     long ldy;               // output row pitch in elements
-    int8_t* Hq;             // gate/up: q8_1 codes of H [rows][F]
+    __half* Hq;             // gate/up: q8_1 codes of H [rows][F], exact f16 integers
     __half* Hd;             // gate/up: q8_1 d per 32-block [rows][F/32]
     __half* Hs;             // gate/up: q8_1 s per 32-block [rows][F/32]
     float* Hd32;            // gate/up: fp32 value of the fp16 d, [entry][F/32][128 rows]

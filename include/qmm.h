@@ -134,7 +134,9 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t *X, const float *logits, int T
  *   0 ids [T*k] i32     1 w [T*k] f32       2 counts [E] i32    3 offsets [E+1] i32
  *   4 src [T*k] i32     5 row [T*k] i32     6 chunk counts
  *   7 tile list, 128-row entries   8 its count   9 tile list, 256-row entries   10 its count
- *  11 X_perm [T*k][D] bf16   12 Hq [T*k][F] int8   13 Hd [T*k][F/32] fp16   14 Hs [T*k][F/32] fp16
+ *  11 X_perm [T*k][D] bf16   12 Hq [T*k][F] fp16: the q8_1 codes (integers in [-127, 127]) held
+ *     exactly as f16, the operand type of the down product's tensor-core MMA
+ *  13 Hd [T*k][F/32] fp16   14 Hs [T*k][F/32] fp16
  *  15 d of H as fp32 per 128-row tile (internal)   16 Yslot [T*k][D] fp32
  *  17 total size */
 #define QMM_WS_FIELDS 18

@@ -87,7 +87,7 @@ def test_expert_stage_workspace_layout_is_consistent(L):
         P = T * k
         # the large regions have at least their nominal sizes
         assert off[12] - off[11] >= P * D * 2         # X_perm
-        assert off[13] - off[12] >= P * F             # Hq
+        assert off[13] - off[12] >= P * F * 2         # Hq (f16 codes)
         assert off[17] - off[16] >= P * D * 4         # Yslot
     arr = (ctypes.c_size_t * QMM_WS_FIELDS)()
     assert L.moe_expert_stage_workspace_layout(10, 100, 128, 8, 2, arr) == 2     # D % 128

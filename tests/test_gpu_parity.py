@@ -189,7 +189,10 @@ def run_stage(qlib, g, k):
     lay = qlib.moe_expert_stage_workspace_layout(T, D, F, E, k)
     P = T * k
     view = lambda name, dt, shape: qlib.workspace_view(ws, lay, name, dt, shape).cpu().numpy()  # noqa: E731
-    return dict(Y=Y.cpu().numpy(), Hq=view("Hq", torch.int8, (P, F)), Hd=view("Hd", torch.int16, (P, F // 32)),
+    # the q8_1 codes are held as f16; every one must be an integer in [-127, 127]
+    hq16 = view("Hq", torch.float16, (P, F)).astype(np.float64)
+    assert np.all(hq16 == np.round(hq16)) and np.all(np.abs(hq16) <= 127)
+    return dict(Y=Y.cpu().numpy(), Hq=hq16.astype(np.int8), Hd=view("Hd", torch.int16, (P, F // 32)),
                 Yslot=view("Yslot", torch.float32, (P, D)), row=view("row", torch.int32, (T, k)),
                 src=view("src", torch.int32, (P,)), offsets=view("offsets", torch.int32, (E + 1,)))
 
