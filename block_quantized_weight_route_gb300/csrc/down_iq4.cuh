@@ -97,22 +97,6 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t saddr) {
     return v;
 }
 
-__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
 // p.K = F (reduction), p.N = D (weight rows per expert), p.n_tiles = D / 128,
 // p.tiles / num_entries / max_entries: the 128-token tile list of the routing,
 // p.dW: IQ4_NL scales [E][D][F/32] fp16, p.dH32: d_H fp32 [entry][F/32][128],
@@ -318,9 +302,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t sbase = smem_u32(sstage + ss * C::SSTAGE_BYTES);
             const uint32_t dh_base = sbase + cq * C::CPW * 4;
             const uint32_t dw_addr = sbase + C::DH_BYTES + (uint32_t)(r * groups * 2);
-            uint64_t y[C::CPW / 2];                               // CPW token columns as f32 pairs
+            // CPW token columns as f32 pairs (the packed f32x2 FMA path; the
+            // compiler keeps each pair in an aligned register pair)
+            float2 y[C::CPW / 2];
 #pragma unroll
-            for (int j = 0; j < C::CPW / 2; ++j) y[j] = 0ull;
+            for (int j = 0; j < C::CPW / 2; ++j) y[j] = make_float2(0.f, 0.f);
             for (int g = 0; g < groups; ++g) {
                 if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                     ok = false;
@@ -328,7 +314,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 tc_fence_after();
                 const float dwf = __half2float(__ushort_as_half((unsigned short)lds_u16(dw_addr + g * 2)));
-                const uint64_t dw2 = f32x2_pack(dwf, dwf);
+                const float2 dw2 = make_float2(dwf, dwf);
                 const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + cq * C::CPW);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
@@ -344,12 +330,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const uint4 dh = lds128(dh_base + (uint32_t)((g * C::BN + c * 32 + 4 * j) * 4));
-                        const uint64_t i01 = f32x2_pack(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
-                        const uint64_t i23 = f32x2_pack(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                        const uint64_t d01 = f32x2_pack(__uint_as_float(dh.x), __uint_as_float(dh.y));
-                        const uint64_t d23 = f32x2_pack(__uint_as_float(dh.z), __uint_as_float(dh.w));
-                        y[c * 16 + 2 * j] = f32x2_fma(f32x2_mul(i01, d01), dw2, y[c * 16 + 2 * j]);
-                        y[c * 16 + 2 * j + 1] = f32x2_fma(f32x2_mul(i23, d23), dw2, y[c * 16 + 2 * j + 1]);
+                        const float2 i01 = make_float2(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
+                        const float2 i23 = make_float2(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                        const float2 d01 = make_float2(__uint_as_float(dh.x), __uint_as_float(dh.y));
+                        const float2 d23 = make_float2(__uint_as_float(dh.z), __uint_as_float(dh.w));
+                        // y += (I * d_H) * d_W, both products rounded to fp32
+                        y[c * 16 + 2 * j] = __ffma2_rn(__fmul2_rn(i01, d01), dw2, y[c * 16 + 2 * j]);
+                        y[c * 16 + 2 * j + 1] = __ffma2_rn(__fmul2_rn(i23, d23), dw2, y[c * 16 + 2 * j + 1]);
                     }
                 }
                 if (++buf == C::NBUF) {
@@ -369,10 +356,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int tok0 = cq * C::CPW;
 #pragma unroll
             for (int j = 0; j < C::CPW / 2; ++j) {
-                float lo, hi;
-                asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(y[j]));
-                if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = lo;
-                if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = hi;
+                if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = y[j].x;
+                if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = y[j].y;
             }
             g4 = g4n;
         }
