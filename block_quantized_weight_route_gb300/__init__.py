@@ -63,6 +63,14 @@ def lib() -> ctypes.CDLL:
         L.qmm_profile_read.argtypes = [P]
         L.moe_expert_stage_w4_iq4.restype = i32
         L.moe_expert_stage_w4_iq4.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+        L.qmm_dbg_workspace_size.restype = sz
+        L.qmm_dbg_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.qmm_dbg_gate_up_q8_1.restype = i32
+        L.qmm_dbg_gate_up_q8_1.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+        L.qmm_dbg_down_iq4.restype = i32
+        L.qmm_dbg_down_iq4.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, sz, P]
+        L.qmm_dbg_combine.restype = i32
+        L.qmm_dbg_combine.argtypes = [P, i32, P, P, i32, i32, i32, P, P]
         _lib = L
     return _lib
 
@@ -197,6 +205,72 @@ def moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, k:
                                        _ptr(gu_scale2), _ptr(Wd_idx), _ptr(Wd_s), _ptr(Y), _ptr(ws), ws.numel(),
                                        _stream(dev))
     _check("moe_expert_stage_w4_iq4", st)
+    return Y
+
+
+def qmm_dbg_workspace_size(P: int, D: int, F: int, E: int) -> int:
+    return int(lib().qmm_dbg_workspace_size(P, D, F, E))
+
+
+def _dbg_ws(ws, P, D, F, E, dev):
+    if ws is None:
+        ws = torch.empty(max(qmm_dbg_workspace_size(P, D, F, E), 256), dtype=torch.uint8, device=dev)
+    return _need(ws, "ws", _U8)
+
+
+def qmm_dbg_gate_up_q8_1(X_perm, offsets, Wgu_c, Wgu_s, gu_scale2, ws=None):
+    """Gate/up + SwiGLU + q8_1 of expert-grouped rows X_perm [P, D] (expert e owns
+    rows offsets[e] .. offsets[e+1]-1).  Returns (Hq int8 [P, F], Hd, Hs fp16 bits
+    as int16 [P, F/32])."""
+    P, D = X_perm.shape
+    E, F2 = Wgu_c.shape[0], Wgu_c.shape[1]
+    F = F2 // 2
+    _need(X_perm, "X_perm", _BF16, (P, D))
+    _need(offsets, "offsets", (torch.int32,), (E + 1,))
+    _need(Wgu_c, "Wgu_c", _U8, (E, F2, D // 2))
+    _need(Wgu_s, "Wgu_s", _U8, (E, F2, D // 16))
+    _need(gu_scale2, "gu_scale2", (torch.float32,), (E,))
+    dev = X_perm.device
+    ws = _dbg_ws(ws, P, D, F, E, dev)
+    Hq = torch.empty((P, F), dtype=torch.int8, device=dev)
+    Hd = torch.empty((P, F // 32), dtype=torch.int16, device=dev)
+    Hs = torch.empty((P, F // 32), dtype=torch.int16, device=dev)
+    st = lib().qmm_dbg_gate_up_q8_1(_ptr(X_perm), _ptr(offsets), P, D, F, E, _ptr(Wgu_c), _ptr(Wgu_s),
+                                    _ptr(gu_scale2), _ptr(Hq), _ptr(Hd), _ptr(Hs), _ptr(ws), ws.numel(), _stream(dev))
+    _check("qmm_dbg_gate_up_q8_1", st)
+    return Hq, Hd, Hs
+
+
+def qmm_dbg_down_iq4(Hq, Hd, offsets, Wd_idx, Wd_s, ws=None):
+    """Down product of q8_1 rows (Hq int8 [P, F], Hd fp16 bits [P, F/32]) against
+    IQ4_NL weights, grouped by offsets.  Returns Yslot fp32 [P, D]."""
+    P, F = Hq.shape
+    E, D = Wd_idx.shape[0], Wd_idx.shape[1]
+    _need(Hq, "Hq", (torch.int8,), (P, F))
+    _need(Hd, "Hd", _F16, (P, F // 32))
+    _need(offsets, "offsets", (torch.int32,), (E + 1,))
+    _need(Wd_idx, "Wd_idx", _U8, (E, D, F // 2))
+    _need(Wd_s, "Wd_s", _F16, (E, D, F // 32))
+    dev = Hq.device
+    ws = _dbg_ws(ws, P, D, F, E, dev)
+    Yslot = torch.empty((P, D), dtype=torch.float32, device=dev)
+    st = lib().qmm_dbg_down_iq4(_ptr(Hq), _ptr(Hd), _ptr(offsets), P, D, F, E, _ptr(Wd_idx), _ptr(Wd_s),
+                                _ptr(Yslot), _ptr(ws), ws.numel(), _stream(dev))
+    _check("qmm_dbg_down_iq4", st)
+    return Yslot
+
+
+def qmm_dbg_combine(Yslot, row, w):
+    """Y[t] = sum_j w[t, j] * Yslot[row[t, j]] (j ascending).  Returns Y fp32 [T, D]."""
+    P, D = Yslot.shape
+    T, k = row.shape
+    _need(Yslot, "Yslot", (torch.float32,), (P, D))
+    _need(row, "row", (torch.int32,), (T, k))
+    _need(w, "w", (torch.float32,), (T, k))
+    dev = Yslot.device
+    Y = torch.empty((T, D), dtype=torch.float32, device=dev)
+    st = lib().qmm_dbg_combine(_ptr(Yslot), P, _ptr(row), _ptr(w), T, k, D, _ptr(Y), _stream(dev))
+    _check("qmm_dbg_combine", st)
     return Y
 
 

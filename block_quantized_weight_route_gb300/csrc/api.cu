@@ -7,6 +7,7 @@
 #include <string>
 
 #include "../../include/qmm.h"
+#include "ptx.cuh"
 #include "qmm_internal.h"
 
 namespace qmm {
@@ -184,6 +185,9 @@ qmm_status qmm_check_status(cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
     if (code != 0) {
         cudaMemset(d->err, 0, sizeof code);
+        if (code == DEV_BAD_OFFSETS)
+            return fail(QMM_ERR_INVALID_ARG, "expert offsets must satisfy 0 = o[0] <= ... <= o[E] = P (device check)");
+        if (code == DEV_BAD_ROW) return fail(QMM_ERR_INVALID_ARG, "combine row index outside [0, P) (device check)");
         return fail(QMM_ERR_TIMEOUT, "a kernel wait timed out (device code %u)", code);
     }
     return QMM_OK;
@@ -302,6 +306,74 @@ qmm_status moe_route_permute(const float* logits, int T, int E, int k, int32_t* 
     return QMM_OK;
 }
 
+// Gate/up + SwiGLU + q8_1 over permuted rows Xp [P][D], grouped by the 256-row
+// tile list: 256 token rows x (64 gate + 64 up weight rows) per tile, clusters
+// of CTAs sharing the token rows.  Writes Hq (f16 codes), Hd, Hs, Hd32.
+static qmm_status run_gate_up(DeviceState* d, const uint16_t* Xp, int P, int D, int F, int E, const uint8_t* Wgu_c,
+                              const uint8_t* Wgu_s, const float* gu_scale2, const int4* tiles2,
+                              const int32_t* num_entries2, int max_entries2, __half* Hq, __half* Hd, __half* Hs,
+                              float* Hd32, cudaStream_t stream) {
+    qmm_status st;
+    const int gu_cn = cluster_for(F / 64);
+    CUtensorMap ta, tb;
+    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, 256 / gu_cn,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
+        return st;
+    if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, 64,
+                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+        return st;
+    GemmParams g{};
+    g.K = D;
+    g.F = F;
+    g.n_tiles = F / 64;
+    g.n_step = 64;
+    g.tiles = tiles2;
+    g.num_entries = num_entries2;
+    g.max_entries = max_entries2;
+    g.w_scale = Wgu_s;
+    g.scale2 = gu_scale2;
+    g.Hq = Hq;
+    g.Hd = Hd;
+    g.Hs = Hs;
+    g.Hd32 = Hd32;
+    g.err = d->err;
+    cudaError_t e = launch_w4_gate_up_swiglu(ta, tb, g, gu_cn, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "expert stage: gate/up launch");
+    return QMM_OK;
+}
+
+// Down product Yslot [P][D] = IQ4_NL weights x q8_1 H (f16 codes Hq, fp32 d in
+// the per-128-row-entry layout Hd32), grouped by the 128-row tile list.
+static qmm_status run_down(DeviceState* d, const __half* Hq, const float* Hd32, int P, int D, int F, int E,
+                           const uint8_t* Wd_idx, const uint16_t* Wd_s, const int4* tiles, const int32_t* num_entries,
+                           int max_entries, float* Yslot, cudaStream_t stream) {
+    qmm_status st;
+    CUtensorMap ta, tb;
+    if ((st = make_tmap(&ta, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
+                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+        return st;
+    if ((st = make_tmap(&tb, Hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, F, P, (uint64_t)F * 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
+        return st;
+    GemmParams q{};
+    q.N = D;
+    q.K = F;
+    q.n_tiles = D / 128;
+    q.n_step = 128;
+    q.tiles = tiles;
+    q.num_entries = num_entries;
+    q.max_entries = max_entries;
+    q.dH32 = Hd32;
+    q.dW = reinterpret_cast<const __half*>(Wd_s);
+    q.Y = Yslot;
+    q.ydt = 0;
+    q.ldy = D;
+    q.err = d->err;
+    cudaError_t e = launch_iq4_down(ta, tb, q, d->sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "expert stage: down launch");
+    return QMM_OK;
+}
+
 static qmm_status check_stage_shape(int T, int D, int F, int E, int k) {
     qmm_status st = check_route_shape("moe_expert_stage_w4_iq4", T, E, k);
     if (st != QMM_OK) return st;
@@ -373,64 +445,130 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     float* Yslot = static_cast<float*>(at(16));
 
     // gate/up + SwiGLU + q8_1
-    // 256 token rows x (64 gate + 64 up weight rows) per tile; clusters share the rows
-    const int gu_cn = cluster_for(F / 64);
-    CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, 256 / gu_cn,
-                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
+    if ((st = run_gate_up(d, Xp, P, D, F, E, Wgu_c, Wgu_s, gu_scale2, rb.tiles2, rb.num_entries2, max_entries2, Hq, Hd,
+                          Hs, Hd32, stream)) != QMM_OK)
         return st;
-    if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, 64,
-                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
-        return st;
-    GemmParams g{};
-    g.K = D;
-    g.F = F;
-    g.n_tiles = F / 64;
-    g.n_step = 64;
-    g.tiles = rb.tiles2;
-    g.num_entries = rb.num_entries2;
-    g.max_entries = max_entries2;
-    g.w_scale = Wgu_s;
-    g.scale2 = gu_scale2;
-    g.Hq = Hq;
-    g.Hd = Hd;
-    g.Hs = Hs;
-    g.Hd32 = Hd32;
-    g.err = d->err;
-    e = launch_w4_gate_up_swiglu(ta, tb, g, gu_cn, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "expert stage: gate/up launch");
     if ((e = mark(d, 3, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
     // down (IQ4_NL weights on the MMA's M side, q8_1 H codes on its N side)
-    CUtensorMap ta2, tb2;
-    if ((st = make_tmap(&ta2, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
-                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+    if ((st = run_down(d, Hq, Hd32, P, D, F, E, Wd_idx, Wd_s, rb.tiles, rb.num_entries, max_entries, Yslot, stream)) !=
+        QMM_OK)
         return st;
-    if ((st = make_tmap(&tb2, Hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, F, P, (uint64_t)F * 2, 64, 128,
-                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
-        return st;
-    GemmParams q{};
-    q.N = D;
-    q.K = F;
-    q.n_tiles = D / 128;
-    q.n_step = 128;
-    q.tiles = rb.tiles;
-    q.num_entries = rb.num_entries;
-    q.max_entries = max_entries;
-    q.dH32 = Hd32;
-    q.dW = reinterpret_cast<const __half*>(Wd_s);
-    q.Y = Yslot;
-    q.ydt = 0;
-    q.ldy = D;
-    q.err = d->err;
-    e = launch_iq4_down(ta2, tb2, q, d->sms, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "expert stage: down launch");
     if ((e = mark(d, 4, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
-    e = launch_combine(Yslot, rb.row, rb.w, T, k, D, Y, stream);
+    e = launch_combine(Yslot, P, rb.row, rb.w, T, k, D, Y, d->err, stream);
     if (e != cudaSuccess) return cuda_fail(e, "expert stage: combine");
     if ((e = mark(d, 5, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
     return QMM_OK;
+}
+
+// ---------------------------------------------------------------- sub-step entry points
+
+// Workspace of the qmm_dbg_* calls: 128-row tile list + count, 256-row tile list
+// + count, f16 H codes [P][F], fp32 d of H per 128-row entry.
+static void dbg_layout(int P, int F, int E, size_t* off) {
+    const int me = (P + 127) / 128 + E, me2 = (P + 255) / 256 + E;
+    const size_t sz[6] = {(size_t)me * 16, 16, (size_t)me2 * 16, 16, (size_t)P * F * 2,
+                          (size_t)me * (F / 32) * 128 * 4};
+    size_t o = 0;
+    for (int i = 0; i < 6; ++i) {
+        off[i] = o;
+        o = align_up(o + sz[i], 256);
+    }
+    off[6] = o;
+}
+
+size_t qmm_dbg_workspace_size(int P, int D, int F, int E) {
+    if (P < 0 || D < 0 || F < 32 || E < 1) return 0;
+    size_t off[7];
+    dbg_layout(P, F, E, off);
+    return off[6];
+}
+
+static qmm_status dbg_common(const char* who, int P, int D, int F, int E, const void* const* bufs, int nbufs,
+                             void* ws, size_t ws_bytes, DeviceState** d) {
+    if (P < 0 || E < 1 || E > 512 || D < 128 || D % 128 || F < 128 || F % 128 || F > 1024)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE, "%s: need P >= 0, 1 <= E <= 512, D %% 128 == 0, F %% 128 == 0, F <= 1024",
+                    who);
+    for (int i = 0; i < nbufs; ++i) {
+        if (!bufs[i] && P > 0) return fail(QMM_ERR_INVALID_ARG, "%s: null pointer", who);
+        if (!aligned16(bufs[i])) return fail(QMM_ERR_INVALID_ARG, "%s: buffers must be 16-byte aligned", who);
+    }
+    if (P > 0 && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+        return fail(QMM_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+    const size_t need = qmm_dbg_workspace_size(P, D, F, E);
+    if (ws_bytes < need) return fail(QMM_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", who, ws_bytes, need);
+    return device_state(d);
+}
+
+// Tile lists from the caller's offsets into the dbg workspace.
+static qmm_status dbg_tiles(DeviceState* d, const int32_t* offsets, int P, int E, uint8_t* base, const size_t* off,
+                            RouteBufs* rb, cudaStream_t stream) {
+    *rb = RouteBufs{};
+    rb->tiles = reinterpret_cast<int4*>(base + off[0]);
+    rb->num_entries = reinterpret_cast<int32_t*>(base + off[1]);
+    rb->max_entries = (P + 127) / 128 + E;
+    rb->tiles2 = reinterpret_cast<int4*>(base + off[2]);
+    rb->num_entries2 = reinterpret_cast<int32_t*>(base + off[3]);
+    rb->max_entries2 = (P + 255) / 256 + E;
+    cudaError_t e = launch_tiles_from_offsets(offsets, E, P, d->err, *rb, stream);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "tile lists from offsets");
+}
+
+qmm_status qmm_dbg_gate_up_q8_1(const uint16_t* X_perm, const int32_t* offsets, int P, int D, int F, int E,
+                                const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2, int8_t* Hq,
+                                uint16_t* Hd, uint16_t* Hs, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const void* bufs[] = {X_perm, offsets, Wgu_c, Wgu_s, gu_scale2, Hq, Hd, Hs};
+    DeviceState* d = nullptr;
+    qmm_status st = dbg_common("qmm_dbg_gate_up_q8_1", P, D, F, E, bufs, 8, ws, ws_bytes, &d);
+    if (st != QMM_OK || P == 0) return st;
+    size_t off[7];
+    dbg_layout(P, F, E, off);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    RouteBufs rb;
+    if ((st = dbg_tiles(d, offsets, P, E, base, off, &rb, stream)) != QMM_OK) return st;
+    __half* Hq16 = reinterpret_cast<__half*>(base + off[4]);
+    float* Hd32 = reinterpret_cast<float*>(base + off[5]);
+    if ((st = run_gate_up(d, X_perm, P, D, F, E, Wgu_c, Wgu_s, gu_scale2, rb.tiles2, rb.num_entries2, rb.max_entries2,
+                          Hq16, reinterpret_cast<__half*>(Hd), reinterpret_cast<__half*>(Hs), Hd32, stream)) != QMM_OK)
+        return st;
+    cudaError_t e = launch_codes_f16_to_i8(Hq16, Hq, (long)P * F, stream);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "qmm_dbg_gate_up_q8_1: code conversion");
+}
+
+qmm_status qmm_dbg_down_iq4(const int8_t* Hq, const uint16_t* Hd, const int32_t* offsets, int P, int D, int F, int E,
+                            const uint8_t* Wd_idx, const uint16_t* Wd_s, float* Yslot, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+    const void* bufs[] = {Hq, Hd, offsets, Wd_idx, Wd_s, Yslot};
+    DeviceState* d = nullptr;
+    qmm_status st = dbg_common("qmm_dbg_down_iq4", P, D, F, E, bufs, 6, ws, ws_bytes, &d);
+    if (st != QMM_OK || P == 0) return st;
+    size_t off[7];
+    dbg_layout(P, F, E, off);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    RouteBufs rb;
+    if ((st = dbg_tiles(d, offsets, P, E, base, off, &rb, stream)) != QMM_OK) return st;
+    __half* Hq16 = reinterpret_cast<__half*>(base + off[4]);
+    float* Hd32 = reinterpret_cast<float*>(base + off[5]);
+    cudaError_t e = launch_codes_i8_to_f16(Hq, Hq16, (long)P * F, stream);
+    if (e == cudaSuccess)
+        e = launch_hd_to_entries(reinterpret_cast<const __half*>(Hd), rb.tiles, rb.num_entries, rb.max_entries, F / 32,
+                                 Hd32, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_dbg_down_iq4: operand layout");
+    return run_down(d, Hq16, Hd32, P, D, F, E, Wd_idx, Wd_s, rb.tiles, rb.num_entries, rb.max_entries, Yslot, stream);
+}
+
+qmm_status qmm_dbg_combine(const float* Yslot, int P, const int32_t* row, const float* w, int T, int k, int D,
+                           float* Y, cudaStream_t stream) {
+    if (T < 0 || P < 0 || k < 1 || k > 16 || D < 4 || D % 4)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE, "qmm_dbg_combine: need T, P >= 0, 1 <= k <= 16, D %% 4 == 0");
+    if (T > 0 && (!Yslot || !row || !w || !Y)) return fail(QMM_ERR_INVALID_ARG, "qmm_dbg_combine: null pointer");
+    if (!aligned16(Yslot) || !aligned16(Y)) return fail(QMM_ERR_INVALID_ARG, "qmm_dbg_combine: Yslot, Y 16-byte aligned");
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK || T == 0) return st;
+    cudaError_t e = launch_combine(Yslot, P, row, w, T, k, D, Y, d->err, stream);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "qmm_dbg_combine launch");
 }
 
 qmm_status qmm_profile_enable(int on) {

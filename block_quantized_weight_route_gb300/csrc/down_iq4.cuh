@@ -24,16 +24,22 @@
 // conversion; only the IQ4 indices are expanded (codebook lookup) to f16.
 //
 //   warp 0: TMA producer (IQ4 codes + f16 H codes per K block, d_H and d_W per tile)
-//   warp 1: TMEM owner and MMA issuer
+//   warp 2: MMA issuer
 //   warps 4 .. 4+EPI_WARPS-1: epilogue (EPI_WARPS/4 per TMEM lane quarter)
-//   warps 2, 3 (and with four converters two more after the epilogue, on
-//   sub-partitions 0 and 2): IQ4 converters; none shares sub-partition 1 with
-//   the MMA issuer
+//   warps 1, 3 (and with four converters two more after the epilogue, on
+//   sub-partitions 0 and 2): IQ4 converters; warp 1 also allocates TMEM.
+// A warp's SM sub-partition is its index mod 4, the same as the TMEM lane
+// quarter it may read, so every sub-partition holds EPI_WARPS/4 epilogue warps
+// and one of the producer, a converter or the MMA issuer.  The producer and
+// the MMA issuer run on one lane each.
 #pragma once
 #include "qgemm.cuh"
 
 namespace qmm {
 
+#ifndef QMM_DOWN_CSTAGES
+#define QMM_DOWN_CSTAGES 3
+#endif
 template <int EPI_WARPS_, int CONV_WARPS_, int TSTAGES_>
 struct DownCfgT {
     static constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16, GROUP_K = 32;
@@ -43,8 +49,9 @@ struct DownCfgT {
     static constexpr int W2 = EPI_BASE + EPI_WARPS;           // first warp after the epilogue (sub-partition 0)
     static constexpr int THREADS = 32 * (CONV_WARPS == 2 ? W2 : W2 + 3);
     static constexpr int CONV_THREADS = 32 * CONV_WARPS;
+    static constexpr int MMA_WARP = 2;                        // sub-partition 2; TMEM is allocated by warp 1
     __device__ static int conv_slot(int warp) {
-        if (warp == 2) return 0;
+        if (warp == 1) return 0;
         if (warp == 3) return 1;
         if (CONV_WARPS == 4) {
             if (warp == W2) return 2;
@@ -54,7 +61,7 @@ struct DownCfgT {
     }
     static_assert(EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue width");
     static_assert(CONV_WARPS == 2 || CONV_WARPS == 4, "converter count");
-    static constexpr int TSTAGES = TSTAGES_, CSTAGES = 3, SSTAGES = 2, NBUF = 4;
+    static constexpr int TSTAGES = TSTAGES_, CSTAGES = QMM_DOWN_CSTAGES, SSTAGES = 2, NBUF = 4;
     static constexpr int KG_MAX = 32;                         // K <= 1024
     static constexpr int A_RAW_BYTES = BM * 32;               // IQ4 codes: 64 indices per row
     static constexpr int B_BYTES = BN * BK * 2;               // f16 H codes, 128-byte rows
@@ -163,8 +170,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int num_tiles = entries * p.n_tiles;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        {
+        // ------------------------------------------------------------ producer (one lane)
+        if (lane == 0) {
             int s = 0, ss = 0;
             uint32_t ph = 0, sph = 0;
             long issued = 0, s_issued = 0;
@@ -176,33 +183,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int n0 = (t - entry * p.n_tiles) * C::BM;
                 const int4 g = p.tiles[entry];
                 // this tile's d_H and d_W values
-                const bool sfree = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
-                if (__any_sync(0xffffffffu, !sfree)) break;
-                if (elect_one_sync()) {
-                    uint8_t* st = sstage + ss * C::SSTAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_s[ss], dh_bytes + dw_bytes);
-                    bulk_load(st, p.dH32 + (long)entry * groups * C::BN, dh_bytes, &full_s[ss]);
-                    bulk_load(st + C::DH_BYTES, p.dW + ((long)g.x * p.N + n0) * groups, dw_bytes, &full_s[ss]);
-                }
-                __syncwarp();
+                if (!mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) break;
+                uint8_t* sst = sstage + ss * C::SSTAGE_BYTES;
+                mbar_arrive_expect_tx(&full_s[ss], dh_bytes + dw_bytes);
+                bulk_load(sst, p.dH32 + (long)entry * groups * C::BN, dh_bytes, &full_s[ss]);
+                bulk_load(sst + C::DH_BYTES, p.dW + ((long)g.x * p.N + n0) * groups, dw_bytes, &full_s[ss]);
                 ++s_issued;
                 if (++ss == C::SSTAGES) {
                     ss = 0;
                     sph ^= 1u;
                 }
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
-                    if (__any_sync(0xffffffffu, !got)) {
+                    if (!mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    if (elect_one_sync()) {
-                        uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                        mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
-                        tma_load_2d(st, &tmA, &full_t[s], kb * 32, g.x * p.N + n0);
-                        tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
-                    }
-                    __syncwarp();
+                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                    mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                    tma_load_2d(st, &tmA, &full_t[s], kb * 32, g.x * p.N + n0);
+                    tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
                     ++issued;
                     if (++s == C::TSTAGES) {
                         s = 0;
@@ -210,14 +209,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
             }
-            if (lane == 0) {
-                drain_ring(full_t, issued, C::TSTAGES, p.err);
-                drain_ring(full_s, s_issued, C::SSTAGES, p.err);
-            }
+            drain_ring(full_t, issued, C::TSTAGES, p.err);
+            drain_ring(full_s, s_issued, C::SSTAGES, p.err);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        {
+        __syncwarp();
+    } else if (warp == C::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issuer (one lane)
+        // A single thread runs the whole issue loop: no per-MMA election or warp
+        // votes, so each K block costs a few dozen instructions on this warp.
+        if (lane == 0) {
             int cs = 0, ts = 0, buf = 0;
             uint32_t cph = 0, tph = 0, bph = 0;
             bool ok = true;
@@ -225,9 +225,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
                     // expanded weights ready (the converters saw the TMA stage complete);
                     // the H codes of the same stage are waited on directly
-                    const bool got = mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV) &&
-                                     mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL);
-                    if (__any_sync(0xffffffffu, !got)) {
+                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV) ||
+                        !mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL)) {
                         ok = false;
                         break;
                     }
@@ -236,38 +235,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const uint32_t a_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
                     const uint32_t b_base = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-                        const bool first = (kk & 1) == 0, last = (kk & 1) == 1;
-                        if (first) {
-                            const bool free = mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err,
-                                                        DEV_TIMEOUT_ACC_EMPTY);
-                            if (__any_sync(0xffffffffu, !free)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
+                    for (int h = 0; h < C::BK / C::GROUP_K; ++h) {
+                        // one 32-K block: two K=16 MMAs into its own accumulator
+                        if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                            ok = false;
+                            break;
                         }
-                        const uint64_t adesc = smem_desc_sw128(a_base + kk * 32);
-                        const uint64_t bdesc = smem_desc_sw128(b_base + kk * 32);
+                        tc_fence_after();
                         const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::BN);
-                        if (elect_one_sync()) {
-                            tc_mma_f16(dtmem, adesc, bdesc, C::IDESC, first ? 0u : 1u);
-                            if (last) tc_commit(&acc_full[buf]);
-                        }
-                        __syncwarp();
-                        if (last) {
-                            if (++buf == C::NBUF) {
-                                buf = 0;
-                                bph ^= 1u;
-                            }
+                        const uint32_t off = (uint32_t)(h * C::GROUP_K * 2);
+                        tc_mma_f16(dtmem, smem_desc_sw128(a_base + off), smem_desc_sw128(b_base + off), C::IDESC, 0u);
+                        tc_mma_f16(dtmem, smem_desc_sw128(a_base + off + 32), smem_desc_sw128(b_base + off + 32),
+                                   C::IDESC, 1u);
+                        tc_commit(&acc_full[buf]);
+                        if (++buf == C::NBUF) {
+                            buf = 0;
+                            bph ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    if (elect_one_sync()) {
-                        tc_commit(&empty_c[cs]);
-                        tc_commit(&empty_t[ts]);
-                    }
-                    __syncwarp();
+                    tc_commit(&empty_c[cs]);
+                    tc_commit(&empty_t[ts]);
                     if (++cs == C::CSTAGES) {
                         cs = 0;
                         cph ^= 1u;
@@ -278,10 +266,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
             }
-            if (elect_one_sync()) tc_commit(drain_bar);
-            __syncwarp();
-            if (lane == 0) drain_ring(drain_bar, 1, 1, p.err);
+            tc_commit(drain_bar);
+            drain_ring(drain_bar, 1, 1, p.err);
         }
+        __syncwarp();
     } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;

@@ -20,6 +20,8 @@ enum : uint32_t {
     DEV_TIMEOUT_ACC_EMPTY = 6,   // MMA waited too long for the epilogue
     DEV_TIMEOUT_DRAIN = 7,       // teardown waited too long for copies or MMAs
     DEV_BAD_TILE = 8,            // a tile descriptor pointed outside its buffers
+    DEV_BAD_OFFSETS = 9,         // caller-given expert offsets not 0 <= ... <= P (sub-step calls)
+    DEV_BAD_ROW = 10,            // a combine row index outside [0, P) (sub-step calls)
 };
 
 // A wait gives up after this many nanoseconds of wall-clock time.

@@ -68,8 +68,14 @@ struct RouteBufs {
 constexpr int kRouteChunk = 256;   // tokens per grouping chunk
 cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBufs& b, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* X, const int32_t* src, int rows, int D, uint16_t* Xp, cudaStream_t s);
-cudaError_t launch_combine(const float* Yslot, const int32_t* row, const float* w, int T, int k, int D, float* Y,
-                           cudaStream_t s);
+cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int E, int P, uint32_t* err, const RouteBufs& b,
+                                      cudaStream_t s);
+cudaError_t launch_codes_f16_to_i8(const __half* src, int8_t* dst, long n, cudaStream_t s);
+cudaError_t launch_codes_i8_to_f16(const int8_t* src, __half* dst, long n, cudaStream_t s);
+cudaError_t launch_hd_to_entries(const __half* Hd, const int4* tiles, const int32_t* num_entries, int max_entries,
+                                 int groups, float* Hd32, cudaStream_t s);
+cudaError_t launch_combine(const float* Yslot, int P, const int32_t* row, const float* w, int T, int k, int D,
+                           float* Y, uint32_t* err, cudaStream_t s);
 
 // Set the calling thread's message returned by qmm_last_error().
 void set_last_error(const char* msg);

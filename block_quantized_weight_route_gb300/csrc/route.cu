@@ -14,6 +14,7 @@
 #include <cfloat>
 #include <climits>
 
+#include "ptx.cuh"
 #include "qmm_internal.h"
 
 namespace qmm {
@@ -125,10 +126,36 @@ __device__ int block_exclusive_scan(int v, int* total) {
     return base + x - v;
 }
 
-// One CTA of 1024 threads (E <= 1024): per-expert counts and the exclusive
-// per-chunk bases (in place in chunk_hist), offsets, and the tile lists:
+// Tile lists of the grouped GEMMs, for expert e = threadIdx.x with `cnt` rows
+// starting at row `off` (every thread of the 1024-thread block calls this):
 // 128-row entries {expert, first row, rows, 0} and 256-row entries
 // {expert, first row, rows, index of its first 128-row entry}.
+__device__ void build_tile_lists(int E, int cnt, int off, int4* __restrict__ tiles, int32_t* __restrict__ num_entries,
+                                 int max_entries, int4* __restrict__ tiles2, int32_t* __restrict__ num_entries2,
+                                 int max_entries2) {
+    const int e = threadIdx.x;
+    const int mt = (e < E) ? (cnt + 127) / 128 : 0;
+    int ntiles;
+    const int tbase = block_exclusive_scan(mt, &ntiles);
+    for (int i = 0; i < mt; ++i) {
+        const int idx = tbase + i;
+        if (idx < max_entries) tiles[idx] = make_int4(e, off + 128 * i, min(128, cnt - 128 * i), 0);
+    }
+    if (e == 0) *num_entries = min(ntiles, max_entries);
+    if (tiles2) {
+        const int mt2 = (e < E) ? (cnt + 255) / 256 : 0;
+        int ntiles2;
+        const int tbase2 = block_exclusive_scan(mt2, &ntiles2);
+        for (int i = 0; i < mt2; ++i) {
+            const int idx = tbase2 + i;
+            if (idx < max_entries2) tiles2[idx] = make_int4(e, off + 256 * i, min(256, cnt - 256 * i), tbase + 2 * i);
+        }
+        if (e == 0) *num_entries2 = min(ntiles2, max_entries2);
+    }
+}
+
+// One CTA of 1024 threads (E <= 1024): per-expert counts and the exclusive
+// per-chunk bases (in place in chunk_hist), offsets, and the tile lists.
 __global__ void __launch_bounds__(1024) route_scan_kernel(int chunks, int E, int32_t* __restrict__ chunk_hist,
                                                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                           int4* __restrict__ tiles, int32_t* __restrict__ num_entries,
@@ -148,27 +175,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int chunks, int E, int
     const int off = block_exclusive_scan(e < E ? cnt : 0, &total);
     if (e < E) offsets[e] = off;
     if (e == 0) offsets[E] = total;
-    if (tiles) {
-        const int mt = (e < E) ? (cnt + 127) / 128 : 0;
-        int ntiles;
-        const int tbase = block_exclusive_scan(mt, &ntiles);
-        for (int i = 0; i < mt; ++i) {
-            const int idx = tbase + i;
-            if (idx < max_entries) tiles[idx] = make_int4(e, off + 128 * i, min(128, cnt - 128 * i), 0);
-        }
-        if (e == 0) *num_entries = min(ntiles, max_entries);
-        if (tiles2) {
-            const int mt2 = (e < E) ? (cnt + 255) / 256 : 0;
-            int ntiles2;
-            const int tbase2 = block_exclusive_scan(mt2, &ntiles2);
-            for (int i = 0; i < mt2; ++i) {
-                const int idx = tbase2 + i;
-                if (idx < max_entries2)
-                    tiles2[idx] = make_int4(e, off + 256 * i, min(256, cnt - 256 * i), tbase + 2 * i);
-            }
-            if (e == 0) *num_entries2 = min(ntiles2, max_entries2);
-        }
-    }
+    if (tiles) build_tile_lists(E, cnt, off, tiles, num_entries, max_entries, tiles2, num_entries2, max_entries2);
 }
 
 // One CTA per chunk (blockDim == kRouteChunk, one token per thread): the rank of
@@ -262,9 +269,11 @@ cudaError_t launch_gather_rows(const uint16_t* X, const int32_t* src, int rows, 
 }
 
 // Y[t, :] = sum_j w[t, j] * Yslot[row[t, j], :], j ascending; one warp per token.
-__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ Yslot, const int32_t* __restrict__ row,
-                                                      const float* __restrict__ w, int T, int k, int vec_per_row,
-                                                      float4* __restrict__ Y) {
+// A row index outside [0, P) contributes nothing and raises DEV_BAD_ROW.
+__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ Yslot, int P,
+                                                      const int32_t* __restrict__ row, const float* __restrict__ w,
+                                                      int T, int k, int vec_per_row, float4* __restrict__ Y,
+                                                      uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
@@ -275,6 +284,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
             if (j < k) {
                 rr[j] = __ldg(row + (long)t * k + j);
                 ww[j] = __ldg(w + (long)t * k + j);
+                if (rr[j] < 0 || rr[j] >= P) {
+                    if (lane == 0) atomicCAS(err, 0u, (uint32_t)DEV_BAD_ROW);
+                    rr[j] = 0;
+                    ww[j] = 0.f;
+                }
             }
         }
         for (int i = lane; i < vec_per_row; i += 32) {
@@ -294,16 +308,125 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
     }
 }
 
-cudaError_t launch_combine(const float* Yslot, const int32_t* row, const float* w, int T, int k, int D, float* Y,
-                           cudaStream_t s) {
+cudaError_t launch_combine(const float* Yslot, int P, const int32_t* row, const float* w, int T, int k, int D,
+                           float* Y, uint32_t* err, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     int sms = 148;
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = min((T + 7) / 8, sms * 8);
-    combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(Yslot), row, w, T, k, D / 4,
-                                        reinterpret_cast<float4*>(Y));
+    combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(Yslot), P, row, w, T, k, D / 4,
+                                        reinterpret_cast<float4*>(Y), err);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- sub-step entry points
+// (the qmm_dbg_* calls run one step of the expert stage on caller buffers)
+
+// Tile lists from caller-given expert offsets [E+1] (one CTA of 1024 threads).
+// Offsets that are not 0 = o[0] <= o[1] <= ... <= o[E] = P give empty lists and
+// raise DEV_BAD_OFFSETS in the device error word.
+__global__ void __launch_bounds__(1024) tiles_from_offsets_kernel(const int32_t* __restrict__ offsets, int E, int P,
+                                                                  uint32_t* err, int4* __restrict__ tiles,
+                                                                  int32_t* __restrict__ num_entries, int max_entries,
+                                                                  int4* __restrict__ tiles2,
+                                                                  int32_t* __restrict__ num_entries2, int max_entries2) {
+    const int e = threadIdx.x;
+    int off = 0, cnt = 0;
+    bool bad = false;
+    if (e < E) {
+        off = offsets[e];
+        const int next = offsets[e + 1];
+        bad = off < 0 || next < off || next > P;
+        cnt = bad ? 0 : next - off;
+    }
+    if (e == 0) bad = bad || offsets[0] != 0 || offsets[E] != P;
+    if (__syncthreads_or(bad)) {
+        if (e == 0) {
+            atomicCAS(err, 0u, (uint32_t)DEV_BAD_OFFSETS);
+            *num_entries = 0;
+            *num_entries2 = 0;
+        }
+        return;
+    }
+    build_tile_lists(E, cnt, off, tiles, num_entries, max_entries, tiles2, num_entries2, max_entries2);
+}
+
+// q8_1 codes: f16 (exact integers) <-> int8, 8 per thread (n8 = P * F / 8).
+__global__ void __launch_bounds__(256) codes_f16_to_i8_kernel(const uint4* __restrict__ src, uint2* __restrict__ dst,
+                                                             long n8) {
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
+        const int lo = (int)__low2float(h), hi = (int)__high2float(h);
+        o[j >> 1] |= (((uint32_t)lo & 0xFFu) | (((uint32_t)hi & 0xFFu) << 8)) << (16 * (j & 1));
+    }
+    dst[i] = make_uint2(o[0], o[1]);
+}
+
+__global__ void __launch_bounds__(256) codes_i8_to_f16_kernel(const uint2* __restrict__ src, uint4* __restrict__ dst,
+                                                             long n8) {
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const uint2 v = src[i];
+    const uint32_t w[2] = {v.x, v.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t b = w[j >> 1] >> (16 * (j & 1));
+        const __half2 h = __floats2half2_rn((float)(int8_t)(b & 0xFFu), (float)(int8_t)((b >> 8) & 0xFFu));
+        o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// fp32 d of H in the per-128-row-entry layout [entry][F/32][128] the down kernel
+// reads (rows past an entry's end are 0); one CTA per entry.
+__global__ void __launch_bounds__(256) hd_to_entries_kernel(const __half* __restrict__ Hd, const int4* __restrict__ tiles,
+                                                           const int32_t* __restrict__ num_entries, int groups,
+                                                           float* __restrict__ Hd32) {
+    const int entry = blockIdx.x;
+    if (entry >= *num_entries) return;
+    const int4 t = tiles[entry];
+    for (int i = threadIdx.x; i < groups * 128; i += blockDim.x) {
+        const int b = i >> 7, r = i & 127;
+        Hd32[(long)entry * groups * 128 + i] = r < t.z ? __half2float(Hd[((long)t.y + r) * groups + b]) : 0.f;
+    }
+}
+
+cudaError_t launch_tiles_from_offsets(const int32_t* offsets, int E, int P, uint32_t* err, const RouteBufs& b,
+                                      cudaStream_t s) {
+    tiles_from_offsets_kernel<<<1, 1024, 0, s>>>(offsets, E, P, err, b.tiles, b.num_entries, b.max_entries, b.tiles2,
+                                                 b.num_entries2, b.max_entries2);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_codes_f16_to_i8(const __half* src, int8_t* dst, long n, cudaStream_t s) {
+    const long n8 = n / 8;
+    if (n8 == 0) return cudaSuccess;
+    codes_f16_to_i8_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(src),
+                                                                       reinterpret_cast<uint2*>(dst), n8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_codes_i8_to_f16(const int8_t* src, __half* dst, long n, cudaStream_t s) {
+    const long n8 = n / 8;
+    if (n8 == 0) return cudaSuccess;
+    codes_i8_to_f16_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(reinterpret_cast<const uint2*>(src),
+                                                                       reinterpret_cast<uint4*>(dst), n8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_hd_to_entries(const __half* Hd, const int4* tiles, const int32_t* num_entries, int max_entries,
+                                 int groups, float* Hd32, cudaStream_t s) {
+    if (max_entries == 0) return cudaSuccess;
+    hd_to_entries_kernel<<<max_entries, 256, 0, s>>>(Hd, tiles, num_entries, groups, Hd32);
     return cudaGetLastError();
 }
 

@@ -143,6 +143,39 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t *X, const float *logits, int T
 qmm_status moe_expert_stage_workspace_layout(int T, int D, int F, int E, int k, size_t *offsets_out);
 
 /*
+ * Sub-steps of moe_expert_stage_w4_iq4 on caller-provided buffers, one step per
+ * call, so that each can be checked on its own inputs (same kernels as the
+ * stage).  P routed rows, grouped by expert: rows offsets[e] .. offsets[e+1]-1
+ * belong to expert e (offsets [E+1] int32 on the device, 0 = offsets[0] <= ...
+ * <= offsets[E] = P; other offsets compute nothing and make qmm_check_status
+ * return QMM_ERR_INVALID_ARG).  All pointers are device pointers owned by the
+ * caller; ws is device scratch of at least qmm_dbg_workspace_size(P, D, F, E)
+ * bytes, 256-byte aligned; other buffers 16-byte aligned.
+ * Shapes: P >= 0, 1 <= E <= 512, D % 128 == 0, F % 128 == 0, F <= 1024.
+ *
+ * qmm_dbg_gate_up_q8_1 -- the gate/up product, SwiGLU and the q8_1 rounding of H
+ * ("Run Edge0-145B Q3_K on AMD HIP (Linux, gfx1100)", commit 4cb5224):
+ *   for row r of expert e: g, u, h as in moe_expert_stage_w4_iq4 with
+ *   X[t] replaced by X_perm[r]; Hq [P][F] int8 codes, Hd, Hs [P][F/32] fp16.
+ * qmm_dbg_down_iq4 -- the down product over IQ4_NL weights (same page):
+ *   Yslot[r][n] = sum_b d_H[r][b] * d_W[e][n][b] * sum_{k in b} Hq[r][k] * CB[idx[e][n][k]]
+ *   Hq [P][F] int8, Hd [P][F/32] fp16, Yslot [P][D] fp32.
+ * qmm_dbg_combine -- the weighted combine: Y[t] = sum_j w[t][j] * Yslot[row[t][j]]
+ *   (j ascending); Yslot [P][D] fp32, row/w [T][k], Y [T][D] fp32.  A row index
+ *   outside [0, P) adds nothing and makes qmm_check_status return
+ *   QMM_ERR_INVALID_ARG.  Shapes: 1 <= k <= 16, D % 4 == 0.
+ */
+size_t qmm_dbg_workspace_size(int P, int D, int F, int E);
+qmm_status qmm_dbg_gate_up_q8_1(const uint16_t *X_perm, const int32_t *offsets, int P, int D, int F, int E,
+                                const uint8_t *Wgu_c, const uint8_t *Wgu_s, const float *gu_scale2, int8_t *Hq,
+                                uint16_t *Hd, uint16_t *Hs, void *ws, size_t ws_bytes, cudaStream_t stream);
+qmm_status qmm_dbg_down_iq4(const int8_t *Hq, const uint16_t *Hd, const int32_t *offsets, int P, int D, int F, int E,
+                            const uint8_t *Wd_idx, const uint16_t *Wd_s, float *Yslot, void *ws, size_t ws_bytes,
+                            cudaStream_t stream);
+qmm_status qmm_dbg_combine(const float *Yslot, int P, const int32_t *row, const float *w, int T, int k, int D, float *Y,
+                           cudaStream_t stream);
+
+/*
  * moe_route_permute_noalloc -- moe_route_permute for callers that cannot
  * allocate device memory (no counterpart on the pages: a library convenience).
  * Same inputs, outputs, results and shape rules as moe_route_permute, without

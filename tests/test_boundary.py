@@ -92,3 +92,35 @@ def test_expert_stage_workspace_layout_is_consistent(L):
     arr = (ctypes.c_size_t * QMM_WS_FIELDS)()
     assert L.moe_expert_stage_workspace_layout(10, 100, 128, 8, 2, arr) == 2     # D % 128
     assert L.moe_expert_stage_workspace_layout(10, 128, 2048, 8, 2, arr) == 2    # F > 1024
+
+
+def test_dbg_substep_argument_checks(L):
+    """The qmm_dbg_* sub-step calls reject bad arguments before any device work."""
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.qmm_dbg_workspace_size.restype = sz
+    L.qmm_dbg_workspace_size.argtypes = [i32] * 4
+    n = L.qmm_dbg_workspace_size(1000, 256, 256, 8)
+    assert n >= 1000 * 256 * 2                        # f16 H codes
+    assert L.qmm_dbg_workspace_size(2000, 256, 256, 8) > n
+    L.qmm_dbg_down_iq4.restype = i32
+    L.qmm_dbg_down_iq4.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, sz, P]
+    ok = [P(256)] * 3
+    w = [P(256)] * 3
+    assert L.qmm_dbg_down_iq4(None, P(256), P(256), 1000, 256, 256, 8, *w, P(256), n, None) == 1   # null
+    assert L.qmm_dbg_down_iq4(*ok, 1000, 256, 256, 8, P(264), P(256), P(256), P(256), n, None) == 1  # misaligned
+    assert L.qmm_dbg_down_iq4(*ok, 1000, 256, 256, 8, *w, P(256 + 16), n, None) == 1   # ws not 256-aligned
+    assert L.qmm_dbg_down_iq4(*ok, 1000, 256, 2048, 8, *w, P(256), 1 << 40, None) == 2  # F > 1024
+    assert L.qmm_dbg_down_iq4(*ok, 1000, 200, 256, 8, *w, P(256), 1 << 40, None) == 2   # D % 128
+    assert L.qmm_dbg_down_iq4(*ok, 1000, 256, 256, 1024, *w, P(256), 1 << 40, None) == 2  # E > 512
+    assert L.qmm_dbg_down_iq4(*ok, 1000, 256, 256, 8, *w, P(256), n - 1, None) == 4     # workspace
+    L.qmm_dbg_gate_up_q8_1.restype = i32
+    L.qmm_dbg_gate_up_q8_1.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+    assert L.qmm_dbg_gate_up_q8_1(P(256), None, 1000, 256, 256, 8, *([P(256)] * 6), P(256), n, None) == 1
+    assert L.qmm_dbg_gate_up_q8_1(*([P(256)] * 2), 1000, 256, 100, 8, *([P(256)] * 6), P(256), n, None) == 2
+    L.qmm_dbg_combine.restype = i32
+    L.qmm_dbg_combine.argtypes = [P, i32, P, P, i32, i32, i32, P, P]
+    assert L.qmm_dbg_combine(P(256), 100, P(256), P(256), 50, 2, 66, P(256), None) == 2    # D % 4
+    assert L.qmm_dbg_combine(P(256), 100, P(256), P(256), 50, 17, 64, P(256), None) == 2   # k > 16
+    assert L.qmm_dbg_combine(None, 100, P(256), P(256), 50, 2, 64, P(256), None) == 1      # null
+    L.qmm_last_error.restype = ctypes.c_char_p
+    assert b"qmm_dbg_combine" in L.qmm_last_error()
