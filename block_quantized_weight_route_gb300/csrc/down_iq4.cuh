@@ -45,7 +45,10 @@ struct DownCfgT {
     static constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16, GROUP_K = 32;
     static constexpr int EPI_WARPS = EPI_WARPS_, CONV_WARPS = CONV_WARPS_, EPI_BASE = 4;
     static constexpr int CPW = 128 / (EPI_WARPS_ / 4);        // token columns per epilogue warp
-    static constexpr int NCH = CPW / 32;                      // 32-column TMEM loads per block
+    // TMEM loads of CW columns, NCH per 32-K block (16-column loads when every
+    // sub-partition also hosts a converter warp: fewer live registers)
+    static constexpr int CW = (EPI_WARPS_ == 16 && CONV_WARPS_ == 4) ? 16 : 32;
+    static constexpr int NCH = CPW / CW;
     static constexpr int W2 = EPI_BASE + EPI_WARPS;           // first warp after the epilogue (sub-partition 0)
     static constexpr int THREADS = 32 * (CONV_WARPS == 2 ? W2 : W2 + 3);
     static constexpr int CONV_THREADS = 32 * CONV_WARPS;
@@ -306,8 +309,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + cq * C::CPW);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(acc + c * 32, v);
+                    uint32_t v[C::CW];
+                    if constexpr (C::CW == 32) tmem_ld32(acc + c * C::CW, v);
+                    else tmem_ld16(acc + c * C::CW, v);
                     tmem_ld_wait();
                     if (c == C::NCH - 1) {
                         // the accumulator is in registers: hand the buffer back before folding
@@ -316,15 +320,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if (lane == 0) mbar_arrive(&acc_empty[buf]);
                     }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 dh = lds128(dh_base + (uint32_t)((g * C::BN + c * 32 + 4 * j) * 4));
+                    for (int j = 0; j < C::CW / 4; ++j) {
+                        const uint4 dh = lds128(dh_base + (uint32_t)((g * C::BN + c * C::CW + 4 * j) * 4));
                         const float2 i01 = make_float2(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
                         const float2 i23 = make_float2(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                         const float2 d01 = make_float2(__uint_as_float(dh.x), __uint_as_float(dh.y));
                         const float2 d23 = make_float2(__uint_as_float(dh.z), __uint_as_float(dh.w));
                         // y += (I * d_H) * d_W, both products rounded to fp32
-                        y[c * 16 + 2 * j] = __ffma2_rn(__fmul2_rn(i01, d01), dw2, y[c * 16 + 2 * j]);
-                        y[c * 16 + 2 * j + 1] = __ffma2_rn(__fmul2_rn(i23, d23), dw2, y[c * 16 + 2 * j + 1]);
+                        float2& y01 = y[c * (C::CW / 2) + 2 * j];
+                        float2& y23 = y[c * (C::CW / 2) + 2 * j + 1];
+                        y01 = __ffma2_rn(__fmul2_rn(i01, d01), dw2, y01);
+                        y23 = __ffma2_rn(__fmul2_rn(i23, d23), dw2, y23);
                     }
                 }
                 if (++buf == C::NBUF) {

@@ -279,13 +279,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
         int rr[kMaxK];
         float ww[kMaxK];
+        bool bad = false;
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) {
             if (j < k) {
                 rr[j] = __ldg(row + (long)t * k + j);
                 ww[j] = __ldg(w + (long)t * k + j);
-                if (rr[j] < 0 || rr[j] >= P) {
-                    if (lane == 0) atomicCAS(err, 0u, (uint32_t)DEV_BAD_ROW);
+                bad |= (unsigned)rr[j] >= (unsigned)P;
+            }
+        }
+        if (bad) {          // warp-uniform (every lane read the same token's slots)
+            if (lane == 0) atomicCAS(err, 0u, (uint32_t)DEV_BAD_ROW);
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                if (j < k && (unsigned)rr[j] >= (unsigned)P) {
                     rr[j] = 0;
                     ww[j] = 0.f;
                 }
