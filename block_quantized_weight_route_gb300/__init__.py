@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.qmm_dbg_down_iq4.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, sz, P]
         L.qmm_dbg_combine.restype = i32
         L.qmm_dbg_combine.argtypes = [P, i32, P, P, i32, i32, i32, P, P]
+        L.qmm_dbg_wait_timeout.restype = i32
+        L.qmm_dbg_wait_timeout.argtypes = [ctypes.c_uint, P]
         _lib = L
     return _lib
 
@@ -272,6 +274,12 @@ def qmm_dbg_combine(Yslot, row, w):
     st = lib().qmm_dbg_combine(_ptr(Yslot), P, _ptr(row), _ptr(w), T, k, D, _ptr(Y), _stream(dev))
     _check("qmm_dbg_combine", st)
     return Y
+
+
+def qmm_dbg_wait_timeout(timeout_us: int, device=None) -> None:
+    """Launch the wait-timeout probe (a bounded wait that nothing satisfies); the
+    next qmm_check_status raises QmmError with status QMM_ERR_TIMEOUT."""
+    _check("qmm_dbg_wait_timeout", lib().qmm_dbg_wait_timeout(int(timeout_us), _stream(device)))
 
 
 PROFILE_PHASES = ("route", "gather", "gate_up", "down", "combine")

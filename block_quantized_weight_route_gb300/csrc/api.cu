@@ -571,6 +571,16 @@ qmm_status qmm_dbg_combine(const float* Yslot, int P, const int32_t* row, const 
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "qmm_dbg_combine launch");
 }
 
+qmm_status qmm_dbg_wait_timeout(unsigned timeout_us, cudaStream_t stream) {
+    if (timeout_us < 1 || timeout_us > 2000000u)
+        return fail(QMM_ERR_INVALID_ARG, "qmm_dbg_wait_timeout: need 1 <= timeout_us <= 2000000");
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    cudaError_t e = launch_wait_timeout_probe(d->err, (uint64_t)timeout_us * 1000u, stream);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "qmm_dbg_wait_timeout launch");
+}
+
 qmm_status qmm_profile_enable(int on) {
     DeviceState* d = nullptr;
     qmm_status st = device_state(&d);

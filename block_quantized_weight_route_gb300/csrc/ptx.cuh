@@ -22,6 +22,7 @@ enum : uint32_t {
     DEV_BAD_TILE = 8,            // a tile descriptor pointed outside its buffers
     DEV_BAD_OFFSETS = 9,         // caller-given expert offsets not 0 <= ... <= P (sub-step calls)
     DEV_BAD_ROW = 10,            // a combine row index outside [0, P) (sub-step calls)
+    DEV_TIMEOUT_PROBE = 11,      // the wait-timeout probe's wait ran out (qmm_dbg_wait_timeout)
 };
 
 // A wait gives up after this many nanoseconds of wall-clock time.
@@ -87,8 +88,8 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // After a first poll the thread sleeps in try_wait (woken on completion, or
 // after at most 2 us) rather than spinning: polling warps slow the warps that
 // do the work.  The wall clock (slow to read) is consulted every 64 sleeps.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* err, uint32_t code) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* err, uint32_t code, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
@@ -96,12 +97,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicCAS(err, 0u, code);
             *abort_flag = 1;
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* err, uint32_t code) {
+    return mbar_wait_for(bar, parity, abort_flag, err, code, kWaitTimeoutNs);
 }
 
 // ---------------------------------------------------------------- TMA

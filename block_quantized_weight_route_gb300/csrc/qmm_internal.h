@@ -74,6 +74,7 @@ cudaError_t launch_codes_f16_to_i8(const __half* src, int8_t* dst, long n, cudaS
 cudaError_t launch_codes_i8_to_f16(const int8_t* src, __half* dst, long n, cudaStream_t s);
 cudaError_t launch_hd_to_entries(const __half* Hd, const int4* tiles, const int32_t* num_entries, int max_entries,
                                  int groups, float* Hd32, cudaStream_t s);
+cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_combine(const float* Yslot, int P, const int32_t* row, const float* w, int T, int k, int D,
                            float* Y, uint32_t* err, cudaStream_t s);
 

@@ -176,6 +176,17 @@ qmm_status qmm_dbg_combine(const float *Yslot, int P, const int32_t *row, const 
                            cudaStream_t stream);
 
 /*
+ * qmm_dbg_wait_timeout -- test hook for failure detection (no counterpart on
+ * the pages).  Launches one warp that waits, with the same bounded mbarrier
+ * wait every kernel of the library uses, on a barrier that nothing arrives on;
+ * after timeout_us microseconds (1 .. 2,000,000) the wait gives up, records a
+ * code in the device error word and the kernel returns normally.  The next
+ * qmm_check_status on the stream then returns QMM_ERR_TIMEOUT (and clears the
+ * word); the CUDA context stays usable.
+ */
+qmm_status qmm_dbg_wait_timeout(unsigned timeout_us, cudaStream_t stream);
+
+/*
  * moe_route_permute_noalloc -- moe_route_permute for callers that cannot
  * allocate device memory (no counterpart on the pages: a library convenience).
  * Same inputs, outputs, results and shape rules as moe_route_permute, without

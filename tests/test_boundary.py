@@ -124,3 +124,7 @@ def test_dbg_substep_argument_checks(L):
     assert L.qmm_dbg_combine(None, 100, P(256), P(256), 50, 2, 64, P(256), None) == 1      # null
     L.qmm_last_error.restype = ctypes.c_char_p
     assert b"qmm_dbg_combine" in L.qmm_last_error()
+    L.qmm_dbg_wait_timeout.restype = i32
+    L.qmm_dbg_wait_timeout.argtypes = [ctypes.c_uint, P]
+    assert L.qmm_dbg_wait_timeout(0, None) == 1
+    assert L.qmm_dbg_wait_timeout(3000000, None) == 1

@@ -173,3 +173,20 @@ def test_dbg_combine_bad_row_is_reported(qlib):
     assert ei.value.status == 1
     # the bad slot adds nothing; the others are summed
     assert float(Y[3, 0]) == 0.5 and float(Y[0, 0]) == 1.0
+
+
+def test_bounded_wait_times_out_and_context_survives(qlib):
+    """Failure detection without a fault: a bounded wait that nothing satisfies
+    gives up after its limit, the host reads QMM_ERR_TIMEOUT through
+    qmm_check_status, and the context keeps working (a GEMM right after is exact)."""
+    qlib.qmm_dbg_wait_timeout(2000)                                   # 2 ms
+    with pytest.raises(qlib.QmmError) as ei:
+        qlib.qmm_check_status()
+    assert ei.value.status == 6 and "device code 11" in str(ei.value)
+    qlib.qmm_check_status()                                           # the word was cleared
+    g = wl.gen_w4a16(64, 512, 512, 1.0 / 64, seed=27)
+    Y = qlib.qmm_w4a16(dev(g["X"].view(np.int16)).view(torch.bfloat16), dev(g["Wc"]), dev(g["Ws"]),
+                       float(g["scale2"]))
+    qlib.qmm_check_status()
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"])
+    assert rel_err(Y.cpu().numpy().astype(np.float64), ref) <= 1e-5
