@@ -8,9 +8,10 @@
 //                    the tensor core reads, in shared memory; none of them runs on
 //                    the MMA issuer's sub-partition (warp id % 4 == 1)
 //
-// Tile: 128 rows (tokens) x BN columns (weight rows), K step 64.  The MMA is
-// tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16), fp32 accumulation in
-// TMEM.  Operands are K-major in the canonical 128-byte-swizzled layout.
+// Tile: 128*MSUB rows (tokens) x BN columns (weight rows), K step 64.  The MMA
+// is tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16), MSUB of them per K
+// step (one per 128-row sub-tile), fp32 accumulation in TMEM.  Operands are
+// K-major in the canonical 128-byte-swizzled layout.
 //
 // The quantised formats it reads (page titles / sections):
 //  - W4: e2m1 codes with one E4M3 scale per 16 K and an fp32 scale2 applied once
