@@ -381,8 +381,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t ph = 0;
             long issued = 0;
             bool ok = true;
+            TileInfo ti_next{};
+            if (cid < num_tiles) ti_next = decode_tile<C>(p, cid, crank);
             for (int t = cid; t < num_tiles && ok; t += ncl) {
-                const TileInfo ti = decode_tile<C>(p, t, crank);
+                const TileInfo ti = ti_next;                 // read one tile ahead
+                if (t + ncl < num_tiles) ti_next = decode_tile<C>(p, t + ncl, crank);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
                     if (__any_sync(0xffffffffu, !got)) {
@@ -428,10 +431,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             int ts = 0, cs = 0, buf = 0;
             uint32_t tph = 0, cph = 0, bph = 0;
             bool ok = true;
+            // sub-tiles holding at least one live row (a tile of <= 128 rows skips the
+            // second), read one tile ahead so the descriptor load is off the issue path
+            int nsub_next = C::MSUB;
+            if constexpr (C::MSUB == 2)
+                if (cid < num_tiles) nsub_next = (decode_tile<C>(p, cid, crank).rows > 128) ? 2 : 1;
             for (int t = cid; t < num_tiles && ok; t += ncl) {
-                // sub-tiles holding at least one live row (a tile of <= 128 rows skips the second)
-                int nsub = C::MSUB;
-                if constexpr (C::MSUB == 2) nsub = (decode_tile<C>(p, t, crank).rows > 128) ? 2 : 1;
+                const int nsub = nsub_next;
+                if constexpr (C::MSUB == 2)
+                    if (t + ncl < num_tiles) nsub_next = (decode_tile<C>(p, t + ncl, crank).rows > 128) ? 2 : 1;
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
                     bool got = mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL);
                     got = got && mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
@@ -695,16 +703,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 return (long)tt.n0 + crow;
             }
         };
-        auto load_chunk = [&](int t, int ch) -> uint4 {
-            if (t >= num_tiles) return make_uint4(0, 0, 0, 0);
-            const TileInfo tt = decode_tile<C>(p, t, crank);
-            bool in_range;
-            const long wrow = scale_row(tt, in_range);
-            return in_range ? ldg_nc_v4(p.w_scale + wrow * (p.K / 16) + ch * 16) : make_uint4(0, 0, 0, 0);
+        // Scale prefetch two 4-K-block chunks ahead, through a cursor that walks
+        // this CTA's tiles in the order they are converted: the next tile's
+        // descriptor is read one chunk before its first scales are needed, so
+        // neither global load (descriptor, then scales) sits on the critical path.
+        int pf_t = cid, pf_ch = 0;
+        TileInfo pf_ti{};
+        if (pf_t < num_tiles) pf_ti = decode_tile<C>(p, pf_t, crank);
+        auto next_chunk = [&]() -> uint4 {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (pf_t < num_tiles) {
+                bool in_range;
+                const long wrow = scale_row(pf_ti, in_range);
+                if (in_range) v = ldg_nc_v4(p.w_scale + wrow * (p.K / 16) + pf_ch * 16);
+                if (++pf_ch == kchunks) {
+                    pf_ch = 0;
+                    pf_t += ncl;
+                    if (pf_t < num_tiles) pf_ti = decode_tile<C>(p, pf_t, crank);
+                }
+            }
+            return v;
         };
-        uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = make_uint4(0, 0, 0, 0);
+        uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = make_uint4(0, 0, 0, 0), sc_next2 = make_uint4(0, 0, 0, 0);
         if constexpr (C::B == BMode::W4) {
-            if (vec_scales) sc_next = load_chunk(cid, 0);
+            if (vec_scales) {
+                sc_next = next_chunk();
+                sc_next2 = next_chunk();
+            }
         }
         for (int t = cid; t < num_tiles && ok; t += ncl) {
             const TileInfo ti = decode_tile<C>(p, t, crank);
@@ -714,8 +739,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (vec_scales) {
                         if ((kb & 3) == 0) {
                             sc_cur = sc_next;
-                            const int ch = (kb >> 2) + 1;
-                            sc_next = (ch < kchunks) ? load_chunk(t, ch) : load_chunk(t + ncl, 0);
+                            sc_next = sc_next2;
+                            sc_next2 = next_chunk();
                         }
                         const int j = kb & 3;
                         sbytes = j == 0 ? sc_cur.x : (j == 1 ? sc_cur.y : (j == 2 ? sc_cur.z : sc_cur.w));
