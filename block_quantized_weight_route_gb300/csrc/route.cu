@@ -298,19 +298,28 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
                 }
             }
         }
-        for (int i = lane; i < vec_per_row; i += 32) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // two column vectors per lane per pass: 2k independent 16-byte loads in flight
+        for (int i = lane; i < vec_per_row; i += 64) {
+            const bool two = i + 32 < vec_per_row;
+            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll
             for (int j = 0; j < kMaxK; ++j) {
                 if (j < k) {
-                    const float4 v = __ldg(Yslot + (long)rr[j] * vec_per_row + i);
-                    acc.x = fmaf(ww[j], v.x, acc.x);
-                    acc.y = fmaf(ww[j], v.y, acc.y);
-                    acc.z = fmaf(ww[j], v.z, acc.z);
-                    acc.w = fmaf(ww[j], v.w, acc.w);
+                    const float4* src = Yslot + (long)rr[j] * vec_per_row + i;
+                    const float4 v0 = __ldcs(src);
+                    const float4 v1 = two ? __ldcs(src + 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    acc0.x = fmaf(ww[j], v0.x, acc0.x);
+                    acc0.y = fmaf(ww[j], v0.y, acc0.y);
+                    acc0.z = fmaf(ww[j], v0.z, acc0.z);
+                    acc0.w = fmaf(ww[j], v0.w, acc0.w);
+                    acc1.x = fmaf(ww[j], v1.x, acc1.x);
+                    acc1.y = fmaf(ww[j], v1.y, acc1.y);
+                    acc1.z = fmaf(ww[j], v1.z, acc1.z);
+                    acc1.w = fmaf(ww[j], v1.w, acc1.w);
                 }
             }
-            Y[(long)t * vec_per_row + i] = acc;
+            Y[(long)t * vec_per_row + i] = acc0;
+            if (two) Y[(long)t * vec_per_row + i + 32] = acc1;
         }
     }
 }

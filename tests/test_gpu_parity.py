@@ -245,3 +245,14 @@ def test_expert_stage_t21504_zipf_sampled(qlib):
     w = wl.WORKLOADS["moe_t21504_d2560_f1024_e256_k8_zipf"]
     g = wl.generate(w)
     check_stage(qlib, g, w.k, tokens=np.array([0, 9999, 21503]))
+
+
+def test_expert_stage_at_the_shape_limits(qlib):
+    """E = 512, k = 16, F = 1024 (the largest the ABI takes), D an odd multiple of 128."""
+    g = wl.gen_moe(37, 384, 1024, 512, 16, 1.0 / 128, 0.0, seed=15)
+    check_stage(qlib, g, 16)
+
+
+def test_expert_stage_single_token(qlib):
+    g = wl.gen_moe(1, 256, 128, 8, 8, 1.0 / 128, 0.0, seed=16)
+    check_stage(qlib, g, 8)
