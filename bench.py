@@ -37,6 +37,7 @@ from synthetic import workloads as wl  # noqa: E402
 STAGE = "moe_t5268_d2048_f768_e128_k8"
 GEMM_W4 = "w4a16_m2048_k5120_n17408"
 GEMM_FP8 = "fp8blk128_m2048_k5120_n5120"
+GEMM_ROUTER = "w4a16_router_m2048_k2560_n512"
 METRIC = "MoE expert-stage prefill tokens/s; quant-GEMM TFLOP/s vs GB300 tensor peak"
 # DRAM bytes (read + write) per launch of each stage kernel on the 5268-token
 # workload, from one ncu capture of the kernel as it stands (profiles/); None
@@ -352,15 +353,16 @@ def bench_dense(q, torch, device, args, peaks, peak_src):
     out = {}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
-    for name in (GEMM_W4, GEMM_FP8):
+    for name in (GEMM_W4, GEMM_FP8, GEMM_ROUTER):
         w = wl.WORKLOADS[name]
         g = wl.generate(w)
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
         X = d(g["X"].view(np.int16))
         if w.kind == "w4a16":
             Wc, Ws = d(g["Wc"]), d(g["Ws"])
-            Y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
-            call = lambda: q.qmm_w4a16(X, Wc, Ws, float(g["scale2"]), out_dtype=torch.bfloat16, Y=Y)  # noqa: E731
+            odt = torch.bfloat16 if w.out == "bf16" else torch.float32
+            Y = torch.empty((w.M, w.N), dtype=odt, device=device)
+            call = lambda: q.qmm_w4a16(X, Wc, Ws, float(g["scale2"]), out_dtype=odt, Y=Y)  # noqa: E731
         else:
             W, S = d(g["W"]), d(g["S"])
             Y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)

@@ -117,7 +117,7 @@ class Workload:
         return 2.0 * rows * self.D * 2 * self.F + 2.0 * rows * self.F * self.D
 
 
-# The five workloads the path is measured and checked on.  Sizes and value
+# The workloads the path is measured and checked on.  Sizes and value
 # distributions are the problem statement's; seeds are the workload's index.
 WORKLOADS = {
     "w4a16_m64_k512_n512": Workload(
@@ -135,6 +135,11 @@ WORKLOADS = {
     "moe_t21504_d2560_f1024_e256_k8_zipf": Workload(
         name="moe_t21504_d2560_f1024_e256_k8_zipf", kind="moe", seed=4, T=21504, D=2560,
         F=1024, E=256, k=8, gu_scale2=1.0 / 128, zipf_s=1.1),
+    # the router projection in front of routing (logits = X . W_r^T, one row per
+    # expert), at the router shape of the sources' W4A16 measurements; fp32 logits
+    "w4a16_router_m2048_k2560_n512": Workload(
+        name="w4a16_router_m2048_k2560_n512", kind="w4a16", seed=5, M=2048, K=2560, N=512,
+        scale2=1.0 / 64, out="f32"),
 }
 
 

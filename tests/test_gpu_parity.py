@@ -114,6 +114,32 @@ def test_w4a16_full_size_sampled(qlib):
     check_bf16_output(bf16_to_np(Y)[np.ix_(rows, cols)], ref)
 
 
+def test_w4a16_router_shape_sampled(qlib):
+    """The router projection in front of routing, logits = X . W_r^T (one W4 row
+    per expert), at the sources' router shape; fp32 logits."""
+    w = wl.WORKLOADS["w4a16_router_m2048_k2560_n512"]
+    g = wl.generate(w)
+    Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"]))
+    rows = np.concatenate([np.arange(0, 2048, 37), [2047, 2046, 255, 256]])
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"], rows=rows)
+    assert rel_err(Y.cpu().numpy().astype(np.float64)[rows], ref) <= 1e-5
+
+
+def test_router_projection_then_expert_stage(qlib):
+    """X -> logits (W4 router projection) -> expert stage, on the GPU; the routing
+    and the stage checked against the oracle given the GPU's fp32 logits."""
+    T, D, F, E, k = 300, 256, 256, 64, 4
+    g = wl.gen_moe(T, D, F, E, k, 1.0 / 128, 0.0, seed=17)
+    r = wl.gen_w4a16(T, D, E, 1.0 / 64, seed=18)
+    Xd = bf16_dev(g["X"])
+    logits = qlib.qmm_w4a16(Xd, dev(r["Wc"]), dev(r["Ws"]), float(r["scale2"]))
+    ref_logits = oracle.w4a16(g["X"], r["Wc"], r["Ws"], r["scale2"])
+    lg = logits.cpu().numpy()
+    assert rel_err(lg.astype(np.float64), ref_logits) <= 1e-5
+    g2 = dict(g, logits=lg)
+    check_stage(qlib, g2, k)
+
+
 # ---------------------------------------------------------------- dense FP8 block-128
 
 @pytest.mark.parametrize("M,K,N", [(130, 384, 256), (1, 128, 128), (257, 640, 384)])
