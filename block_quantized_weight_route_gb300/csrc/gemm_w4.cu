@@ -11,7 +11,13 @@ template <int CN>
 using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 128, 8, 4, 4, 3, false, CN, 2>;
 // Gate/up: 256 token rows x (64 gate + 64 up) weight rows per tile.
 template <int CN>
-using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, 4, 3, true, CN, 2>;
+#ifndef QMM_GU_TSTAGES
+#define QMM_GU_TSTAGES 4
+#endif
+#ifndef QMM_GU_CSTAGES
+#define QMM_GU_CSTAGES 3
+#endif
+using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, QMM_GU_TSTAGES, QMM_GU_CSTAGES, true, CN, 2>;
 
 int cluster_for(int n_tiles) { return (n_tiles % 4 == 0) ? 4 : ((n_tiles % 2 == 0) ? 2 : 1); }
 
