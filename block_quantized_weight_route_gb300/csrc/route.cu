@@ -164,7 +164,19 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int chunks, int E, int
     const int e = threadIdx.x;
     int cnt = 0;
     if (e < E) {
-        for (int c = 0; c < chunks; ++c) {
+        // exclusive running sum over the chunks, 8 independent loads at a time
+        int c = 0;
+        for (; c + 8 <= chunks; c += 8) {
+            int h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = chunk_hist[(long)(c + i) * E + e];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                chunk_hist[(long)(c + i) * E + e] = cnt;
+                cnt += h[i];
+            }
+        }
+        for (; c < chunks; ++c) {
             const int h = chunk_hist[(long)c * E + e];
             chunk_hist[(long)c * E + e] = cnt;
             cnt += h;
