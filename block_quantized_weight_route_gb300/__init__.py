@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.qmm_profile_enable.argtypes = [i32]
         L.qmm_profile_read.restype = i32
         L.qmm_profile_read.argtypes = [P]
+        L.qmm_profile_read_call.restype = i32
+        L.qmm_profile_read_call.argtypes = [ctypes.c_long, P]
         L.moe_expert_stage_w4_iq4.restype = i32
         L.moe_expert_stage_w4_iq4.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
         L.qmm_dbg_workspace_size.restype = sz
@@ -293,6 +295,14 @@ def qmm_profile_read() -> dict:
     """Phase times (ms) of the last profiled expert-stage call (waits for it)."""
     arr = (ctypes.c_float * len(PROFILE_PHASES))()
     _check("qmm_profile_read", lib().qmm_profile_read(ctypes.cast(arr, ctypes.c_void_p)))
+    return dict(zip(PROFILE_PHASES, [float(v) for v in arr]))
+
+
+def qmm_profile_read_call(i: int) -> dict:
+    """Phase times (ms) of the i-th profiled expert-stage call since profiling was
+    switched on (one of the last 256; waits for that call only)."""
+    arr = (ctypes.c_float * len(PROFILE_PHASES))()
+    _check("qmm_profile_read_call", lib().qmm_profile_read_call(int(i), ctypes.cast(arr, ctypes.c_void_p)))
     return dict(zip(PROFILE_PHASES, [float(v) for v in arr]))
 
 

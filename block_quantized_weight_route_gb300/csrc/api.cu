@@ -39,9 +39,10 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 struct DeviceState {
     bool ready = false;
     bool profile = false;
-    bool events_ready = false;
-    bool profiled_once = false;
-    cudaEvent_t ev[QMM_PROFILE_PHASES + 1];
+    long calls = 0;                                   // profiled calls since profiling was enabled
+    int slot = 0;                                     // ring slot of the call being recorded
+    bool slot_ready[QMM_PROFILE_RING] = {};
+    cudaEvent_t ev[QMM_PROFILE_RING][QMM_PROFILE_PHASES + 1];
     qmm_status status = QMM_OK;
     std::string why;
     int sms = 0;
@@ -110,18 +111,24 @@ qmm_status make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, u
     return QMM_OK;
 }
 
-// Record phase boundary i of a profiled expert-stage call.
+// Record phase boundary i of a profiled expert-stage call, into the ring slot of
+// this call (the last QMM_PROFILE_RING calls stay readable without a host sync
+// in between).
 cudaError_t mark(DeviceState* d, int i, cudaStream_t s) {
     if (!d->profile) return cudaSuccess;
-    if (!d->events_ready) {
-        for (int j = 0; j <= QMM_PROFILE_PHASES; ++j) {
-            cudaError_t e = cudaEventCreate(&d->ev[j]);
-            if (e != cudaSuccess) return e;
+    if (i == 0) {
+        d->slot = (int)(d->calls % QMM_PROFILE_RING);
+        if (!d->slot_ready[d->slot]) {
+            for (int j = 0; j <= QMM_PROFILE_PHASES; ++j) {
+                cudaError_t e = cudaEventCreate(&d->ev[d->slot][j]);
+                if (e != cudaSuccess) return e;
+            }
+            d->slot_ready[d->slot] = true;
         }
-        d->events_ready = true;
     }
-    d->profiled_once = true;
-    return cudaEventRecord(d->ev[i], s);
+    cudaError_t e = cudaEventRecord(d->ev[d->slot][i], s);
+    if (i == QMM_PROFILE_PHASES) ++d->calls;
+    return e;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -585,7 +592,26 @@ qmm_status qmm_profile_enable(int on) {
     DeviceState* d = nullptr;
     qmm_status st = device_state(&d);
     if (st != QMM_OK) return st;
+    if (on && !d->profile) d->calls = 0;
     d->profile = on != 0;
+    return QMM_OK;
+}
+
+qmm_status qmm_profile_read_call(long i, float* ms_out) {
+    if (!ms_out) return fail(QMM_ERR_INVALID_ARG, "qmm_profile_read_call: null pointer");
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    if (i < 0 || i >= d->calls || i < d->calls - QMM_PROFILE_RING)
+        return fail(QMM_ERR_INVALID_ARG, "qmm_profile_read_call: call %ld is not among the last %d of %ld profiled calls",
+                    i, QMM_PROFILE_RING, d->calls);
+    cudaEvent_t* ev = d->ev[i % QMM_PROFILE_RING];
+    cudaError_t e = cudaEventSynchronize(ev[QMM_PROFILE_PHASES]);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_profile_read_call");
+    for (int j = 0; j < QMM_PROFILE_PHASES; ++j) {
+        e = cudaEventElapsedTime(&ms_out[j], ev[j], ev[j + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "qmm_profile_read_call");
+    }
     return QMM_OK;
 }
 
@@ -594,14 +620,8 @@ qmm_status qmm_profile_read(float* ms_out) {
     DeviceState* d = nullptr;
     qmm_status st = device_state(&d);
     if (st != QMM_OK) return st;
-    if (!d->profiled_once) return fail(QMM_ERR_INVALID_ARG, "qmm_profile_read: no profiled call yet");
-    cudaError_t e = cudaEventSynchronize(d->ev[QMM_PROFILE_PHASES]);
-    if (e != cudaSuccess) return cuda_fail(e, "qmm_profile_read");
-    for (int i = 0; i < QMM_PROFILE_PHASES; ++i) {
-        e = cudaEventElapsedTime(&ms_out[i], d->ev[i], d->ev[i + 1]);
-        if (e != cudaSuccess) return cuda_fail(e, "qmm_profile_read");
-    }
-    return QMM_OK;
+    if (d->calls == 0) return fail(QMM_ERR_INVALID_ARG, "qmm_profile_read: no profiled call yet");
+    return qmm_profile_read_call(d->calls - 1, ms_out);
 }
 
 }  // extern "C"

@@ -218,12 +218,17 @@ qmm_status moe_route_permute_noalloc(const float *logits, int T, int E, int k, i
  * phases: 0 routing (top-k, counts, scan, permutation), 1 row gather of X,
  * 2 gate/up + SwiGLU + q8_1, 3 down, 4 combine.  qmm_profile_read() waits for
  * the last profiled call's events and writes its QMM_PROFILE_PHASES phase times
- * in milliseconds.  Events belong to the current device and are created on the
- * first profiled call; profiling is off by default.
+ * in milliseconds; qmm_profile_read_call(i, ...) does the same for the i-th call
+ * (0-based) since profiling was switched on, for the last QMM_PROFILE_RING such
+ * calls, so that a caller can profile many calls without waiting between them.
+ * Events belong to the current device and are created on first use; profiling
+ * is off by default.  Other calls: QMM_ERR_INVALID_ARG.
  */
 #define QMM_PROFILE_PHASES 5
+#define QMM_PROFILE_RING 256
 qmm_status qmm_profile_enable(int on);
 qmm_status qmm_profile_read(float *ms_out);
+qmm_status qmm_profile_read_call(long i, float *ms_out);
 
 #ifdef __cplusplus
 }

@@ -128,3 +128,6 @@ def test_dbg_substep_argument_checks(L):
     L.qmm_dbg_wait_timeout.argtypes = [ctypes.c_uint, P]
     assert L.qmm_dbg_wait_timeout(0, None) == 1
     assert L.qmm_dbg_wait_timeout(3000000, None) == 1
+    L.qmm_profile_read_call.restype = i32
+    L.qmm_profile_read_call.argtypes = [ctypes.c_long, P]
+    assert L.qmm_profile_read_call(0, None) == 1
