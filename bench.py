@@ -360,6 +360,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.empty_cache()
 
     quant = {} if args.no_gemm else bench_dense(q, torch, device, args, peaks, peak_src)
+    other = {} if args.no_gemm else bench_other_stage(q, torch, device, args)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -370,13 +371,46 @@ def run_gpu(args, world, rank, local):
                    "l2": "inputs larger than L2 (340 MB of expert weights read per step)",
                    "timing": "CUDA events per step; phase events between the stage's kernels inside the timed steps "
                              "(the e2e loop records none)"},
-        "roofline": roof, "phases": phase_roof, "quant_gemm": quant, "e2e": e2e, "clocks": clk,
+        "roofline": roof, "phases": phase_roof, "quant_gemm": quant, "other_stage": other, "e2e": e2e, "clocks": clk,
         "gpu_launches": 8 * args.steps, "wall_s": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(g, w.k)
     if rank == 0:
         print(json.dumps(line))
+
+
+STAGE_LARGE = "moe_t21504_d2560_f1024_e256_k8_zipf"
+
+
+def bench_other_stage(q, torch, device, args):
+    """The larger stage configuration (skewed expert popularity), timed the same
+    way as the headline stage but for a few steps: context, not the metric."""
+    w = wl.WORKLOADS[STAGE_LARGE]
+    g = wl.generate(w)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+    X, L = d(g["X"].view(np.int16)), d(g["logits"])
+    args_ = (d(g["Wgu_c"]), d(g["Wgu_s"]), d(g["gu_scale2"]), d(g["Wd_idx"]), d(g["Wd_s"].view(np.int16)))
+    ws = torch.empty(q.moe_expert_stage_workspace_size(w.T, w.D, w.F, w.E, w.k), dtype=torch.uint8, device=device)
+    Y = torch.empty((w.T, w.D), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        q.moe_expert_stage_w4_iq4(X, L, *args_, w.k, ws=ws, Y=Y)
+    torch.cuda.synchronize()
+    n = max(3, min(20, args.steps // 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        q.moe_expert_stage_w4_iq4(X, L, *args_, w.k, ws=ws, Y=Y)
+    b.record(stream)
+    torch.cuda.synchronize()
+    q.qmm_check_status()
+    ms = a.elapsed_time(b) / n
+    out = {STAGE_LARGE: {"ms": ms, "tokens_per_s": w.T / (ms * 1e-3), "tflops": w.flops() / (ms * 1e-3) / 1e12,
+                         "steps": n}}
+    del ws, Y, X, L, args_
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_dense(q, torch, device, args, peaks, peak_src):
