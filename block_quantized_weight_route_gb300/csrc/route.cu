@@ -264,7 +264,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
         const uint4* in = X + (long)src[r] * vec_per_row;
         uint4* out = Xp + (long)r * vec_per_row;
-        for (int i = lane; i < vec_per_row; i += 32) out[i] = __ldg(in + i);
+        int i = lane;
+        for (; i + 96 < vec_per_row; i += 128) {           // four 16-byte loads in flight per lane
+            const uint4 a0 = __ldg(in + i), a1 = __ldg(in + i + 32), a2 = __ldg(in + i + 64), a3 = __ldg(in + i + 96);
+            out[i] = a0;
+            out[i + 32] = a1;
+            out[i + 64] = a2;
+            out[i + 96] = a3;
+        }
+        for (; i < vec_per_row; i += 32) out[i] = __ldg(in + i);
     }
 }
 
