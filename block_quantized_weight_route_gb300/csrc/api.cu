@@ -212,23 +212,24 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     DeviceState* d = nullptr;
     qmm_status st = device_state(&d);
     if (st != QMM_OK) return st;
-    // 256 x 128 tiles; clusters of cn CTAs share the activation rows
-    const int n_tiles = (N + 127) / 128;
+    // sh.rows x sh.bn tiles; clusters of cn CTAs share the activation rows
+    const TileShape sh = w4_dense_shape(M, N, d->sms);
+    const int n_tiles = (N + sh.bn - 1) / sh.bn;
     const int cn = cluster_for(n_tiles);
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 256 / cn,
+    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, sh.rows / cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
-    if ((st = make_tmap(&tb, Wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, 32, 128,
+    if ((st = make_tmap(&tb, Wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, 32, sh.bn,
                         CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
         return st;
     GemmParams p{};
     p.M = M;
     p.N = N;
     p.K = K;
-    p.m_tiles = (M + 255) / 256;
+    p.m_tiles = (M + sh.rows - 1) / sh.rows;
     p.n_tiles = n_tiles;
-    p.n_step = 128;
+    p.n_step = sh.bn;
     p.w_scale = Ws;
     p.scale2_dense = scale2;
     p.Y = Y;
@@ -253,7 +254,8 @@ qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t*
     if (st != QMM_OK) return st;
     const int cn = cluster_for(N / 128);
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, 128 / cn,
+    const int bm = fp8_tile_rows();
+    if ((st = make_tmap(&ta, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, (uint64_t)K * 2, 64, bm / cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
     if ((st = make_tmap(&tb, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) != QMM_OK)
@@ -262,7 +264,7 @@ qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t*
     p.M = M;
     p.N = N;
     p.K = K;
-    p.m_tiles = (M + 127) / 128;
+    p.m_tiles = (M + bm - 1) / bm;
     p.n_tiles = N / 128;
     p.n_step = 128;
     p.blk_scale = S;
@@ -317,26 +319,29 @@ qmm_status moe_route_permute(const float* logits, int T, int E, int k, int32_t* 
 // tile list: 256 token rows x (64 gate + 64 up weight rows) per tile, clusters
 // of CTAs sharing the token rows.  Writes Hq (f16 codes), Hd, Hs, Hd32.
 static qmm_status run_gate_up(DeviceState* d, const uint16_t* Xp, int P, int D, int F, int E, const uint8_t* Wgu_c,
-                              const uint8_t* Wgu_s, const float* gu_scale2, const int4* tiles2,
-                              const int32_t* num_entries2, int max_entries2, __half* Hq, __half* Hd, __half* Hs,
-                              float* Hd32, cudaStream_t stream) {
+                              const uint8_t* Wgu_s, const float* gu_scale2, const RouteBufs& rb, __half* Hq,
+                              __half* Hd, __half* Hs, float* Hd32, cudaStream_t stream) {
     qmm_status st;
-    const int gu_cn = cluster_for(F / 64);
+    // sh.rows token rows x (sh.bn / 2 gate + sh.bn / 2 up) weight rows per tile
+    const TileShape sh = w4_gate_up_shape();
+    const int hstep = sh.bn / 2;
+    if (F % hstep) return fail(QMM_ERR_UNSUPPORTED_SHAPE, "expert stage: F %% %d != 0 (F=%d)", hstep, F);
+    const int gu_cn = cluster_for(F / hstep);
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, 256 / gu_cn,
+    if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, sh.rows / gu_cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
-    if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, 64,
+    if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, hstep,
                         CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
         return st;
     GemmParams g{};
     g.K = D;
     g.F = F;
-    g.n_tiles = F / 64;
-    g.n_step = 64;
-    g.tiles = tiles2;
-    g.num_entries = num_entries2;
-    g.max_entries = max_entries2;
+    g.n_tiles = F / hstep;
+    g.n_step = hstep;
+    g.tiles = sh.rows == 256 ? rb.tiles2 : rb.tiles;
+    g.num_entries = sh.rows == 256 ? rb.num_entries2 : rb.num_entries;
+    g.max_entries = sh.rows == 256 ? rb.max_entries2 : rb.max_entries;
     g.w_scale = Wgu_s;
     g.scale2 = gu_scale2;
     g.Hq = Hq;
@@ -452,8 +457,7 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     float* Yslot = static_cast<float*>(at(16));
 
     // gate/up + SwiGLU + q8_1
-    if ((st = run_gate_up(d, Xp, P, D, F, E, Wgu_c, Wgu_s, gu_scale2, rb.tiles2, rb.num_entries2, max_entries2, Hq, Hd,
-                          Hs, Hd32, stream)) != QMM_OK)
+    if ((st = run_gate_up(d, Xp, P, D, F, E, Wgu_c, Wgu_s, gu_scale2, rb, Hq, Hd, Hs, Hd32, stream)) != QMM_OK)
         return st;
     if ((e = mark(d, 3, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
@@ -536,8 +540,8 @@ qmm_status qmm_dbg_gate_up_q8_1(const uint16_t* X_perm, const int32_t* offsets, 
     if ((st = dbg_tiles(d, offsets, P, E, base, off, &rb, stream)) != QMM_OK) return st;
     __half* Hq16 = reinterpret_cast<__half*>(base + off[4]);
     float* Hd32 = reinterpret_cast<float*>(base + off[5]);
-    if ((st = run_gate_up(d, X_perm, P, D, F, E, Wgu_c, Wgu_s, gu_scale2, rb.tiles2, rb.num_entries2, rb.max_entries2,
-                          Hq16, reinterpret_cast<__half*>(Hd), reinterpret_cast<__half*>(Hs), Hd32, stream)) != QMM_OK)
+    if ((st = run_gate_up(d, X_perm, P, D, F, E, Wgu_c, Wgu_s, gu_scale2, rb, Hq16, reinterpret_cast<__half*>(Hd),
+                          reinterpret_cast<__half*>(Hs), Hd32, stream)) != QMM_OK)
         return st;
     cudaError_t e = launch_codes_f16_to_i8(Hq16, Hq, (long)P * F, stream);
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "qmm_dbg_gate_up_q8_1: code conversion");

@@ -310,7 +310,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const float dwf = __half2float(__ushort_as_half((unsigned short)lds_u16(dw_addr + g * 2)));
                 const float2 dw2 = make_float2(dwf, dwf);
                 const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + cq * C::CPW);
-#pragma unroll
                 // all of this warp's accumulator columns for the block: loads issued
                 // together, one wait, the buffer handed back before the fold
                 uint32_t v[C::NCH][C::CW];

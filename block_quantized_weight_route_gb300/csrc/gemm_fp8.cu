@@ -5,8 +5,14 @@
 
 namespace qmm {
 
+// Two 128-row sub-tiles (256 token rows) share each expanded weight tile, which
+// halves the E4M3 -> bf16 conversion per FLOP; the fold then needs 16 epilogue
+// warps so that the two sub-tiles' running sums fit in registers, and two
+// converter warps expand two weight rows per thread.
 template <int CN>
-using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 4, 8, 4, 4, false, CN>;
+using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 2, 16, 4, 4, false, CN, 2>;
+
+int fp8_tile_rows() { return CfgFp8<1>::BM; }
 
 cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                               cudaStream_t s) {

@@ -5,25 +5,50 @@
 
 namespace qmm {
 
-// Dense: 256 x 128 tiles (two 128-row sub-tiles share each converted weight
-// tile), 8 converter warps (two per weight row), 4 epilogue warps.
-template <int CN>
-using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 128, 8, 4, 4, 3, false, CN, 2>;
-// Gate/up: 256 token rows x (64 gate + 64 up) weight rows per tile.
-template <int CN>
 #ifndef QMM_GU_TSTAGES
 #define QMM_GU_TSTAGES 4
 #endif
 #ifndef QMM_GU_CSTAGES
 #define QMM_GU_CSTAGES 3
 #endif
+
+// Dense: 256 token rows per tile (two 128-row sub-tiles share each converted
+// weight tile), 8 converter warps, 4 epilogue warps.  Wide: 256 weight rows per
+// tile, which halves the conversion per FLOP again; the two 128 x 256
+// accumulators fill TMEM, so the epilogue of one tile is not overlapped with the
+// next tile's MMAs.  Narrow: 128 weight rows, double-buffered accumulators, twice
+// the tiles (for problems too small to fill the SMs with wide tiles).
+template <int CN>
+using CfgW4DenseWide = GemmCfg<BMode::W4, Epi::STORE, 256, 8, 4, 3, 2, false, CN, 2>;
+template <int CN>
+using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 128, 8, 4, 4, 3, false, CN, 2>;
+// Gate/up: 256 token rows x (64 gate + 64 up) weight rows per tile.
+template <int CN>
 using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, QMM_GU_TSTAGES, QMM_GU_CSTAGES, true, CN, 2>;
+
+// Wide tiles do a tile's work in about 1.75x the time of a narrow one (measured:
+// 0.305 against 0.349 ms at M=2048, K=5120, N=17408), so they win unless their
+// coarser waves leave more SMs idle.
+TileShape w4_dense_shape(int M, int N, int sms) {
+    const long wide = (long)((M + 255) / 256) * ((N + 255) / 256);
+    const long narrow = (long)((M + 255) / 256) * ((N + 127) / 128);
+    const long wide_waves = (wide + sms - 1) / sms, narrow_waves = (narrow + sms - 1) / sms;
+    return (wide_waves * 7 < narrow_waves * 4) ? TileShape{256, 256} : TileShape{256, 128};
+}
+TileShape w4_gate_up_shape() { return TileShape{CfgW4GateUp<1>::BM, CfgW4GateUp<1>::BN}; }
 
 int cluster_for(int n_tiles) { return (n_tiles % 4 == 0) ? 4 : ((n_tiles % 2 == 0) ? 2 : 1); }
 
 cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                cudaStream_t s) {
     const int items = p.m_tiles * (p.n_tiles / cn);
+    if (p.n_step == 256) {
+        switch (cn) {
+            case 4: return launch_qgemm<CfgW4DenseWide<4>>(tmA, tmB, p, items, s);
+            case 2: return launch_qgemm<CfgW4DenseWide<2>>(tmA, tmB, p, items, s);
+            default: return launch_qgemm<CfgW4DenseWide<1>>(tmA, tmB, p, items, s);
+        }
+    }
     switch (cn) {
         case 4: return launch_qgemm<CfgW4Dense<4>>(tmA, tmB, p, items, s);
         case 2: return launch_qgemm<CfgW4Dense<2>>(tmA, tmB, p, items, s);

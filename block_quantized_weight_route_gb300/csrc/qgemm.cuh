@@ -57,7 +57,18 @@ struct GemmCfg {
     // must not share its sub-partition with ALU-heavy converter warps, or its
     // mbarrier waits are starved and the tensor pipe idles.
     static constexpr int EPI_BASE = (EPI_WARPS_ == 4) ? 12 : 4;
-    static constexpr int THREADS = 512;
+    // 16 fold warps (FP8 with two row sub-tiles): 20 warps, five per
+    // sub-partition (a sixth would cap registers at 80), the two converters on
+    // warps 2 and 3
+    static constexpr int THREADS = (EPI_WARPS_ == 16) ? 32 * 20 : 512;
+    // one CTA per SM: each sub-partition's 16384 registers shared by its warps,
+    // in the allocation unit of 8 per thread
+    static constexpr int WARPS_PER_SMSP = (THREADS / 32 + 3) / 4;
+    static constexpr int MAXNREG_RAW = 16384 / (WARPS_PER_SMSP * 32) / 8 * 8;
+    static constexpr int MAXNREG = MAXNREG_RAW > 255 ? 255 : MAXNREG_RAW;
+    // fold epilogue: token columns per warp, and the TMEM load width
+    static constexpr int FOLD_CPW = 128 / (EPI_WARPS_ >= 8 ? EPI_WARPS_ / 4 : 1);
+    static constexpr int FOLD_LDW = (EPI_WARPS_ == 16) ? 16 : 32;
     static constexpr int TSTAGES = TSTAGES_, CSTAGES = CSTAGES_;
     // raw (TMA) stage: bf16 activation tile (read by the MMA in place) + weight codes
     static constexpr int A_RAW_BYTES = BM * BK * 2;
@@ -72,28 +83,38 @@ struct GemmCfg {
     static_assert(GROUP_K == 0 || GROUP_K == 2 * BK, "fold groups span two K blocks");
     static constexpr int NBUF = 512 / (BN * MSUB_);
     static constexpr uint32_t IDESC = idesc_kind_f16(128, BN, true);
-    static constexpr int TPR = CONV_WARPS_ * 32 / BN_;   // converter threads per weight row
+    // converter threads per weight row, or weight rows per converter thread
+    static constexpr int TPR = (CONV_WARPS_ * 32 >= BN_) ? CONV_WARPS_ * 32 / BN_ : 1;
+    static constexpr int RPT = (CONV_WARPS_ * 32 >= BN_) ? 1 : BN_ / (CONV_WARPS_ * 32);
     static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * NBUF + 1;
     static constexpr int SMEM_BYTES =
         1024 /*align slack*/ + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES + BAR_COUNT * 8 + 64;
     static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
-    static_assert(!FOLD || EPI_WARPS == 8, "fold epilogue splits columns over two warpgroups");
+    static_assert(!FOLD || EPI_WARPS == 8 || EPI_WARPS == 16, "fold epilogue: two or four warps per lane quarter");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
     static_assert(TPR == 1 || (TPR == 2 && B_ == BMode::W4), "one or (W4) two converter threads per weight row");
-    static_assert(CONV_WARPS * 32 == TPR * BN, "converters cover the weight rows");
+    static_assert(CONV_WARPS * 32 * RPT == TPR * BN, "converters cover the weight rows");
+    static_assert(RPT == 1 || (RPT == 2 && B_ == BMode::FP8), "two rows per converter thread: FP8 only");
     static_assert(MSUB == 1 || MSUB == 2, "row sub-tiles");
-    static_assert(MSUB == 1 || !FOLD, "the fold epilogue uses one row sub-tile");
+    static_assert(MSUB == 1 || !FOLD || EPI_WARPS == 16, "two-sub-tile folds need 16 fold warps (registers)");
     static_assert(NBUF >= 1, "TMEM columns");
     static_assert(CLUSTER_N == 1 || CLUSTER_N == 2 || CLUSTER_N == 4, "cluster size");
-    static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4), "warp layout");
+    static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4) ||
+                      (EPI_WARPS == 16 && CONV_WARPS == 2),
+                  "warp layout");
     // converter slot of a warp, -1 if it is not a converter:
-    //   4 epilogue warps (12..15): converters on warps 2,3,4,6,7,8,10,11
-    //   8 epilogue warps (4..11):  converters on warps 2,3,12,14
+    //   4 epilogue warps (12..15):  converters on warps 2,3,4,6,7,8,10,11
+    //   8 epilogue warps (4..11):   converters on warps 2,3,12,14
+    //   16 epilogue warps (4..19):  converters on warps 2,3
     __device__ static int conv_slot(int warp) {
-        // slot + 1 per warp, one nibble each (0: not a converter)
-        constexpr unsigned long long tab = (EPI_WARPS == 4) ? 0x870654032100ull : 0x403000000002100ull;
-        return (int)((tab >> (4 * warp)) & 15u) - 1;
+        if constexpr (EPI_WARPS == 16) {
+            return (warp == 2 || warp == 3) ? warp - 2 : -1;
+        } else {
+            // slot + 1 per warp, one nibble each (0: not a converter)
+            constexpr unsigned long long tab = (EPI_WARPS == 4) ? 0x870654032100ull : 0x403000000002100ull;
+            return (int)((tab >> (4 * warp)) & 15u) - 1;
+        }
     }
 };
 
@@ -226,23 +247,34 @@ __device__ __forceinline__ void convert_w4_half(uint32_t raw_tile, uint32_t dst_
     }
 }
 
-// FP8: 64 E4M3 bytes (64-byte-swizzled rows) -> exact bf16.
-__device__ __forceinline__ void convert_fp8_row(uint32_t raw_tile, uint32_t dst_tile, int r) {
-    const int sw = (r >> 1) & 3;
+// FP8: RPT rows (r0, r0 + rstride, ...) of 64 E4M3 bytes (64-byte-swizzled rows) -> exact bf16.
+template <int RPT>
+__device__ __forceinline__ void convert_fp8_rows(uint32_t raw_tile, uint32_t dst_tile, int r0, int rstride) {
+    // all raw chunks first: the shared loads overlap instead of each waiting on the last store
+    uint4 v[RPT][4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint4 v = lds128(raw_tile + r * 64 + ((c ^ sw) << 4));
-        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[8];
+    for (int rr = 0; rr < RPT; ++rr) {
+        const int r = r0 + rr * rstride, sw = (r >> 1) & 3;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            uint32_t h[2];
-            cvt_e4m3x4_f16x2(words[w], h);
-            o[2 * w] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[0]), kBf16x2_2p112);
-            o[2 * w + 1] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[1]), kBf16x2_2p112);
+        for (int c = 0; c < 4; ++c) v[rr][c] = lds128(raw_tile + r * 64 + ((c ^ sw) << 4));
+    }
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) {
+        const int r = r0 + rr * rstride;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t words[4] = {v[rr][c].x, v[rr][c].y, v[rr][c].z, v[rr][c].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                uint32_t h[2];
+                cvt_e4m3x4_f16x2(words[w], h);
+                o[2 * w] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[0]), kBf16x2_2p112);
+                o[2 * w + 1] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[1]), kBf16x2_2p112);
+            }
+            sts128(dst_tile + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
+            sts128(dst_tile + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
         }
-        sts128(dst_tile + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
-        sts128(dst_tile + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -314,7 +346,7 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -519,7 +551,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                         // TMEM lane quarter of this warp
-        const int half = (warp - C::EPI_BASE) >> 2;     // column half (fold epilogue only)
         const int row = q * 32 + lane;                  // accumulator row = TMEM lane
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
         int buf = 0;
@@ -633,28 +664,39 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     bph ^= 1u;
                 }
             } else {
-                // FP8 fold: one accumulator per 128-K block, folded into registers with its scale
-                const bool valid = row < ti.rows;
-                const long grow = (long)ti.row0 + row;
+                // FP8 fold: one accumulator per 128-K block and row sub-tile, folded into
+                // registers with its scale; FOLD_CPW token columns per warp
+                constexpr int CPW = C::FOLD_CPW, LDW = C::FOLD_LDW;
+                const int cq = (warp - C::EPI_BASE) >> 2;      // this warp's block of CPW columns
+                const int nsub = min(C::MSUB, (ti.rows + 127) / 128);
                 const int groups = p.K / C::GROUP_K;
-                float sum[64];
+                float sum[C::MSUB][CPW];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) sum[j] = 0.f;
+                for (int m = 0; m < C::MSUB; ++m)
+#pragma unroll
+                    for (int j = 0; j < CPW; ++j) sum[m][j] = 0.f;
                 for (int g = 0; g < groups; ++g) {
+                    const float s = __ldg(p.blk_scale + (long)(ti.n0 / 128) * groups + g);
                     if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const float s = __ldg(p.blk_scale + (long)(ti.n0 / 128) * groups + g);
-                    const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + half * 64);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(acc + c * 32, r);
-                        tmem_ld_wait();
+                    for (int m = 0; m < C::MSUB; ++m) {
+                        if (m < nsub) {
+                            const uint32_t acc = lane_addr + (uint32_t)(buf * C::MSUB * C::BN + m * C::BN + cq * CPW);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sum[c * 32 + j] = fmaf(s, __uint_as_float(r[j]), sum[c * 32 + j]);
+                            for (int c = 0; c < CPW / LDW; ++c) {
+                                uint32_t r[LDW];
+                                if constexpr (LDW == 32) tmem_ld32(acc + c * LDW, r);
+                                else tmem_ld16(acc + c * LDW, r);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < LDW; ++j)
+                                    sum[m][c * LDW + j] = fmaf(s, __uint_as_float(r[j]), sum[m][c * LDW + j]);
+                            }
+                        }
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -665,18 +707,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                if (valid) {
-                    const int col = ti.n0 + half * 64;
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint32_t w[4];
+                for (int m = 0; m < C::MSUB; ++m) {
+                    if (m < nsub && m * 128 + row < ti.rows) {
+                        const long grow = (long)ti.row0 + m * 128 + row;
+                        const int col = ti.n0 + cq * CPW;
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            __nv_bfloat162 b = __floats2bfloat162_rn(sum[8 * j + 2 * i], sum[8 * j + 2 * i + 1]);
-                            w[i] = *reinterpret_cast<uint32_t*>(&b);
+                        for (int j = 0; j < CPW / 8; ++j) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                __nv_bfloat162 b = __floats2bfloat162_rn(sum[m][8 * j + 2 * i], sum[m][8 * j + 2 * i + 1]);
+                                w[i] = *reinterpret_cast<uint32_t*>(&b);
+                            }
+                            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                        dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
@@ -764,7 +810,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     else
                         convert_w4_row(braw, bconv, crow, sbytes);
                 } else {
-                    convert_fp8_row(braw, bconv, crow);
+                    convert_fp8_rows<C::RPT>(braw, bconv, crow, C::BN / C::RPT);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();

@@ -42,6 +42,14 @@ cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, c
                                cudaStream_t s);
 cudaError_t launch_w4_gate_up_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                      cudaStream_t s);
+// token rows and weight rows (gate + up for the gate/up product) of one W4 tile
+struct TileShape {
+    int rows, bn;
+};
+TileShape w4_dense_shape(int M, int N, int sms);   // the launch picks the kernel by n_step (128 or 256)
+TileShape w4_gate_up_shape();
+// token rows of one FP8 tile (the activation box height before the cluster split)
+int fp8_tile_rows();
 cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                               cudaStream_t s);
 cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,

@@ -114,6 +114,18 @@ def test_w4a16_full_size_sampled(qlib):
     check_bf16_output(bf16_to_np(Y)[np.ix_(rows, cols)], ref)
 
 
+def test_w4a16_wide_tiles_ragged_sampled(qlib):
+    """A shape with enough tiles that 256 x 256 tiles are chosen on a 152-SM part
+    (M=2000, N=17440: ragged in M and in N, whose last tile holds 32 weight rows)."""
+    M, K, N = 2000, 256, 17440
+    g = wl.gen_w4a16(M, K, N, 1.0 / 64, seed=91)
+    Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"]))
+    rows = np.array([0, 127, 128, 255, 256, 1791, 1792, 1999])
+    cols = np.concatenate([np.arange(0, N, 53), np.arange(17376, N)])
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"], rows=rows, cols=cols)
+    assert rel_err(Y.cpu().numpy().astype(np.float64)[np.ix_(rows, cols)], ref) <= 1e-5
+
+
 def test_w4a16_router_shape_sampled(qlib):
     """The router projection in front of routing, logits = X . W_r^T (one W4 row
     per expert), at the sources' router shape; fp32 logits."""
