@@ -302,25 +302,6 @@ __device__ __forceinline__ void convert_iq4_row(uint32_t raw_tile, uint32_t dst_
     }
 }
 
-// int8: 64 codes (64-byte-swizzled rows) -> exact f16.
-__device__ __forceinline__ void convert_i8_row(uint32_t raw_tile, uint32_t dst_tile, int r) {
-    const int sw = (r >> 1) & 3;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint4 v = lds128(raw_tile + r * 64 + ((c ^ sw) << 4));
-        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const uint32_t x = words[w] ^ 0x80808080u;
-            o[2 * w] = f16x2_sub(prmt(x, 0x64646464u, 0x5140u), kF16x2_1152);
-            o[2 * w + 1] = f16x2_sub(prmt(x, 0x64646464u, 0x5342u), kF16x2_1152);
-        }
-        sts128(dst_tile + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
-        sts128(dst_tile + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
-    }
-}
-
 // Wait (bounded) for the completion of the `issued` most recent fills of a ring.
 __device__ __forceinline__ void drain_ring(uint64_t* full, long issued, int stages, uint32_t* err) {
     const long pending = issued < stages ? issued : stages;
