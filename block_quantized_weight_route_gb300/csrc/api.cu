@@ -47,6 +47,12 @@ struct DeviceState {
     std::string why;
     int sms = 0;
     uint32_t* err = nullptr;
+    // dense GEMMs' K-split scratch (allocated at the first dense call): partial
+    // tiles for up to one per SM of 256 x 256 fp32; dense calls are ordered
+    // through split_done so that calls on different streams never share it at
+    // the same time
+    float* split_part = nullptr;
+    cudaEvent_t split_done = nullptr;
 };
 
 constexpr int kMaxDevices = 64;
@@ -94,6 +100,25 @@ qmm_status device_state(DeviceState** out) {
     if (d.status != QMM_OK) return fail(d.status, "%s", d.why.c_str());
     *out = &d;
     return QMM_OK;
+}
+
+// The dense GEMMs' K-split scratch of this device, allocated once.
+static qmm_status split_scratch(DeviceState* d, GemmParams* p, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d->split_part) {
+        cudaError_t e = cudaMalloc(&d->split_part, sizeof(float) * 65536 * (size_t)d->sms);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(split scratch)");
+        e = cudaEventCreateWithFlags(&d->split_done, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(split)");
+    }
+    p->split_part = d->split_part;
+    p->split_part_cap = 65536L * d->sms;
+    cudaError_t e = cudaStreamWaitEvent(stream, d->split_done, 0);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "cudaStreamWaitEvent(split)");
+}
+static qmm_status split_scratch_release(DeviceState* d, cudaStream_t stream) {
+    cudaError_t e = cudaEventRecord(d->split_done, stream);
+    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "cudaEventRecord(split)");
 }
 
 // 2-D tiled tensor map over a row-major [outer][inner] matrix.
@@ -236,9 +261,10 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     p.ydt = (ydt == QMM_BF16) ? 1 : 0;
     p.ldy = N;
     p.err = d->err;
+    if ((st = split_scratch(d, &p, stream)) != QMM_OK) return st;
     cudaError_t e = launch_w4a16_dense(ta, tb, p, cn, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_w4a16 launch");
-    return QMM_OK;
+    return split_scratch_release(d, stream);
 }
 
 qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t* W, const float* S, uint16_t* Y,
@@ -272,9 +298,10 @@ qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t*
     p.ydt = 1;
     p.ldy = N;
     p.err = d->err;
+    if ((st = split_scratch(d, &p, stream)) != QMM_OK) return st;
     cudaError_t e = launch_fp8_blk128(ta, tb, p, cn, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_fp8_blk128 launch");
-    return QMM_OK;
+    return split_scratch_release(d, stream);
 }
 
 size_t moe_route_workspace_size(int T, int E, int k) {

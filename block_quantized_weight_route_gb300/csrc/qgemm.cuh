@@ -92,6 +92,8 @@ struct GemmCfg {
     static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
     static_assert(!FOLD || EPI_WARPS == 8 || EPI_WARPS == 16, "fold epilogue: two or four warps per lane quarter");
+    static_assert(!FOLD || FOLD_CPW % 8 == 0, "fold columns per warp: whole 16-byte runs");
+    static_assert(GROUPED_ || 128 * MSUB_ * BN_ <= 65536, "split partial tile at most 256 x 256");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
     static_assert(TPR == 1 || (TPR == 2 && B_ == BMode::W4), "one or (W4) two converter threads per weight row");
     static_assert(CONV_WARPS * 32 * RPT == TPR * BN, "converters cover the weight rows");
@@ -120,6 +122,8 @@ struct GemmCfg {
 
 struct TileInfo {
     int expert, row0, rows, n0, entry;
+    int kb0, kb1;   // K blocks [kb0, kb1) of this work item
+    int split, s;   // dense K split: index of the split tile and of this split, or split = -1
 };
 
 // Work item g of a cluster: one block of activation rows and CLUSTER_N
@@ -138,13 +142,36 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int g, int 
         ti.n0 = nt * p.n_step;
         // index of the first 128-row routing entry the tile covers (two per tile when MSUB == 2)
         ti.entry = (C::MSUB == 2) ? e4.w : entry;
+        ti.kb0 = 0;
+        ti.kb1 = p.K / C::BK;
+        ti.split = -1;
+        ti.s = 0;
     } else {
-        const int mt = g % p.m_tiles, nt = (g / p.m_tiles) * C::CLUSTER_N + crank;
+        // items from split_from on: split_S K ranges (whole 4-K-block chunks) per tile
+        int tile = g, split = -1, s = 0;
+        if (g >= p.split_from) {
+            const int j = g - p.split_from;
+            split = j / p.split_S;
+            s = j - split * p.split_S;
+            tile = p.split_from + split;
+        }
+        const int mt = tile % p.m_tiles, nt = (tile / p.m_tiles) * C::CLUSTER_N + crank;
         ti.expert = 0;
         ti.row0 = mt * C::BM;
         ti.rows = min(C::BM, p.M - ti.row0);
         ti.n0 = nt * p.n_step;
         ti.entry = mt;
+        const int kblocks = p.K / C::BK;
+        if (split >= 0) {
+            const int nch = kblocks / 4;
+            ti.kb0 = 4 * (s * nch / p.split_S);
+            ti.kb1 = 4 * ((s + 1) * nch / p.split_S);
+        } else {
+            ti.kb0 = 0;
+            ti.kb1 = kblocks;
+        }
+        ti.split = split;
+        ti.s = s;
     }
     return ti;
 }
@@ -326,6 +353,65 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     return v;
 }
 
+// 32 consecutive outputs of one row, times s2, as fp32 or bf16 (RNE).
+__device__ __forceinline__ void store_out32(const GemmParams& p, long grow, int col, const float (&v)[32], float s2) {
+    if (p.ydt == 0) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + grow * p.ldy + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(v[4 * j] * s2, v[4 * j + 1] * s2, v[4 * j + 2] * s2, v[4 * j + 3] * s2);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * j + 2 * i] * s2, v[8 * j + 2 * i + 1] * s2);
+                w[i] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// K splits of the last wave: out[tile rows, tile columns] = scale x (sum of the
+// S partial tiles in split order), one thread per 4 consecutive columns; rows
+// and columns outside [M, N) are not written.  Partials as in GemmParams.
+static __global__ void __launch_bounds__(256) split_reduce_kernel(GemmParams p, int BM, int BN, int CN, int rem, float scale) {
+    const long per_tile = (long)BM * (BN / 4);
+    const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long)rem * CN * per_tile) return;
+    const int pair = (int)(idx / per_tile);                 // split tile x cluster rank
+    const int within = (int)(idx - (long)pair * per_tile);
+    const int r = within / (BN / 4), c4 = within - r * (BN / 4);
+    const int j = pair / CN, crank = pair - j * CN;
+    const int tile = p.split_from + j;
+    const int mt = tile % p.m_tiles, nt = (tile / p.m_tiles) * CN + crank;
+    const long grow = (long)mt * BM + r;
+    const int col = nt * p.n_step + c4 * 4;
+    if (grow >= p.M || col >= p.N) return;
+    const float4* src = reinterpret_cast<const float4*>(p.split_part + (long)pair * p.split_S * BM * BN + (long)r * BN) + c4;
+    const long sstride = (long)BM * BN / 4;
+    float4 v = __ldcg(src);
+    for (int s = 1; s < p.split_S; ++s) {
+        const float4 x = __ldcg(src + s * sstride);
+        v.x += x.x;
+        v.y += x.y;
+        v.z += x.z;
+        v.w += x.w;
+    }
+    if (p.ydt == 0) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.Y) + grow * p.ldy + col) =
+            make_float4(v.x * scale, v.y * scale, v.z * scale, v.w * scale);
+    } else {
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+        __nv_bfloat162 b = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
@@ -375,7 +461,6 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int kblocks = p.K / C::BK;
     const int crank = (C::CLUSTER_N > 1) ? (int)cluster_ctarank() : 0;
     const int cid = (C::CLUSTER_N > 1) ? (int)cluster_id_x() : (int)blockIdx.x;
     const int ncl = (C::CLUSTER_N > 1) ? (int)cluster_count_x() : (int)gridDim.x;
@@ -384,7 +469,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         const int entries = min(*p.num_entries, p.max_entries);
         num_tiles = entries * (p.n_tiles / C::CLUSTER_N);
     } else {
-        num_tiles = p.m_tiles * (p.n_tiles / C::CLUSTER_N);
+        const int items = p.m_tiles * (p.n_tiles / C::CLUSTER_N);
+        num_tiles = (p.split_S > 1) ? p.split_from + (items - p.split_from) * p.split_S : items;
     }
 
     if (warp == 0) {
@@ -399,7 +485,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             for (int t = cid; t < num_tiles && ok; t += ncl) {
                 const TileInfo ti = ti_next;                 // read one tile ahead
                 if (t + ncl < num_tiles) ti_next = decode_tile<C>(p, t + ncl, crank);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                     const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
                     if (__any_sync(0xffffffffu, !got)) {
                         ok = false;
@@ -444,16 +530,16 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             int ts = 0, cs = 0, buf = 0;
             uint32_t tph = 0, cph = 0, bph = 0;
             bool ok = true;
-            // sub-tiles holding at least one live row (a tile of <= 128 rows skips the
-            // second), read one tile ahead so the descriptor load is off the issue path
-            int nsub_next = C::MSUB;
-            if constexpr (C::MSUB == 2)
-                if (cid < num_tiles) nsub_next = (decode_tile<C>(p, cid, crank).rows > 128) ? 2 : 1;
+            // the work item, read one ahead so the descriptor load is off the issue
+            // path: its K range, and the sub-tiles holding at least one live row (a
+            // tile of <= 128 rows skips the second)
+            TileInfo mi_next{};
+            if (cid < num_tiles) mi_next = decode_tile<C>(p, cid, crank);
             for (int t = cid; t < num_tiles && ok; t += ncl) {
-                const int nsub = nsub_next;
-                if constexpr (C::MSUB == 2)
-                    if (t + ncl < num_tiles) nsub_next = (decode_tile<C>(p, t + ncl, crank).rows > 128) ? 2 : 1;
-                for (int kb = 0; kb < kblocks && ok; ++kb) {
+                const TileInfo mi = mi_next;
+                if (t + ncl < num_tiles) mi_next = decode_tile<C>(p, t + ncl, crank);
+                const int nsub = (C::MSUB == 2 && mi.rows <= 128) ? 1 : C::MSUB;
+                for (int kb = mi.kb0; kb < mi.kb1 && ok; ++kb) {
                     bool got = mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL);
                     got = got && mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
                     if (__any_sync(0xffffffffu, !got)) {
@@ -466,16 +552,16 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     const uint32_t b_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-                        // first / last MMA of an accumulation group (the whole K, or one
-                        // 128-K block = two K blocks for the FP8 fold); no divisions here:
-                        // this loop sits between consecutive MMA issues
+                        // first / last MMA of an accumulation group (the item's K range, or
+                        // one 128-K block = two K blocks for the FP8 fold); no divisions
+                        // here: this loop sits between consecutive MMA issues
                         bool first, last;
                         if constexpr (C::GROUP_K == 128) {
                             first = (kk == 0) && ((kb & 1) == 0);
                             last = (kk == C::BK / C::UMMA_K - 1) && ((kb & 1) == 1);
                         } else {
-                            first = (kk == 0) && (kb == 0);
-                            last = (kk == C::BK / C::UMMA_K - 1) && (kb == kblocks - 1);
+                            first = (kk == 0) && (kb == mi.kb0);
+                            last = (kk == C::BK / C::UMMA_K - 1) && (kb == mi.kb1 - 1);
                         }
                         if (first) {
                             const bool free = mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err,
@@ -537,6 +623,11 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         int buf = 0;
         uint32_t bph = 0;
         bool ok = true;
+        // K splits: this CTA's partial tile of split s, [BM][BN] fp32
+        constexpr long kTileFloats = (long)C::BM * C::BN;
+        auto split_part = [&](const TileInfo& tt, int s_) -> float* {
+            return p.split_part + ((long)(tt.split * C::CLUSTER_N + crank) * p.split_S + s_) * kTileFloats;
+        };
         for (int t = cid; t < num_tiles && ok; t += ncl) {
             const TileInfo ti = decode_tile<C>(p, t, crank);
             if constexpr (!C::FOLD) {
@@ -553,35 +644,24 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     const long grow = (long)ti.row0 + m * 128 + row;
                     const uint32_t acc = lane_addr + (uint32_t)(buf * C::MSUB * C::BN + m * C::BN);
                     if constexpr (C::EPI == Epi::STORE) {
-                        const float s2 = p.scale2_dense;
     #pragma unroll 1
                         for (int c = 0; c < C::BN / 32; ++c) {
                             uint32_t r[32];
                             tmem_ld32(acc + c * 32, r);
                             tmem_ld_wait();
+                            float v[32];
+    #pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) v[jj] = __uint_as_float(r[jj]);
                             const int col = ti.n0 + c * 32;
-                            if (valid && col < p.N) {
-                                if (p.ydt == 0) {
-                                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + grow * p.ldy + col);
+                            if (ti.split >= 0) {
+                                // K split: the unscaled partial, every row and column of the tile
+                                float4* dst = reinterpret_cast<float4*>(split_part(ti, ti.s) +
+                                                                        (long)(m * 128 + row) * C::BN + c * 32);
     #pragma unroll
-                                    for (int j = 0; j < 8; ++j)
-                                        dst[j] = make_float4(__uint_as_float(r[4 * j]) * s2, __uint_as_float(r[4 * j + 1]) * s2,
-                                                             __uint_as_float(r[4 * j + 2]) * s2,
-                                                             __uint_as_float(r[4 * j + 3]) * s2);
-                                } else {
-                                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
-    #pragma unroll
-                                    for (int j = 0; j < 4; ++j) {
-                                        uint32_t w[4];
-    #pragma unroll
-                                        for (int i = 0; i < 4; ++i) {
-                                            __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]) * s2,
-                                                                                     __uint_as_float(r[8 * j + 2 * i + 1]) * s2);
-                                            w[i] = *reinterpret_cast<uint32_t*>(&b);
-                                        }
-                                        dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
-                                    }
-                                }
+                                for (int jj = 0; jj < 8; ++jj)
+                                    dst[jj] = make_float4(v[4 * jj], v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
+                            } else if (valid && col < p.N) {
+                                store_out32(p, grow, col, v, p.scale2_dense);
                             }
                         }
                     } else {   // SWIGLU_Q81: columns [0, BN/2) gate, [BN/2, BN) up
@@ -656,7 +736,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 for (int m = 0; m < C::MSUB; ++m)
 #pragma unroll
                     for (int j = 0; j < CPW; ++j) sum[m][j] = 0.f;
-                for (int g = 0; g < groups; ++g) {
+                for (int g = ti.kb0 / 2; g < ti.kb1 / 2; ++g) {
                     const float s = __ldg(p.blk_scale + (long)(ti.n0 / 128) * groups + g);
                     if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                         ok = false;
@@ -688,6 +768,21 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     }
                 }
                 if (!ok) break;
+                if (ti.split >= 0) {
+                    // K split: this split's folded sums, every row of the live sub-tiles;
+                    // the split-reduce kernel adds the splits and writes the output
+#pragma unroll
+                    for (int m = 0; m < C::MSUB; ++m) {
+                        if (m < nsub) {
+                            float4* dst = reinterpret_cast<float4*>(split_part(ti, ti.s) +
+                                                                    (long)(m * 128 + row) * C::BN + cq * CPW);
+#pragma unroll
+                            for (int j = 0; j < CPW / 4; ++j)
+                                dst[j] = make_float4(sum[m][4 * j], sum[m][4 * j + 1], sum[m][4 * j + 2], sum[m][4 * j + 3]);
+                        }
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int m = 0; m < C::MSUB; ++m) {
                     if (m < nsub && m * 128 + row < ti.rows) {
@@ -719,7 +814,6 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         // W4 scales: 16-byte loads covering 4 K blocks, one chunk ahead (K % 256 == 0),
         // else one 4-byte load per K block.
         const bool vec_scales = (p.K % 256) == 0;
-        const int kchunks = kblocks / 4;
         auto scale_row = [&](const TileInfo& tt, bool& in_range) -> long {
             if constexpr (C::EPI == Epi::SWIGLU_Q81) {
                 const int hr = (crow < C::BN / 2) ? (tt.n0 + crow) : (p.F + tt.n0 + crow - C::BN / 2);
@@ -731,22 +825,28 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             }
         };
         // Scale prefetch two 4-K-block chunks ahead, through a cursor that walks
-        // this CTA's tiles in the order they are converted: the next tile's
-        // descriptor is read one chunk before its first scales are needed, so
-        // neither global load (descriptor, then scales) sits on the critical path.
+        // this CTA's work items (and each item's K range) in the order they are
+        // converted: the next item's descriptor is read one chunk before its first
+        // scales are needed, so neither global load (descriptor, then scales) sits
+        // on the critical path.
         int pf_t = cid, pf_ch = 0;
         TileInfo pf_ti{};
-        if (pf_t < num_tiles) pf_ti = decode_tile<C>(p, pf_t, crank);
+        if (pf_t < num_tiles) {
+            pf_ti = decode_tile<C>(p, pf_t, crank);
+            pf_ch = pf_ti.kb0 / 4;
+        }
         auto next_chunk = [&]() -> uint4 {
             uint4 v = make_uint4(0, 0, 0, 0);
             if (pf_t < num_tiles) {
                 bool in_range;
                 const long wrow = scale_row(pf_ti, in_range);
                 if (in_range) v = ldg_nc_v4(p.w_scale + wrow * (p.K / 16) + pf_ch * 16);
-                if (++pf_ch == kchunks) {
-                    pf_ch = 0;
+                if (++pf_ch == pf_ti.kb1 / 4) {
                     pf_t += ncl;
-                    if (pf_t < num_tiles) pf_ti = decode_tile<C>(p, pf_t, crank);
+                    if (pf_t < num_tiles) {
+                        pf_ti = decode_tile<C>(p, pf_t, crank);
+                        pf_ch = pf_ti.kb0 / 4;
+                    }
                 }
             }
             return v;
@@ -760,7 +860,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         }
         for (int t = cid; t < num_tiles && ok; t += ncl) {
             const TileInfo ti = decode_tile<C>(p, t, crank);
-            for (int kb = 0; kb < kblocks; ++kb) {
+            for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                 uint32_t sbytes = 0;
                 if constexpr (C::B == BMode::W4) {
                     if (vec_scales) {
@@ -822,7 +922,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
 // Host-side launch of a GemmCfg instantiation: cluster launch when CLUSTER_N > 1,
 // persistent grid of (max co-resident clusters, capped by the work) x CLUSTER_N.
 template <class C>
-cudaError_t launch_qgemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int max_items,
+cudaError_t launch_qgemm(const CUtensorMap& tmA, const CUtensorMap& tmB, GemmParams p, int max_items,
                          cudaStream_t s) {
     static_assert(C::SMEM_BYTES <= 232448, "shared memory");
     cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -858,10 +958,36 @@ cudaError_t launch_qgemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const G
         max_clusters[dev] = n;
     }
     int clusters = max_clusters[dev];
+    p.split_S = 1;
+    if constexpr (!C::GROUPED) {
+        // Dense: when the last wave of tiles fills at most half the clusters, split
+        // each of its tiles into S K ranges (whole 4-K-block chunks, at least two
+        // per split) so that S x as many clusters share it.
+        const int items = p.m_tiles * (p.n_tiles / C::CLUSTER_N);
+        const int kblocks = p.K / C::BK;
+        const int full = items / clusters * clusters, rem = items - full;
+        p.split_from = items;
+        if (p.split_part && kblocks % 4 == 0 && rem > 0 && 2 * rem <= clusters) {
+            int S = clusters / rem;
+            if (S > 8) S = 8;
+            if (S > kblocks / 8) S = kblocks / 8;
+            if (S >= 2 && (long)rem * C::CLUSTER_N * S * C::BM * C::BN <= p.split_part_cap) {
+                p.split_from = full;
+                p.split_S = S;
+            }
+        }
+        max_items = p.split_from + (items - p.split_from) * p.split_S;
+    }
     if (max_items > 0 && max_items < clusters) clusters = max_items;
     cfg.gridDim = dim3(C::CLUSTER_N * clusters, 1, 1);
     e = cudaLaunchKernelEx(&cfg, qgemm_kernel<C>, tmA, tmB, p);
     if (e != cudaSuccess) return e;
+    if (p.split_S > 1) {
+        const int rem = (p.m_tiles * (p.n_tiles / C::CLUSTER_N)) - p.split_from;
+        const long threads = (long)rem * C::CLUSTER_N * C::BM * (C::BN / 4);
+        const float scale = (C::EPI == Epi::STORE) ? p.scale2_dense : 1.0f;
+        split_reduce_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, C::BM, C::BN, C::CLUSTER_N, rem, scale);
+    }
     return cudaGetLastError();
 }
 

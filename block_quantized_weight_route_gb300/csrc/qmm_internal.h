@@ -31,6 +31,15 @@ struct GemmParams {
     __half* Hs;             // gate/up: q8_1 s per 32-block [rows][F/32]
     float* Hd32;            // gate/up: fp32 value of the fp16 d, [entry][F/32][128 rows]
     uint32_t* err;          // device error word
+    // dense only: K splits of the last, partly filled wave of tiles.  Work items
+    // [split_from, ...) are split_S consecutive K ranges of the tiles (items)
+    // split_from, split_from + 1, ...; each split writes its fp32 partial tile
+    // to split_part, and a reduction kernel launched after the GEMM adds them in
+    // split order and writes the output.  split_S == 1: no splits.
+    int split_from;
+    int split_S;
+    float* split_part;      // [split tile][cluster rank][split][BM][BN] fp32 (null: never split)
+    long split_part_cap;    // floats available at split_part
 };
 
 // Launchers (return a cudaError_t from the launch).  Each takes two encoded

@@ -80,7 +80,23 @@ def test_w4a16_unit_scales_integer_inputs_are_exact(qlib):
     assert np.array_equal(Y.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("M,K,N", [(64, 512, 512), (1, 64, 32), (129, 192, 96), (300, 1024, 544)])
+def test_w4a16_k_split_integer_inputs_are_exact(qlib):
+    """Few tiles and a long K: the dense GEMM splits each tile's K range over
+    several CTAs (3 tiles on a 152-SM part: 4 splits) and adds the fp32 partials
+    in split order.  With unit scales and small-integer X every partial sum is
+    exact, so the result must equal the oracle exactly."""
+    rng = np.random.default_rng(2)
+    M, K, N = 150, 2048, 288
+    Xi = rng.integers(-20, 21, size=(M, K)).astype(np.float32)
+    X = torch.from_numpy(Xi).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    Wc = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    Ws = np.full((N, K // 16), 0x38, np.uint8)
+    Y = qlib.qmm_w4a16(bf16_dev(X), dev(Wc), dev(Ws), 1.0).cpu().numpy()
+    ref = oracle.w4a16(X, Wc, Ws, 1.0)
+    assert np.array_equal(Y.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("M,K,N", [(64, 512, 512), (1, 64, 32), (129, 192, 96), (300, 1024, 544), (40, 4096, 256)])
 def test_w4a16_matches_oracle(qlib, M, K, N):
     g = wl.gen_w4a16(M, K, N, 1.0 / 64, seed=M + K + N)
     Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"])).cpu().numpy()
@@ -154,7 +170,7 @@ def test_router_projection_then_expert_stage(qlib):
 
 # ---------------------------------------------------------------- dense FP8 block-128
 
-@pytest.mark.parametrize("M,K,N", [(130, 384, 256), (1, 128, 128), (257, 640, 384)])
+@pytest.mark.parametrize("M,K,N", [(130, 384, 256), (1, 128, 128), (257, 640, 384), (300, 2048, 640)])
 def test_fp8_blk128_matches_oracle(qlib, M, K, N):
     g = wl.gen_fp8_blk128(M, K, N, seed=M * 3 + N)
     Y = qlib.qmm_fp8_blk128(bf16_dev(g["X"]), dev(g["W"]), dev(g["S"]))
