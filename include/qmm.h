@@ -66,6 +66,14 @@ qmm_status qmm_check_status(cudaStream_t stream);
  *   Ws  [N][K/16] OCP E4M3 scale bytes
  *   Y   [M][N]    fp32 (ydt = QMM_F32) or bf16 rounded to nearest even (QMM_BF16)
  * fp32 accumulation.  Shapes: M >= 1, K % 64 == 0, N % 32 == 0.
+ * Scratch: when the last wave of tiles would leave at least half the SMs idle
+ * (few tiles, or a ragged last wave), its tiles are split along K over several
+ * CTAs and the fp32 partials are added in split order by a second kernel on the
+ * same stream; the result is deterministic for a given GPU.  The partials live
+ * in library-owned device memory (256 KB per SM, allocated at the first dense
+ * call on a device and kept); dense calls on different streams of one device
+ * are ordered one after another by the library (an event) so that they never
+ * share it at the same time.
  */
 qmm_status qmm_w4a16(const uint16_t *X, int M, int K, int N, const uint8_t *Wc, const uint8_t *Ws, float scale2,
                      void *Y, qmm_dtype ydt, cudaStream_t stream);
@@ -77,6 +85,8 @@ qmm_status qmm_w4a16(const uint16_t *X, int M, int K, int N, const uint8_t *Wc, 
  * "perf: strix-hip BF16 GEMMs via hipBLASLt", FP8 block-scaling twin commit.
  *   X [M][K] bf16;  W [N][K] OCP E4M3 bytes;  S [N/128][K/128] fp32;  Y [M][N] bf16 (RNE).
  * fp32 accumulation.  Shapes: M >= 1, K % 128 == 0, N % 128 == 0.
+ * Scratch and ordering: as qmm_w4a16 (K splits of the last wave add the folded
+ * partials in split order).
  */
 qmm_status qmm_fp8_blk128(const uint16_t *X, int M, int K, int N, const uint8_t *W, const float *S, uint16_t *Y,
                           cudaStream_t stream);
