@@ -858,51 +858,67 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 sc_next2 = next_chunk();
             }
         }
+        // one K block: wait for its raw codes and a free converted stage, expand,
+        // hand the stage to the MMA; false if a wait timed out
+        auto convert_step = [&](uint32_t sbytes) -> bool {
+            if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
+                !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY))
+                return false;
+            const uint32_t braw = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
+            const uint32_t bconv = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+            if constexpr (C::B == BMode::W4) {
+                if constexpr (C::TPR == 2)
+                    convert_w4_half(braw, bconv, crow, chalf, sbytes);
+                else
+                    convert_w4_row(braw, bconv, crow, sbytes);
+            } else {
+                convert_fp8_rows<C::RPT>(braw, bconv, crow, C::BN / C::RPT);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_c[cs]);
+            if (++ts == C::TSTAGES) {
+                ts = 0;
+                tph ^= 1u;
+            }
+            if (++cs == C::CSTAGES) {
+                cs = 0;
+                cph ^= 1u;
+            }
+            return true;
+        };
         for (int t = cid; t < num_tiles && ok; t += ncl) {
             const TileInfo ti = decode_tile<C>(p, t, crank);
-            for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
-                uint32_t sbytes = 0;
-                if constexpr (C::B == BMode::W4) {
-                    if (vec_scales) {
-                        if ((kb & 3) == 0) {
-                            sc_cur = sc_next;
-                            sc_next = sc_next2;
-                            sc_next2 = next_chunk();
+            if (C::B == BMode::W4 && vec_scales) {
+                // K % 256 == 0: the item's K range is whole 4-K-block chunks; the chunk's
+                // four scale words are picked at compile time in the unrolled steps
+                for (int ch = ti.kb0 >> 2; ch < (ti.kb1 >> 2) && ok; ++ch) {
+                    if constexpr (C::B == BMode::W4) {
+                        sc_cur = sc_next;
+                        sc_next = sc_next2;
+                        sc_next2 = next_chunk();
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t sbytes = (C::B == BMode::W4)
+                                                    ? (j == 0 ? sc_cur.x : (j == 1 ? sc_cur.y : (j == 2 ? sc_cur.z : sc_cur.w)))
+                                                    : 0u;
+                        if (!convert_step(sbytes)) {
+                            ok = false;
+                            break;
                         }
-                        const int j = kb & 3;
-                        sbytes = j == 0 ? sc_cur.x : (j == 1 ? sc_cur.y : (j == 2 ? sc_cur.z : sc_cur.w));
-                    } else {
+                    }
+                }
+            } else {
+                for (int kb = ti.kb0; kb < ti.kb1 && ok; ++kb) {
+                    uint32_t sbytes = 0;
+                    if constexpr (C::B == BMode::W4) {
                         bool in_range;
                         const long wrow = scale_row(ti, in_range);
                         sbytes = in_range ? __ldg(reinterpret_cast<const uint32_t*>(p.w_scale + wrow * (p.K / 16) + kb * 4))
                                           : 0u;
                     }
-                }
-                if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
-                    !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t braw = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
-                const uint32_t bconv = smem_u32(cstage + cs * C::CSTAGE_BYTES);
-                if constexpr (C::B == BMode::W4) {
-                    if constexpr (C::TPR == 2)
-                        convert_w4_half(braw, bconv, crow, chalf, sbytes);
-                    else
-                        convert_w4_row(braw, bconv, crow, sbytes);
-                } else {
-                    convert_fp8_rows<C::RPT>(braw, bconv, crow, C::BN / C::RPT);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full_c[cs]);
-                if (++ts == C::TSTAGES) {
-                    ts = 0;
-                    tph ^= 1u;
-                }
-                if (++cs == C::CSTAGES) {
-                    cs = 0;
-                    cph ^= 1u;
+                    if (!convert_step(sbytes)) ok = false;
                 }
             }
         }

@@ -288,72 +288,57 @@ cudaError_t launch_gather_rows(const uint16_t* X, const int32_t* src, int rows, 
     return cudaGetLastError();
 }
 
-// Y[t, :] = sum_j w[t, j] * Yslot[row[t, j], :], j ascending; one warp per token.
+// Y[t, :] = sum_j w[t, j] * Yslot[row[t, j], :], j ascending; one CTA of 256
+// threads per token, so that each slot row is read as one contiguous run (two
+// 16-byte vectors per thread per slot, 2k loads in flight per thread).
 // A row index outside [0, P) contributes nothing and raises DEV_BAD_ROW.
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ Yslot, int P,
                                                       const int32_t* __restrict__ row, const float* __restrict__ w,
-                                                      int T, int k, int vec_per_row, float4* __restrict__ Y,
-                                                      uint32_t* err) {
-    const int lane = threadIdx.x & 31;
-    const int warps = (gridDim.x * blockDim.x) >> 5;
-    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-        int rr[kMaxK];
-        float ww[kMaxK];
-        bool bad = false;
+                                                      int k, int vec_per_row, float4* __restrict__ Y, uint32_t* err) {
+    const long t = blockIdx.x;
+    int rr[kMaxK];
+    float ww[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+            rr[j] = __ldg(row + t * k + j);
+            ww[j] = __ldg(w + t * k + j);
+            if ((unsigned)rr[j] >= (unsigned)P) {   // the same for every thread of the CTA
+                if (threadIdx.x == 0) atomicCAS(err, 0u, (uint32_t)DEV_BAD_ROW);
+                rr[j] = 0;
+                ww[j] = 0.f;
+            }
+        }
+    }
+    for (int i = threadIdx.x; i < vec_per_row; i += 512) {
+        const bool two = i + 256 < vec_per_row;
+        float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) {
             if (j < k) {
-                rr[j] = __ldg(row + (long)t * k + j);
-                ww[j] = __ldg(w + (long)t * k + j);
-                bad |= (unsigned)rr[j] >= (unsigned)P;
+                const float4* src = Yslot + (long)rr[j] * vec_per_row + i;
+                const float4 v0 = __ldcs(src);
+                const float4 v1 = two ? __ldcs(src + 256) : make_float4(0.f, 0.f, 0.f, 0.f);
+                acc0.x = fmaf(ww[j], v0.x, acc0.x);
+                acc0.y = fmaf(ww[j], v0.y, acc0.y);
+                acc0.z = fmaf(ww[j], v0.z, acc0.z);
+                acc0.w = fmaf(ww[j], v0.w, acc0.w);
+                acc1.x = fmaf(ww[j], v1.x, acc1.x);
+                acc1.y = fmaf(ww[j], v1.y, acc1.y);
+                acc1.z = fmaf(ww[j], v1.z, acc1.z);
+                acc1.w = fmaf(ww[j], v1.w, acc1.w);
             }
         }
-        if (bad) {          // warp-uniform (every lane read the same token's slots)
-            if (lane == 0) atomicCAS(err, 0u, (uint32_t)DEV_BAD_ROW);
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                if (j < k && (unsigned)rr[j] >= (unsigned)P) {
-                    rr[j] = 0;
-                    ww[j] = 0.f;
-                }
-            }
-        }
-        // two column vectors per lane per pass: 2k independent 16-byte loads in flight
-        for (int i = lane; i < vec_per_row; i += 64) {
-            const bool two = i + 32 < vec_per_row;
-            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                if (j < k) {
-                    const float4* src = Yslot + (long)rr[j] * vec_per_row + i;
-                    const float4 v0 = __ldcs(src);
-                    const float4 v1 = two ? __ldcs(src + 32) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    acc0.x = fmaf(ww[j], v0.x, acc0.x);
-                    acc0.y = fmaf(ww[j], v0.y, acc0.y);
-                    acc0.z = fmaf(ww[j], v0.z, acc0.z);
-                    acc0.w = fmaf(ww[j], v0.w, acc0.w);
-                    acc1.x = fmaf(ww[j], v1.x, acc1.x);
-                    acc1.y = fmaf(ww[j], v1.y, acc1.y);
-                    acc1.z = fmaf(ww[j], v1.z, acc1.z);
-                    acc1.w = fmaf(ww[j], v1.w, acc1.w);
-                }
-            }
-            Y[(long)t * vec_per_row + i] = acc0;
-            if (two) Y[(long)t * vec_per_row + i + 32] = acc1;
-        }
+        Y[t * vec_per_row + i] = acc0;
+        if (two) Y[t * vec_per_row + i + 256] = acc1;
     }
 }
 
 cudaError_t launch_combine(const float* Yslot, int P, const int32_t* row, const float* w, int T, int k, int D,
                            float* Y, uint32_t* err, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    int sms = 148;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = min((T + 7) / 8, sms * 8);
-    combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(Yslot), P, row, w, T, k, D / 4,
-                                        reinterpret_cast<float4*>(Y), err);
+    combine_kernel<<<T, 256, 0, s>>>(reinterpret_cast<const float4*>(Yslot), P, row, w, k, D / 4,
+                                     reinterpret_cast<float4*>(Y), err);
     return cudaGetLastError();
 }
 
