@@ -42,7 +42,7 @@ METRIC = "MoE expert-stage prefill tokens/s; quant-GEMM TFLOP/s vs GB300 tensor 
 # DRAM bytes (read + write) per launch of each stage kernel on the 5268-token
 # workload, from one ncu capture of the kernel as it stands (profiles/); None
 # once a kernel changes after its capture.
-DRAM_TRAFFIC = {"down": 182.84e6 + 289.72e6, "gate_up": None}
+DRAM_TRAFFIC = {"down": 182.84e6 + 289.72e6, "gate_up": 472.55e6 + 61.48e6}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

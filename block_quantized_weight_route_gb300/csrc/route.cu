@@ -288,11 +288,12 @@ cudaError_t launch_gather_rows(const uint16_t* X, const int32_t* src, int rows, 
     return cudaGetLastError();
 }
 
-// Y[t, :] = sum_j w[t, j] * Yslot[row[t, j], :], j ascending; one CTA of 256
+// Y[t, :] = sum_j w[t, j] * Yslot[row[t, j], :], j ascending; one CTA of NT
 // threads per token, so that each slot row is read as one contiguous run (two
 // 16-byte vectors per thread per slot, 2k loads in flight per thread).
 // A row index outside [0, P) contributes nothing and raises DEV_BAD_ROW.
-__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ Yslot, int P,
+template <int NT>
+__global__ void __launch_bounds__(NT) combine_kernel(const float4* __restrict__ Yslot, int P,
                                                       const int32_t* __restrict__ row, const float* __restrict__ w,
                                                       int k, int vec_per_row, float4* __restrict__ Y, uint32_t* err) {
     const long t = blockIdx.x;
@@ -310,15 +311,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
             }
         }
     }
-    for (int i = threadIdx.x; i < vec_per_row; i += 512) {
-        const bool two = i + 256 < vec_per_row;
+    for (int i = threadIdx.x; i < vec_per_row; i += 2 * NT) {
+        const bool two = i + NT < vec_per_row;
         float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) {
             if (j < k) {
                 const float4* src = Yslot + (long)rr[j] * vec_per_row + i;
                 const float4 v0 = __ldcs(src);
-                const float4 v1 = two ? __ldcs(src + 256) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 v1 = two ? __ldcs(src + NT) : make_float4(0.f, 0.f, 0.f, 0.f);
                 acc0.x = fmaf(ww[j], v0.x, acc0.x);
                 acc0.y = fmaf(ww[j], v0.y, acc0.y);
                 acc0.z = fmaf(ww[j], v0.z, acc0.z);
@@ -330,15 +331,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
             }
         }
         Y[t * vec_per_row + i] = acc0;
-        if (two) Y[t * vec_per_row + i + 256] = acc1;
+        if (two) Y[t * vec_per_row + i + NT] = acc1;
     }
 }
 
 cudaError_t launch_combine(const float* Yslot, int P, const int32_t* row, const float* w, int T, int k, int D,
                            float* Y, uint32_t* err, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    combine_kernel<<<T, 256, 0, s>>>(reinterpret_cast<const float4*>(Yslot), P, row, w, k, D / 4,
-                                     reinterpret_cast<float4*>(Y), err);
+    // one pass over the row where a CTA size fits it exactly (D = 2560: 320 threads)
+    const int vec = D / 4;
+    const float4* ys = reinterpret_cast<const float4*>(Yslot);
+    float4* y = reinterpret_cast<float4*>(Y);
+    if (vec == 640)
+        combine_kernel<320><<<T, 320, 0, s>>>(ys, P, row, w, k, vec, y, err);
+    else
+        combine_kernel<256><<<T, 256, 0, s>>>(ys, P, row, w, k, vec, y, err);
     return cudaGetLastError();
 }
 

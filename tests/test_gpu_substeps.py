@@ -107,7 +107,7 @@ def test_dbg_down_iq4_extreme_codes_exact(qlib):
     assert np.array_equal(Ys.cpu().numpy().astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("T,k,D", [(300, 2, 256), (1, 8, 128), (1000, 16, 64)])
+@pytest.mark.parametrize("T,k,D", [(300, 2, 256), (1, 8, 128), (1000, 16, 64), (50, 8, 2560), (20, 4, 3072)])
 def test_dbg_combine_matches_oracle(qlib, T, k, D):
     E = max(2 * k, 8)
     logits = (2.0 * wl.normal(31, 1, T * E)).astype(np.float32).reshape(T, E)
