@@ -103,7 +103,15 @@ qmm_status device_state(DeviceState** out) {
 }
 
 // The dense GEMMs' K-split scratch of this device, allocated once.
+// Under stream capture the calls do not split (no scratch, no event), so a graph
+// never holds library-owned memory that two replays could share.
+static bool capturing(cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
+}
 static qmm_status split_scratch(DeviceState* d, GemmParams* p, cudaStream_t stream) {
+    p->split_part = nullptr;
+    if (capturing(stream)) return QMM_OK;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!d->split_part) {
         cudaError_t e = cudaMalloc(&d->split_part, sizeof(float) * 65536 * (size_t)d->sms);
@@ -117,6 +125,7 @@ static qmm_status split_scratch(DeviceState* d, GemmParams* p, cudaStream_t stre
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "cudaStreamWaitEvent(split)");
 }
 static qmm_status split_scratch_release(DeviceState* d, cudaStream_t stream) {
+    if (capturing(stream)) return QMM_OK;
     cudaError_t e = cudaEventRecord(d->split_done, stream);
     return e == cudaSuccess ? QMM_OK : cuda_fail(e, "cudaEventRecord(split)");
 }

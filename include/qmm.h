@@ -73,7 +73,8 @@ qmm_status qmm_check_status(cudaStream_t stream);
  * in library-owned device memory (256 KB per SM, allocated at the first dense
  * call on a device and kept); dense calls on different streams of one device
  * are ordered one after another by the library (an event) so that they never
- * share it at the same time.
+ * share it at the same time.  On a stream that is being captured into a graph
+ * the calls never split (no scratch, no event).
  */
 qmm_status qmm_w4a16(const uint16_t *X, int M, int K, int N, const uint8_t *Wc, const uint8_t *Ws, float scale2,
                      void *Y, qmm_dtype ydt, cudaStream_t stream);

@@ -153,6 +153,31 @@ def test_w4a16_router_shape_sampled(qlib):
     assert rel_err(Y.cpu().numpy().astype(np.float64)[rows], ref) <= 1e-5
 
 
+def test_w4a16_captured_in_cuda_graph(qlib):
+    """The router shape splits its tiles along K when run eagerly; captured into
+    a CUDA graph the call does not split (no library scratch inside a graph).
+    Both agree with the oracle."""
+    w = wl.WORKLOADS["w4a16_router_m2048_k2560_n512"]
+    g = wl.generate(w)
+    X, Wc, Ws, s2 = bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"])
+    Y1 = qlib.qmm_w4a16(X, Wc, Ws, s2)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        qlib.qmm_w4a16(X, Wc, Ws, s2)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        Y2 = qlib.qmm_w4a16(X, Wc, Ws, s2)
+    graph.replay()
+    torch.cuda.synchronize()
+    qlib.qmm_check_status()
+    rows = np.concatenate([np.arange(0, 2048, 97), [2047]])
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"], rows=rows)
+    for Y in (Y1, Y2):
+        assert rel_err(Y.cpu().numpy().astype(np.float64)[rows], ref) <= 1e-5
+
+
 def test_router_projection_then_expert_stage(qlib):
     """X -> logits (W4 router projection) -> expert stage, on the GPU; the routing
     and the stage checked against the oracle given the GPU's fp32 logits."""
