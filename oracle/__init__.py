@@ -55,6 +55,8 @@ def lib():
         L.orc_moe_gate_up_q8_1.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, i32, P, P, P, P]
         L.orc_moe_down_iq4.restype = None
         L.orc_moe_down_iq4.argtypes = [P, P, i32, i32, i32, P, P, P, P, i32, P]
+        L.orc_q8_0_q8_1.restype = None
+        L.orc_q8_0_q8_1.argtypes = [P, P, i32, i32, i32, P, P, P, i32, P, i32, P]
         L.orc_moe_combine.restype = None
         L.orc_moe_combine.argtypes = [P, P, P, i32, i32, i32, P]
         _lib = L
@@ -235,3 +237,42 @@ def moe_expert_stage(X, logits, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, k, tokens
     Y = moe_combine(r["w"][toks], slot, Ys)
     return dict(Y=Y, route=r, tokens=toks, pair_rows=pair_rows, Hq=gu["Hq"], Hd=gu["Hd"],
                 Hs=gu["Hs"], Yslot=Ys)
+
+
+def q8_0_q8_1(Xq, Xd, Wq, Wd, rows=None, cols=None) -> np.ndarray:
+    """Dense Q8_0 weights x q8_1 activations (exact int block dots, fp64 fold),
+    fp64 [rows][cols].  Xq int8 [M,K], Xd fp16 bits [M,K/32], Wq int8 [N,K],
+    Wd fp16 bits [N,K/32]."""
+    Xqa, Xqp = _c(Xq, np.int8)
+    Xda, Xdp = _c(Xd, np.uint16)
+    Wqa, Wqp = _c(Wq, np.int8)
+    Wda, Wdp = _c(Wd, np.uint16)
+    M, K = Xqa.shape
+    N = Wqa.shape[0]
+    ra, rp, nr = _sel(rows)
+    ca, cp, nc = _sel(cols)
+    nr = nr if rows is not None else M
+    nc = nc if cols is not None else N
+    Y = np.zeros((nr, nc), dtype=np.float64)
+    lib().orc_q8_0_q8_1(Xqp, Xdp, M, K, N, Wqp, Wdp, rp, nr, cp, nc, Y.ctypes.data)
+    return Y
+
+
+def q8_0_q8_1_requant(Xq, Xd, Wq, Wd, rows=None) -> dict:
+    """The projection followed by its re-quantisation to q8_1: each output row's
+    fp32 values (the fp64 sum rounded once) in blocks of 32 columns, as the
+    q8_1 rounding of H.  Returns Y (fp64), Yq int8, Yd / Ys fp16 bits."""
+    Y = q8_0_q8_1(Xq, Xd, Wq, Wd, rows=rows)
+    nr, N = Y.shape
+    Yq = np.zeros((nr, N), np.int8)
+    Yd = np.zeros((nr, N // 32), np.uint16)
+    Ys = np.zeros((nr, N // 32), np.uint16)
+    y32 = Y.astype(np.float32)
+    for i in range(nr):
+        for b in range(N // 32):
+            q, d, s_ = q8_1_block(y32[i, b * 32:(b + 1) * 32])
+            Yq[i, b * 32:(b + 1) * 32] = q
+            Yd[i, b] = d
+            Ys[i, b] = s_
+    return {"Y": Y, "Yq": Yq, "Yd": Yd, "Ys": Ys}
+

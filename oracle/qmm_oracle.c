@@ -376,6 +376,41 @@ void orc_moe_down_iq4(const int8_t *Hq, const uint16_t *Hd, int F, int D, int E,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Dense Q8_0 weights x q8_1 activations, one exact integer dot per 32-block */
+/* ------------------------------------------------------------------------ */
+
+/* The dense latent projections of "Run Edge0-145B Q3_K on AMD HIP (Linux,
+ * gfx1100)" (commit 17c02cd's message: Q8_0 x q8_1 integer dots; D re-quantises
+ * its products to q8_1 blocks).  Q8_0 is read as 32 int8 codes with one fp16
+ * scale per block; the q8_1 activations carry their fp16 d (s is not needed by
+ * a symmetric weight format).
+ *   y[m,n] = sum_b fp16(Xd[m,b]) * fp16(Wd[n,b]) * I_b,
+ *   I_b    = sum_{k in block b} Xq[m,k] * Wq[n,k]      (exact integer).
+ * Selected rows / columns (NULL: all); Y is [nrows][ncols] in fp64. */
+void orc_q8_0_q8_1(const int8_t *Xq, const uint16_t *Xd, int M, int K, int N,
+                   const int8_t *Wq, const uint16_t *Wd,
+                   const int32_t *rows, int nrows, const int32_t *cols, int ncols, double *Y)
+{
+    (void)M;
+    (void)N;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int i = 0; i < nrows; i++) {
+        for (int j = 0; j < ncols; j++) {
+            long m = rows ? rows[i] : i;
+            long n = cols ? cols[j] : j;
+            double acc = 0.0;
+            for (int b = 0; b < K / 32; b++) {
+                long long I = 0;
+                for (int k = b * 32; k < b * 32 + 32; k++)
+                    I += (long long)Xq[m * K + k] * (long long)Wq[n * K + k];
+                acc += orc_f16(Xd[m * (K / 32) + b]) * orc_f16(Wd[n * (K / 32) + b]) * (double)I;
+            }
+            Y[(long)i * ncols + j] = acc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Weighted combine: Y[t,:] = sum_j w[t,j] * Yslot[row(t,j), :], j ascending  */
 /* ------------------------------------------------------------------------ */
 

@@ -189,6 +189,19 @@ def gen_moe(T: int, D: int, F: int, E: int, k: int, gu_scale2: float, zipf_s: fl
                 Wd_idx=Wd_idx, Wd_s=Wd_s)
 
 
+def gen_q8_0_q8_1(M: int, K: int, N: int, seed: int) -> dict:
+    """Dense Q8_0 x q8_1 inputs, codes drawn directly: activation codes Xq int8
+    uniform in [-127, 127] [M,K] with fp16 d bits [M,K/32] uniform in
+    [2^-10, 2^-4]; weight codes Wq int8 uniform in [-127, 127] [N,K] with fp16
+    scale bits [N,K/32] uniform in [2^-12, 2^-8]."""
+    Xq = ((random_bytes(seed, 1, M * K).astype(np.int16) % 255) - 127).astype(np.int8).reshape(M, K)
+    Xd = (2.0 ** -10 + uniform(seed, 2, M * K // 32) * (2.0 ** -4 - 2.0 ** -10)).astype(np.float16)
+    Wq = ((random_bytes(seed, 3, N * K).astype(np.int16) % 255) - 127).astype(np.int8).reshape(N, K)
+    Wd = (2.0 ** -12 + uniform(seed, 4, N * K // 32) * (2.0 ** -8 - 2.0 ** -12)).astype(np.float16)
+    return dict(Xq=Xq, Xd=Xd.view(np.uint16).reshape(M, K // 32), Wq=Wq,
+                Wd=Wd.view(np.uint16).reshape(N, K // 32))
+
+
 def generate(w: Workload) -> dict:
     if w.kind == "w4a16":
         return gen_w4a16(w.M, w.K, w.N, w.scale2, w.seed)

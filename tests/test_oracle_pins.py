@@ -445,3 +445,56 @@ def test_synthetic_inputs_are_seeded_and_follow_the_stated_distributions():
     assert g["logits"].dtype == np.float32 and g["logits"].shape == (64, 16)
     ws = g["Wd_s"].view(np.float16).astype(np.float64)
     assert ws.min() >= 2 ** -12 and ws.max() <= 2 ** -10
+
+
+# ------------------------------------------------ dense Q8_0 x q8_1 (next row)
+
+def test_q8_0_q8_1_unit_scales_is_exact_integer_matmul():
+    """d = 1 on both sides: the projection is the plain integer matrix product."""
+    g = wl.gen_q8_0_q8_1(9, 96, 7, seed=41)
+    one = np.float16(1.0).view(np.uint16)
+    Xd = np.full_like(g["Xd"], one)
+    Wd = np.full_like(g["Wd"], one)
+    Y = oracle.q8_0_q8_1(g["Xq"], Xd, g["Wq"], Wd)
+    ref = g["Xq"].astype(np.int64) @ g["Wq"].astype(np.int64).T
+    assert np.array_equal(Y, ref.astype(np.float64))
+
+
+def test_q8_0_q8_1_matches_dequantised_torch_matmul():
+    g = wl.gen_q8_0_q8_1(13, 160, 21, seed=42)
+    Y = oracle.q8_0_q8_1(g["Xq"], g["Xd"], g["Wq"], g["Wd"])
+    A = g["Xq"].astype(np.float64) * np.repeat(g["Xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    B = g["Wq"].astype(np.float64) * np.repeat(g["Wd"].view(np.float16).astype(np.float64), 32, axis=1)
+    ref = (torch.from_numpy(A) @ torch.from_numpy(B).T).numpy()
+    assert np.max(np.abs(Y - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_q8_0_q8_1_single_code_selects_one_block():
+    """One non-zero weight code picks one column, scaled by its two block scales."""
+    g = wl.gen_q8_0_q8_1(5, 128, 6, seed=43)
+    Wq = np.zeros_like(g["Wq"])
+    n0, k0 = 4, 77
+    Wq[n0, k0] = -3
+    Y = oracle.q8_0_q8_1(g["Xq"], g["Xd"], Wq, g["Wd"])
+    f16 = lambda a: a.view(np.float16).astype(np.float64)  # noqa: E731
+    want = f16(g["Xd"][:, k0 // 32]) * f16(g["Wd"][n0, k0 // 32]) * g["Xq"][:, k0].astype(np.float64) * -3
+    assert np.array_equal(Y[:, n0], want)
+    assert not np.any(np.delete(Y, n0, axis=1))
+
+
+def test_q8_0_q8_1_sampling_and_requant_compose():
+    """Row / column sampling equals the full run; the q8_1 output is the q8_1
+    rounding of each row's fp32 values per 32 columns, with its invariants."""
+    g = wl.gen_q8_0_q8_1(6, 96, 64, seed=44)
+    full = oracle.q8_0_q8_1(g["Xq"], g["Xd"], g["Wq"], g["Wd"])
+    rows, cols = np.array([5, 0, 3]), np.array([63, 1, 32, 31])
+    part = oracle.q8_0_q8_1(g["Xq"], g["Xd"], g["Wq"], g["Wd"], rows=rows, cols=cols)
+    assert np.array_equal(part, full[np.ix_(rows, cols)])
+    r = oracle.q8_0_q8_1_requant(g["Xq"], g["Xd"], g["Wq"], g["Wd"])
+    assert np.array_equal(r["Y"], full)
+    for i in range(6):
+        for b in range(2):
+            q, d, s = oracle.q8_1_block(full[i, b * 32:(b + 1) * 32].astype(np.float32))
+            assert np.array_equal(r["Yq"][i, b * 32:(b + 1) * 32], q)
+            assert r["Yd"][i, b] == d and r["Ys"][i, b] == s
+            assert np.max(np.abs(q.astype(int))) == 127
