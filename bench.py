@@ -423,15 +423,18 @@ def bench_dense(q, torch, device, args, peaks, peak_src):
         g = wl.generate(w)
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
         X = d(g["X"].view(np.int16))
+        # the K-split workspace, allocated once outside the timed launches
+        nws = q.qmm_dense_workspace_size(w.M, w.K, w.N)
+        dws = torch.empty(max(nws, 1), dtype=torch.uint8, device=device)
         if w.kind == "w4a16":
             Wc, Ws = d(g["Wc"]), d(g["Ws"])
             odt = torch.bfloat16 if w.out == "bf16" else torch.float32
             Y = torch.empty((w.M, w.N), dtype=odt, device=device)
-            call = lambda: q.qmm_w4a16(X, Wc, Ws, float(g["scale2"]), out_dtype=odt, Y=Y)  # noqa: E731
+            call = lambda: q.qmm_w4a16(X, Wc, Ws, float(g["scale2"]), out_dtype=odt, Y=Y, ws=dws)  # noqa: E731
         else:
             W, S = d(g["W"]), d(g["S"])
             Y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
-            call = lambda: q.qmm_fp8_blk128(X, W, S, Y=Y)  # noqa: E731
+            call = lambda: q.qmm_fp8_blk128(X, W, S, Y=Y, ws=dws)  # noqa: E731
         for _ in range(max(3, args.warmup)):
             call()
         torch.cuda.synchronize()
@@ -449,7 +452,7 @@ def bench_dense(q, torch, device, args, peaks, peak_src):
         tfl = w.flops() / (ms * 1e-3) / 1e12
         out[name] = {"ms": ms, "tflops": tfl, "peak": peaks["bf16_tflops"], "frac": tfl / peaks["bf16_tflops"],
                      "peak_source": f"{peak_src} (burst bf16)", "l2": "flushed before each launch"}
-        del X, Y
+        del X, Y, dws
         torch.cuda.empty_cache()
     return out
 

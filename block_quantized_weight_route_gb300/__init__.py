@@ -47,6 +47,12 @@ def lib() -> ctypes.CDLL:
         L.qmm_w4a16.argtypes = [P, i32, i32, i32, P, P, ctypes.c_float, P, i32, P]
         L.qmm_fp8_blk128.restype = i32
         L.qmm_fp8_blk128.argtypes = [P, i32, i32, i32, P, P, P, P]
+        L.qmm_dense_workspace_size.restype = sz
+        L.qmm_dense_workspace_size.argtypes = [i32, i32, i32]
+        L.qmm_w4a16_ws.restype = i32
+        L.qmm_w4a16_ws.argtypes = [P, i32, i32, i32, P, P, ctypes.c_float, P, i32, P, sz, P]
+        L.qmm_fp8_blk128_ws.restype = i32
+        L.qmm_fp8_blk128_ws.argtypes = [P, i32, i32, i32, P, P, P, P, sz, P]
         L.moe_route_workspace_size.restype = sz
         L.moe_route_workspace_size.argtypes = [i32, i32, i32]
         L.moe_route_permute.restype = i32
@@ -114,8 +120,25 @@ def qmm_check_status(device=None) -> None:
     _check("qmm_check_status", lib().qmm_check_status(_stream(device)))
 
 
-def qmm_w4a16(X, Wc, Ws, scale2: float, out_dtype=torch.float32, Y=None):
-    """Y[M,N] = scale2 * X . dequant(Wc, Ws)^T  (e2m1 codes, E4M3 per-16 scales)."""
+def qmm_dense_workspace_size(M: int, K: int, N: int) -> int:
+    return int(lib().qmm_dense_workspace_size(M, K, N))
+
+
+def _dense_ws(ws, M: int, K: int, N: int, device):
+    """The K-split workspace of a dense call: the caller's uint8 tensor, else one
+    of qmm_dense_workspace_size bytes from torch's allocator (None if 0)."""
+    if ws is None:
+        n = qmm_dense_workspace_size(M, K, N)
+        if n == 0:
+            return None, 0
+        ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _need(ws, "ws", _U8, (ws.numel(),))
+    return ws, ws.numel()
+
+
+def qmm_w4a16(X, Wc, Ws, scale2: float, out_dtype=torch.float32, Y=None, ws=None):
+    """Y[M,N] = scale2 * X . dequant(Wc, Ws)^T  (e2m1 codes, E4M3 per-16 scales).
+    ws: device workspace for K splits of the last wave (default: allocated)."""
     M, K = X.shape
     N = Wc.shape[0]
     _need(X, "X", _BF16, (M, K))
@@ -126,14 +149,17 @@ def qmm_w4a16(X, Wc, Ws, scale2: float, out_dtype=torch.float32, Y=None):
     if Y is None:
         Y = torch.empty((M, N), dtype=out_dtype, device=X.device)
     _need(Y, "Y", (out_dtype,), (M, N))
-    st = lib().qmm_w4a16(_ptr(X), M, K, N, _ptr(Wc), _ptr(Ws), float(scale2), _ptr(Y),
-                         0 if out_dtype == torch.float32 else 1, _stream(X.device))
+    ws, nws = _dense_ws(ws, M, K, N, X.device)
+    st = lib().qmm_w4a16_ws(_ptr(X), M, K, N, _ptr(Wc), _ptr(Ws), float(scale2), _ptr(Y),
+                            0 if out_dtype == torch.float32 else 1, _ptr(ws) if ws is not None else None, nws,
+                            _stream(X.device))
     _check("qmm_w4a16", st)
     return Y
 
 
-def qmm_fp8_blk128(X, W, S, Y=None):
-    """Y[M,N] (bf16) = sum over 128x128 blocks of S[n/128, kb] * X . e4m3(W)^T."""
+def qmm_fp8_blk128(X, W, S, Y=None, ws=None):
+    """Y[M,N] (bf16) = sum over 128x128 blocks of S[n/128, kb] * X . e4m3(W)^T.
+    ws: device workspace for K splits of the last wave (default: allocated)."""
     M, K = X.shape
     N = W.shape[0]
     _need(X, "X", _BF16, (M, K))
@@ -142,7 +168,9 @@ def qmm_fp8_blk128(X, W, S, Y=None):
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     _need(Y, "Y", _BF16, (M, N))
-    st = lib().qmm_fp8_blk128(_ptr(X), M, K, N, _ptr(W), _ptr(S), _ptr(Y), _stream(X.device))
+    ws, nws = _dense_ws(ws, M, K, N, X.device)
+    st = lib().qmm_fp8_blk128_ws(_ptr(X), M, K, N, _ptr(W), _ptr(S), _ptr(Y),
+                                 _ptr(ws) if ws is not None else None, nws, _stream(X.device))
     _check("qmm_fp8_blk128", st)
     return Y
 

@@ -47,12 +47,6 @@ struct DeviceState {
     std::string why;
     int sms = 0;
     uint32_t* err = nullptr;
-    // dense GEMMs' K-split scratch (allocated at the first dense call): partial
-    // tiles for up to one per SM of 256 x 256 fp32; dense calls are ordered
-    // through split_done so that calls on different streams never share it at
-    // the same time
-    float* split_part = nullptr;
-    cudaEvent_t split_done = nullptr;
 };
 
 constexpr int kMaxDevices = 64;
@@ -102,32 +96,16 @@ qmm_status device_state(DeviceState** out) {
     return QMM_OK;
 }
 
-// The dense GEMMs' K-split scratch of this device, allocated once.
-// Under stream capture the calls do not split (no scratch, no event), so a graph
-// never holds library-owned memory that two replays could share.
-static bool capturing(cudaStream_t stream) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    return cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
-}
-static qmm_status split_scratch(DeviceState* d, GemmParams* p, cudaStream_t stream) {
+// The dense GEMMs' K-split scratch: the caller's workspace (none: no splits).
+static qmm_status split_workspace(const char* who, void* ws, size_t ws_bytes, GemmParams* p) {
     p->split_part = nullptr;
-    if (capturing(stream)) return QMM_OK;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!d->split_part) {
-        cudaError_t e = cudaMalloc(&d->split_part, sizeof(float) * 65536 * (size_t)d->sms);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(split scratch)");
-        e = cudaEventCreateWithFlags(&d->split_done, cudaEventDisableTiming);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(split)");
-    }
-    p->split_part = d->split_part;
-    p->split_part_cap = 65536L * d->sms;
-    cudaError_t e = cudaStreamWaitEvent(stream, d->split_done, 0);
-    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "cudaStreamWaitEvent(split)");
-}
-static qmm_status split_scratch_release(DeviceState* d, cudaStream_t stream) {
-    if (capturing(stream)) return QMM_OK;
-    cudaError_t e = cudaEventRecord(d->split_done, stream);
-    return e == cudaSuccess ? QMM_OK : cuda_fail(e, "cudaEventRecord(split)");
+    p->split_part_cap = 0;
+    if (!ws || ws_bytes == 0) return QMM_OK;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return fail(QMM_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+    p->split_part = static_cast<float*>(ws);
+    p->split_part_cap = (long)(ws_bytes / sizeof(float));
+    return QMM_OK;
 }
 
 // 2-D tiled tensor map over a row-major [outer][inner] matrix.
@@ -234,8 +212,21 @@ qmm_status qmm_check_status(cudaStream_t stream) {
     return QMM_OK;
 }
 
+size_t qmm_dense_workspace_size(int M, int K, int N) {
+    // partial tiles of at most 256 x 256 fp32 for at most one work item per SM
+    if (M < 1 || N < 1 || K < 256 || K % 256) return 0;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != QMM_OK) return 0;
+    return sizeof(float) * 65536 * (size_t)d->sms;
+}
+
 qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, const uint8_t* Ws, float scale2,
                      void* Y, qmm_dtype ydt, cudaStream_t stream) {
+    return qmm_w4a16_ws(X, M, K, N, Wc, Ws, scale2, Y, ydt, nullptr, 0, stream);
+}
+
+qmm_status qmm_w4a16_ws(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, const uint8_t* Ws, float scale2,
+                        void* Y, qmm_dtype ydt, void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (!X || !Wc || !Ws || !Y) return fail(QMM_ERR_INVALID_ARG, "qmm_w4a16: null pointer");
     if (!aligned16(X) || !aligned16(Wc) || !aligned16(Ws) || !aligned16(Y))
         return fail(QMM_ERR_INVALID_ARG, "qmm_w4a16: buffers must be 16-byte aligned");
@@ -243,8 +234,11 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     if (M < 1 || K < 64 || N < 32 || K % 64 || N % 32)
         return fail(QMM_ERR_UNSUPPORTED_SHAPE, "qmm_w4a16: need M >= 1, K %% 64 == 0, N %% 32 == 0 (M=%d K=%d N=%d)",
                     M, K, N);
+    GemmParams p{};
+    qmm_status st = split_workspace("qmm_w4a16", ws, ws_bytes, &p);
+    if (st != QMM_OK) return st;
     DeviceState* d = nullptr;
-    qmm_status st = device_state(&d);
+    st = device_state(&d);
     if (st != QMM_OK) return st;
     // sh.rows x sh.bn tiles; clusters of cn CTAs share the activation rows
     const TileShape sh = w4_dense_shape(M, N, d->sms);
@@ -257,7 +251,6 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     if ((st = make_tmap(&tb, Wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, 32, sh.bn,
                         CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
         return st;
-    GemmParams p{};
     p.M = M;
     p.N = N;
     p.K = K;
@@ -270,22 +263,29 @@ qmm_status qmm_w4a16(const uint16_t* X, int M, int K, int N, const uint8_t* Wc, 
     p.ydt = (ydt == QMM_BF16) ? 1 : 0;
     p.ldy = N;
     p.err = d->err;
-    if ((st = split_scratch(d, &p, stream)) != QMM_OK) return st;
     cudaError_t e = launch_w4a16_dense(ta, tb, p, cn, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_w4a16 launch");
-    return split_scratch_release(d, stream);
+    return QMM_OK;
 }
 
 qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t* W, const float* S, uint16_t* Y,
                           cudaStream_t stream) {
+    return qmm_fp8_blk128_ws(X, M, K, N, W, S, Y, nullptr, 0, stream);
+}
+
+qmm_status qmm_fp8_blk128_ws(const uint16_t* X, int M, int K, int N, const uint8_t* W, const float* S, uint16_t* Y,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (!X || !W || !S || !Y) return fail(QMM_ERR_INVALID_ARG, "qmm_fp8_blk128: null pointer");
     if (!aligned16(X) || !aligned16(W) || !aligned16(S) || !aligned16(Y))
         return fail(QMM_ERR_INVALID_ARG, "qmm_fp8_blk128: buffers must be 16-byte aligned");
     if (M < 1 || K < 128 || N < 128 || K % 128 || N % 128)
         return fail(QMM_ERR_UNSUPPORTED_SHAPE,
                     "qmm_fp8_blk128: need M >= 1, K %% 128 == 0, N %% 128 == 0 (M=%d K=%d N=%d)", M, K, N);
+    GemmParams p{};
+    qmm_status st = split_workspace("qmm_fp8_blk128", ws, ws_bytes, &p);
+    if (st != QMM_OK) return st;
     DeviceState* d = nullptr;
-    qmm_status st = device_state(&d);
+    st = device_state(&d);
     if (st != QMM_OK) return st;
     const int cn = cluster_for(N / 128);
     CUtensorMap ta, tb;
@@ -295,7 +295,6 @@ qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t*
         return st;
     if ((st = make_tmap(&tb, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) != QMM_OK)
         return st;
-    GemmParams p{};
     p.M = M;
     p.N = N;
     p.K = K;
@@ -307,10 +306,9 @@ qmm_status qmm_fp8_blk128(const uint16_t* X, int M, int K, int N, const uint8_t*
     p.ydt = 1;
     p.ldy = N;
     p.err = d->err;
-    if ((st = split_scratch(d, &p, stream)) != QMM_OK) return st;
     cudaError_t e = launch_fp8_blk128(ta, tb, p, cn, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_fp8_blk128 launch");
-    return split_scratch_release(d, stream);
+    return QMM_OK;
 }
 
 size_t moe_route_workspace_size(int T, int E, int k) {

@@ -66,18 +66,27 @@ qmm_status qmm_check_status(cudaStream_t stream);
  *   Ws  [N][K/16] OCP E4M3 scale bytes
  *   Y   [M][N]    fp32 (ydt = QMM_F32) or bf16 rounded to nearest even (QMM_BF16)
  * fp32 accumulation.  Shapes: M >= 1, K % 64 == 0, N % 32 == 0.
- * Scratch: when the last wave of tiles would leave at least half the SMs idle
- * (few tiles, or a ragged last wave), its tiles are split along K over several
- * CTAs and the fp32 partials are added in split order by a second kernel on the
- * same stream; the result is deterministic for a given GPU.  The partials live
- * in library-owned device memory (256 KB per SM, allocated at the first dense
- * call on a device and kept); dense calls on different streams of one device
- * are ordered one after another by the library (an event) so that they never
- * share it at the same time.  On a stream that is being captured into a graph
- * the calls never split (no scratch, no event).
  */
 qmm_status qmm_w4a16(const uint16_t *X, int M, int K, int N, const uint8_t *Wc, const uint8_t *Ws, float scale2,
                      void *Y, qmm_dtype ydt, cudaStream_t stream);
+
+/*
+ * qmm_w4a16_ws / qmm_fp8_blk128_ws -- the same products with a caller-owned
+ * device workspace `ws` (256-byte aligned; NULL or 0 bytes: as the calls
+ * without it).  When the last wave of tiles would leave at least half the SMs
+ * idle (few tiles, or a ragged last wave) and K % 256 == 0, its tiles are split
+ * along K over several CTAs: each split writes its fp32 partial tile to ws and
+ * a second kernel on the same stream adds the partials in split order, scales,
+ * rounds and writes Y (deterministic for a given GPU).  A workspace smaller than
+ * a split needs only turns the split off.  ws must not be used by another call
+ * until this one has finished on `stream`.
+ * qmm_dense_workspace_size: bytes that always suffice for an M x K x N call on
+ * the current device (256 KB per SM), 0 when the shape never splits (or no
+ * device is usable).
+ */
+size_t qmm_dense_workspace_size(int M, int K, int N);
+qmm_status qmm_w4a16_ws(const uint16_t *X, int M, int K, int N, const uint8_t *Wc, const uint8_t *Ws, float scale2,
+                        void *Y, qmm_dtype ydt, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * qmm_fp8_blk128 -- dense prefill product with FP8 weights and 128x128 block scales.
@@ -86,11 +95,13 @@ qmm_status qmm_w4a16(const uint16_t *X, int M, int K, int N, const uint8_t *Wc, 
  * "perf: strix-hip BF16 GEMMs via hipBLASLt", FP8 block-scaling twin commit.
  *   X [M][K] bf16;  W [N][K] OCP E4M3 bytes;  S [N/128][K/128] fp32;  Y [M][N] bf16 (RNE).
  * fp32 accumulation.  Shapes: M >= 1, K % 128 == 0, N % 128 == 0.
- * Scratch and ordering: as qmm_w4a16 (K splits of the last wave add the folded
- * partials in split order).
+ * qmm_fp8_blk128_ws: with a workspace as qmm_w4a16_ws (a split adds the folded
+ * partials of its K range).
  */
 qmm_status qmm_fp8_blk128(const uint16_t *X, int M, int K, int N, const uint8_t *W, const float *S, uint16_t *Y,
                           cudaStream_t stream);
+qmm_status qmm_fp8_blk128_ws(const uint16_t *X, int M, int K, int N, const uint8_t *W, const float *S, uint16_t *Y,
+                             void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * moe_route_permute -- top-k routing and per-expert grouping of T tokens.

@@ -61,6 +61,22 @@ def test_argument_checks_return_before_any_device_work(L):
     assert L.qmm_fp8_blk128(P(256), 64, 200, 256, P(256), P(256), P(256), None) == 2
     L.qmm_last_error.restype = ctypes.c_char_p
     assert b"qmm_fp8_blk128" in L.qmm_last_error()
+    # the workspace variants: a workspace that is not 256-byte aligned
+    sz = ctypes.c_size_t
+    L.qmm_w4a16_ws.restype = ctypes.c_int
+    L.qmm_w4a16_ws.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_float, P, ctypes.c_int,
+                               P, sz, P]
+    assert L.qmm_w4a16_ws(P(256), 64, 512, 512, P(256), P(256), 1.0, P(256), 0, P(4096 + 16), 1 << 20, None) == 1
+    assert b"256-byte" in L.qmm_last_error()
+    assert L.qmm_w4a16_ws(P(256), 64, 100, 512, P(256), P(256), 1.0, P(256), 0, P(4096), 1 << 20, None) == 2
+    L.qmm_fp8_blk128_ws.restype = ctypes.c_int
+    L.qmm_fp8_blk128_ws.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, sz, P]
+    assert L.qmm_fp8_blk128_ws(P(256), 64, 256, 256, P(256), P(256), P(256), P(4096 + 128), 1 << 20, None) == 1
+    # the workspace size: none for shapes that never split (K % 256 != 0)
+    L.qmm_dense_workspace_size.restype = sz
+    L.qmm_dense_workspace_size.argtypes = [ctypes.c_int] * 3
+    assert L.qmm_dense_workspace_size(64, 384, 512) == 0
+    assert L.qmm_dense_workspace_size(0, 512, 512) == 0
     L.moe_route_permute.restype = ctypes.c_int
     L.moe_route_permute.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int] + [P] * 7 + [ctypes.c_size_t, P]
     # k > 16, E > 512

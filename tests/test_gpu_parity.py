@@ -80,6 +80,24 @@ def test_w4a16_unit_scales_integer_inputs_are_exact(qlib):
     assert np.array_equal(Y.astype(np.float64), ref)
 
 
+def test_dense_without_workspace_does_not_split_and_agrees(qlib):
+    """The calls without a workspace never split; with one, the router shape
+    does.  Both agree with the oracle (the fp32 sums differ only in order)."""
+    w = wl.WORKLOADS["w4a16_router_m2048_k2560_n512"]
+    g = wl.generate(w)
+    X, Wc, Ws, s2 = bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"])
+    Y_split = qlib.qmm_w4a16(X, Wc, Ws, s2)
+    Y_plain = torch.empty_like(Y_split)
+    st = qlib.lib().qmm_w4a16(qlib._ptr(X), 2048, 2560, 512, qlib._ptr(Wc), qlib._ptr(Ws), s2, qlib._ptr(Y_plain), 0,
+                              qlib._stream(X.device))
+    assert st == 0
+    qlib.qmm_check_status()
+    rows = np.concatenate([np.arange(0, 2048, 131), [2047]])
+    ref = oracle.w4a16(g["X"], g["Wc"], g["Ws"], g["scale2"], rows=rows)
+    for Y in (Y_split, Y_plain):
+        assert rel_err(Y.cpu().numpy().astype(np.float64)[rows], ref) <= 1e-5
+
+
 def test_w4a16_k_split_integer_inputs_are_exact(qlib):
     """Few tiles and a long K: the dense GEMM splits each tile's K range over
     several CTAs (3 tiles on a 152-SM part: 4 splits) and adds the fp32 partials
@@ -154,9 +172,9 @@ def test_w4a16_router_shape_sampled(qlib):
 
 
 def test_w4a16_captured_in_cuda_graph(qlib):
-    """The router shape splits its tiles along K when run eagerly; captured into
-    a CUDA graph the call does not split (no library scratch inside a graph).
-    Both agree with the oracle."""
+    """The router shape splits its tiles along K (partials in the caller's
+    workspace, here allocated by the binding); the same call captured into a
+    CUDA graph and replayed agrees with the oracle like the eager one."""
     w = wl.WORKLOADS["w4a16_router_m2048_k2560_n512"]
     g = wl.generate(w)
     X, Wc, Ws, s2 = bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"])
