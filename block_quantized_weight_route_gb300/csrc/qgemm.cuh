@@ -3,7 +3,7 @@
 //   warp 0        : TMA producer (activations tile + raw quantised weight tile)
 //   warp 1        : TMEM owner and MMA issuer (one elected thread issues tcgen05.mma)
 //   epilogue warps: read fp32 accumulators from TMEM, scale / fold / quantise, store
-//                   (12..15, or 4..11 for the two-warpgroup fold epilogue)
+//                   (12..15; 4..19 for the FP8 fold over two row sub-tiles)
 //   converter warps: turn raw weight codes into the exact 16-bit operand tiles
 //                    the tensor core reads, in shared memory; none of them runs on
 //                    the MMA issuer's sub-partition (warp id % 4 == 1)
@@ -11,7 +11,10 @@
 // Tile: 128*MSUB rows (tokens) x BN columns (weight rows), K step 64.  The MMA
 // is tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16), MSUB of them per K
 // step (one per 128-row sub-tile), fp32 accumulation in TMEM.  Operands are
-// K-major in the canonical 128-byte-swizzled layout.
+// K-major in the canonical 128-byte-swizzled layout.  Dense problems whose last
+// wave of tiles would leave half the clusters idle split those tiles along K
+// (fp32 partials in the caller's workspace, added in split order by
+// split_reduce_kernel).
 //
 // The quantised formats it reads (page titles / sections):
 //  - W4: e2m1 codes with one E4M3 scale per 16 K and an fp32 scale2 applied once
@@ -53,7 +56,7 @@ struct GemmCfg {
     static constexpr bool GROUPED = GROUPED_;
     static constexpr int BM = 128 * MSUB_, BN = BN_, BK = 64, UMMA_K = 16;
     static constexpr int CONV_WARPS = CONV_WARPS_, EPI_WARPS = EPI_WARPS_;
-    // 16 warps.  Warp w runs on SM sub-partition w % 4; the MMA issuer (warp 1)
+    // 16 warps (20 for the FP8 fold).  Warp w runs on SM sub-partition w % 4; the MMA issuer (warp 1)
     // must not share its sub-partition with ALU-heavy converter warps, or its
     // mbarrier waits are starved and the tensor pipe idles.
     static constexpr int EPI_BASE = (EPI_WARPS_ == 4) ? 12 : 4;
