@@ -235,7 +235,7 @@ def test_fp8_blk128_matches_blockwise_torch_and_unit_scale_case():
 # routing
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("T,E,k", [(37, 16, 4), (200, 128, 8), (64, 256, 8), (5, 8, 8)])
+@pytest.mark.parametrize("T,E,k", [(37, 16, 4), (200, 128, 8), (64, 256, 8), (5, 8, 8), (23, 512, 16), (9, 3, 1)])
 def test_route_matches_torch_topk_and_invariants(T, E, k):
     rng = np.random.default_rng(T * 1000 + E)
     logits = (2 * rng.standard_normal((T, E))).astype(np.float32)
