@@ -24,6 +24,8 @@
  *    (Linux, gfx1100)", "Contents" (commit 4cb5224) and that commit's message.
  *  - Top-k routing with renormalised weights: "AMD_HIP.md", RDNA4 speed
  *    switches (router_top10).
+ *  - Dense Q8_0 x q8_1 projections re-quantised to q8_1: "Run Edge0-145B Q3_K on
+ *    AMD HIP (Linux, gfx1100)", commit 17c02cd's message (lat_dense_w11).
  * Format details the pages leave open (nibble order, codebook, q8_1 rounding)
  * follow the workload statement; each reading is named where it is used.
  */
