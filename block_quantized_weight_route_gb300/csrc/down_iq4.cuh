@@ -65,6 +65,8 @@ struct DownCfgT {
     static_assert(EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue width");
     static_assert(CONV_WARPS == 2 || CONV_WARPS == 4, "converter count");
     static constexpr int TSTAGES = TSTAGES_, CSTAGES = QMM_DOWN_CSTAGES, SSTAGES = 2, NBUF = 4;
+    static constexpr int TMA_GROUPS = TSTAGES_;   // producer lane pairs (IQ4 codes, H codes)
+    static_assert(2 * TMA_GROUPS <= 31, "producer lanes: pairs below lane 31");
     static constexpr int KG_MAX = 32;                         // K <= 1024
     static constexpr int A_RAW_BYTES = BM * 32;               // IQ4 codes: 64 indices per row
     static constexpr int B_BYTES = BN * BK * 2;               // f16 H codes, 128-byte rows
@@ -176,8 +178,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int num_tiles = entries * p.n_tiles;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer (one lane)
-        if (lane == 0) {
+        // ------------------------------------------------------------ producer (one warp)
+        // A thread has one TMA copy executing at a time (~0.8-0.9k cycles each on
+        // GB300, whatever the size), so the two copies of stage s come from lanes
+        // 2*(s % TMA_GROUPS) and 2*(s % TMA_GROUPS) + 1, and the per-tile scale
+        // copies from lane 31: copies of different stages overlap.
+        {
             int s = 0, ss = 0;
             uint32_t ph = 0, sph = 0;
             long issued = 0, s_issued = 0;
@@ -189,25 +195,35 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int n0 = (t - entry * p.n_tiles) * C::BM;
                 const int4 g = p.tiles[entry];
                 // this tile's d_H and d_W values
-                if (!mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) break;
-                uint8_t* sst = sstage + ss * C::SSTAGE_BYTES;
-                mbar_arrive_expect_tx(&full_s[ss], dh_bytes + dw_bytes);
-                bulk_load(sst, p.dH32 + (long)entry * groups * C::BN, dh_bytes, &full_s[ss]);
-                bulk_load(sst + C::DH_BYTES, p.dW + ((long)g.x * p.N + n0) * groups, dw_bytes, &full_s[ss]);
+                const bool got_s = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                if (__any_sync(0xffffffffu, !got_s)) break;
+                if (lane == 31) {
+                    uint8_t* sst = sstage + ss * C::SSTAGE_BYTES;
+                    mbar_arrive_expect_tx(&full_s[ss], dh_bytes + dw_bytes);
+                    bulk_load(sst, p.dH32 + (long)entry * groups * C::BN, dh_bytes, &full_s[ss]);
+                    bulk_load(sst + C::DH_BYTES, p.dW + ((long)g.x * p.N + n0) * groups, dw_bytes, &full_s[ss]);
+                }
+                __syncwarp();
                 ++s_issued;
                 if (++ss == C::SSTAGES) {
                     ss = 0;
                     sph ^= 1u;
                 }
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY)) {
+                    const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                    if (__any_sync(0xffffffffu, !got)) {
                         ok = false;
                         break;
                     }
+                    const int l0 = 2 * (s % C::TMA_GROUPS);
                     uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                    mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
-                    tma_load_2d(st, &tmA, &full_t[s], kb * 32, g.x * p.N + n0);
-                    tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
+                    if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                    __syncwarp();
+                    if (lane == l0)
+                        tma_load_2d(st, &tmA, &full_t[s], kb * 32, g.x * p.N + n0);
+                    else if (lane == l0 + 1)
+                        tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
+                    __syncwarp();
                     ++issued;
                     if (++s == C::TSTAGES) {
                         s = 0;
@@ -215,8 +231,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
             }
-            drain_ring(full_t, issued, C::TSTAGES, p.err);
-            drain_ring(full_s, s_issued, C::SSTAGES, p.err);
+            if (lane == 0) {
+                drain_ring(full_t, issued, C::TSTAGES, p.err);
+                drain_ring(full_s, s_issued, C::SSTAGES, p.err);
+            }
         }
         __syncwarp();
     } else if (warp == C::MMA_WARP) {
@@ -225,14 +243,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // votes, so each K block costs a few dozen instructions on this warp.
         if (lane == 0) {
             int cs = 0, ts = 0, buf = 0;
-            uint32_t cph = 0, tph = 0, bph = 0;
+            uint32_t cph = 0, bph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 for (int kb = 0; kb < kblocks && ok; ++kb) {
-                    // expanded weights ready (the converters saw the TMA stage complete);
-                    // the H codes of the same stage are waited on directly
-                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV) ||
-                        !mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL)) {
+                    // expanded weights ready: the converters arrive on full_c only after they saw
+                    // the TMA stage (IQ4 codes and H codes) complete, so full_c orders the H
+                    // codes of the same stage too
+                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
                         ok = false;
                         break;
                     }
@@ -266,10 +284,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         cs = 0;
                         cph ^= 1u;
                     }
-                    if (++ts == C::TSTAGES) {
-                        ts = 0;
-                        tph ^= 1u;
-                    }
+                    if (++ts == C::TSTAGES) ts = 0;
                 }
             }
             tc_commit(drain_bar);

@@ -68,6 +68,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of phase `parity`: never suspends the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // As mbar_try_wait, but the thread may sleep in hardware until the phase
 // completes (it is woken when it does) or `hint_ns` nanoseconds pass.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
@@ -90,7 +103,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // do the work.  The wall clock (slow to read) is consulted every 64 sleeps.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               uint32_t* err, uint32_t code, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+#ifndef QMM_WAIT_TEST_FIRST
+#define QMM_WAIT_TEST_FIRST 1
+#endif
+    if (QMM_WAIT_TEST_FIRST ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1

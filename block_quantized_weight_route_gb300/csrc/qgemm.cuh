@@ -73,6 +73,9 @@ struct GemmCfg {
     static constexpr int FOLD_CPW = 128 / (EPI_WARPS_ >= 8 ? EPI_WARPS_ / 4 : 1);
     static constexpr int FOLD_LDW = (EPI_WARPS_ == 16) ? 16 : 32;
     static constexpr int TSTAGES = TSTAGES_, CSTAGES = CSTAGES_;
+    // producer lane groups (4 lanes each: activation copy, one or two weight copies)
+    static constexpr int TMA_GROUPS = TSTAGES_;
+    static_assert(TMA_GROUPS * 4 <= 32, "producer lane groups fit one warp");
     // raw (TMA) stage: bf16 activation tile (read by the MMA in place) + weight codes
     static constexpr int A_RAW_BYTES = BM * BK * 2;
     static constexpr int B_ROW_BYTES = (B_ == BMode::FP8) ? 64 : 32;   // bytes of codes per weight row per k-block
@@ -494,9 +497,14 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                         ok = false;
                         break;
                     }
-                    if (elect_one_sync()) {
-                        uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                        mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                    // A thread has one TMA copy executing at a time, so each copy of stage s
+                    // comes from its own lane of lane group s % TMA_GROUPS: copies of
+                    // different stages and kinds overlap.
+                    const int l0 = (s % C::TMA_GROUPS) * 4;
+                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                    if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                    __syncwarp();
+                    if (lane == l0) {
                         if constexpr (C::CLUSTER_N > 1) {
                             // this CTA's slice of the activation tile, written into every CTA of the cluster
                             tma_load_2d_multicast(st + crank * C::A_SLICE_ROWS * 128, &tmA, &full_t[s], kb * C::BK,
@@ -505,14 +513,17 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                         } else {
                             tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
                         }
+                    } else if (lane == l0 + 1 || lane == l0 + 2) {
                         uint8_t* bdst = st + C::A_RAW_BYTES;
                         const int kx = kb * C::B_ROW_BYTES;
                         if constexpr (C::EPI == Epi::SWIGLU_Q81) {
-                            // gate rows e*2F + n0 .. +BN/2, up rows e*2F + F + n0 .. +BN/2
+                            // gate rows e*2F + n0 .. +BN/2 (lane l0+1), up rows e*2F + F + n0 .. +BN/2 (lane l0+2)
                             const int base = ti.expert * 2 * p.F + ti.n0;
-                            tma_load_2d(bdst, &tmB, &full_t[s], kx, base);
-                            tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, &tmB, &full_t[s], kx, base + p.F);
-                        } else {
+                            if (lane == l0 + 1)
+                                tma_load_2d(bdst, &tmB, &full_t[s], kx, base);
+                            else
+                                tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, &tmB, &full_t[s], kx, base + p.F);
+                        } else if (lane == l0 + 1) {
                             tma_load_2d(bdst, &tmB, &full_t[s], kx, ti.expert * p.N + ti.n0);
                         }
                     }
@@ -528,10 +539,13 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             if (lane == 0) drain_ring(full_t, issued, C::TSTAGES, p.err);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        {
+        // ------------------------------------------------------------ MMA issuer (one lane)
+        // One thread runs the whole issue loop: the descriptors of a K block are
+        // built once and advanced by constants, and there is no election or warp
+        // synchronisation between MMAs.
+        if (lane == 0) {
             int ts = 0, cs = 0, buf = 0;
-            uint32_t tph = 0, cph = 0, bph = 0;
+            uint32_t cph = 0, bph = 0;
             bool ok = true;
             // the work item, read one ahead so the descriptor load is off the issue
             // path: its K range, and the sub-tiles holding at least one live row (a
@@ -542,71 +556,59 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 const TileInfo mi = mi_next;
                 if (t + ncl < num_tiles) mi_next = decode_tile<C>(p, t + ncl, crank);
                 const int nsub = (C::MSUB == 2 && mi.rows <= 128) ? 1 : C::MSUB;
-                for (int kb = mi.kb0; kb < mi.kb1 && ok; ++kb) {
-                    bool got = mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL);
-                    got = got && mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
-                    if (__any_sync(0xffffffffu, !got)) {
+                for (int kb = mi.kb0; kb < mi.kb1; ++kb) {
+                    // Only the converted weights are waited on: the converters arrive on
+                    // full_c after they saw this stage's TMA copies complete (full_t), so
+                    // full_c also orders the activation tile.
+                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
                         ok = false;
                         break;
                     }
-                    // (no tcgen05 fence here: the operands are ordered by the mbarrier and the
-                    // writers' proxy fence; a tcgen05 fence per K block would drain the MMA pipe)
-                    const uint32_t a_base = smem_u32(tstage + ts * C::TSTAGE_BYTES);
-                    const uint32_t b_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+                    // first / last K block of an accumulation group (the item's K range, or
+                    // one 128-K block = two K blocks for the FP8 fold)
+                    bool first, last;
+                    if constexpr (C::GROUP_K == 128) {
+                        first = (kb & 1) == 0;
+                        last = (kb & 1) == 1;
+                    } else {
+                        first = kb == mi.kb0;
+                        last = kb == mi.kb1 - 1;
+                    }
+                    if (first) {
+                        if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    // (no tcgen05 fence per K block: the operands are ordered by the mbarrier
+                    // and the writers' proxy fence; such a fence would drain the MMA pipe)
+                    // descriptor start addresses are in 16-byte units: +2 per K step of 16
+                    // (32 bytes), +1024 per 128-row sub-tile (16 KB)
+                    const uint64_t ad = smem_desc_sw128(smem_u32(tstage + ts * C::TSTAGE_BYTES));
+                    const uint64_t bd = smem_desc_sw128(smem_u32(cstage + cs * C::CSTAGE_BYTES));
+                    const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::MSUB * C::BN);
 #pragma unroll
                     for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-                        // first / last MMA of an accumulation group (the item's K range, or
-                        // one 128-K block = two K blocks for the FP8 fold); no divisions
-                        // here: this loop sits between consecutive MMA issues
-                        bool first, last;
-                        if constexpr (C::GROUP_K == 128) {
-                            first = (kk == 0) && ((kb & 1) == 0);
-                            last = (kk == C::BK / C::UMMA_K - 1) && ((kb & 1) == 1);
-                        } else {
-                            first = (kk == 0) && (kb == mi.kb0);
-                            last = (kk == C::BK / C::UMMA_K - 1) && (kb == mi.kb1 - 1);
-                        }
-                        if (first) {
-                            const bool free = mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err,
-                                                        DEV_TIMEOUT_ACC_EMPTY);
-                            if (__any_sync(0xffffffffu, !free)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                        }
-                        const uint64_t bdesc = smem_desc_sw128(b_base + kk * 32);
-                        const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::MSUB * C::BN);
-                        if (elect_one_sync()) {
 #pragma unroll
-                            for (int m = 0; m < C::MSUB; ++m)
-                                if (m < nsub)
-                                    tc_mma_f16(dtmem + (uint32_t)(m * C::BN),
-                                               smem_desc_sw128(a_base + m * 16384 + kk * 32), bdesc, C::IDESC,
-                                               first ? 0u : 1u);
-                            if (last) tc_commit(&acc_full[buf]);
-                        }
-                        __syncwarp();
-                        if (last) {
-                            if (++buf == C::NBUF) {
-                                buf = 0;
-                                bph ^= 1u;
-                            }
+                        for (int m = 0; m < C::MSUB; ++m)
+                            if (m < nsub)
+                                tc_mma_f16(dtmem + (uint32_t)(m * C::BN), ad + (uint64_t)(m * 1024 + kk * 2),
+                                           bd + (uint64_t)(kk * 2), C::IDESC, (first && kk == 0) ? 0u : 1u);
+                    }
+                    if (last) {
+                        tc_commit(&acc_full[buf]);
+                        if (++buf == C::NBUF) {
+                            buf = 0;
+                            bph ^= 1u;
                         }
                     }
-                    if (!ok) break;
-                    if (elect_one_sync()) {
-                        tc_commit(&empty_c[cs]);
-                        if constexpr (C::CLUSTER_N > 1)
-                            tc_commit_multicast(&empty_t[ts], (uint16_t)((1u << C::CLUSTER_N) - 1));
-                        else
-                            tc_commit(&empty_t[ts]);
-                    }
-                    __syncwarp();
-                    if (++ts == C::TSTAGES) {
-                        ts = 0;
-                        tph ^= 1u;
-                    }
+                    tc_commit(&empty_c[cs]);
+                    if constexpr (C::CLUSTER_N > 1)
+                        tc_commit_multicast(&empty_t[ts], (uint16_t)((1u << C::CLUSTER_N) - 1));
+                    else
+                        tc_commit(&empty_t[ts]);
+                    if (++ts == C::TSTAGES) ts = 0;
                     if (++cs == C::CSTAGES) {
                         cs = 0;
                         cph ^= 1u;
@@ -614,10 +616,10 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 }
             }
             // Teardown: wait until every MMA issued has completed before TMEM is freed.
-            if (elect_one_sync()) tc_commit(drain_bar);
-            __syncwarp();
-            if (lane == 0) drain_ring(drain_bar, 1, 1, p.err);
+            tc_commit(drain_bar);
+            drain_ring(drain_bar, 1, 1, p.err);
         }
+        __syncwarp();
     } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                         // TMEM lane quarter of this warp
@@ -682,7 +684,12 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                                 for (int j = 0; j < 32; ++j) {
                                     const float gv = __uint_as_float(g[j]) * s2;
                                     const float uv = __uint_as_float(u[j]) * s2;
-                                    h[j] = gv / (1.0f + expf(-gv)) * uv;
+                                    // silu(g) * u with the fast exponential and division
+                                    // intrinsics (a few ulp: this epilogue's arithmetic
+                                    // competes for issue slots with the converters and the
+                                    // MMA issuer); the exponent is capped so 1 + e stays
+                                    // below 2^126, where the fast division is valid
+                                    h[j] = __fdividef(gv, 1.0f + __expf(fminf(-gv, 80.0f))) * uv;
                                     amax = fmaxf(amax, fabsf(h[j]));
                                 }
                                 // the codes are stored as exact f16 integers: the down
@@ -692,9 +699,13 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                                 float d = 0.f;
                                 if (amax > 0.f) {
                                     d = amax / 127.0f;
+                                    // h / d as h times the correctly rounded 1/d (within
+                                    // 1.5 ulp of the quotient: a code moves only when h/d
+                                    // lies that close to a half-integer)
+                                    const float rd = __frcp_rn(d);
     #pragma unroll
                                     for (int j = 0; j < 16; ++j) {
-                                        float v0 = roundf(h[2 * j] / d), v1 = roundf(h[2 * j + 1] / d);
+                                        float v0 = roundf(h[2 * j] * rd), v1 = roundf(h[2 * j + 1] * rd);
                                         v0 = fminf(fmaxf(v0, -127.f), 127.f);
                                         v1 = fminf(fmaxf(v1, -127.f), 127.f);
                                         sum += (int)v0 + (int)v1;
