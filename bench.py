@@ -350,8 +350,11 @@ def run_gpu(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(world, e0.elapsed_time(e1) / 1e3, device)
-    # the last step's Y, checked against the device-timed run's Y (same inputs)
-    assert torch.equal(Yh[(args.steps - 1) % nb], Y.cpu()), "end-to-end output differs from the device-timed output"
+    # the last step's Y, checked against the device-timed run's Y (same inputs; the
+    # fused combine adds each token's k terms in no fixed order, so up to rounding)
+    Yl, Yr = Yh[(args.steps - 1) % nb], Y.cpu()
+    assert float((Yl - Yr).abs().max()) <= 1e-6 * float(Yr.abs().max()), \
+        "end-to-end output differs from the device-timed output"
     e2e = {"value": w.T * world * args.steps / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": int(Xh[0].numel() * 2 + Lh[0].numel() * 4), "d2h_bytes_per_step": int(Yh[0].numel() * 4),
            "overlap": "double-buffered: H2D of step i+1 and D2H of step i-1 on their own streams while step i computes"}

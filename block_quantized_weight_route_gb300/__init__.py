@@ -14,9 +14,10 @@ import torch
 
 from .build import LIB, build_library  # noqa: F401
 
-QMM_WS_FIELDS = 18
+QMM_WS_FIELDS = 19
 WS_FIELD_NAMES = ("ids", "w", "counts", "offsets", "src", "row", "chunk_counts", "tiles", "tile_count",
-                  "tiles256", "tile_count256", "X_perm", "Hq", "Hd", "Hs", "Hd32", "Yslot", "total")
+                  "tiles256", "tile_count256", "X_perm", "Hq", "Hd", "Hs", "Hd32", "Yslot", "wrow", "total")
+QMM_STAGE_SLOTS = 1
 
 _STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE",
            3: "QMM_ERR_UNSUPPORTED_DEVICE", 4: "QMM_ERR_WORKSPACE", 5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT"}
@@ -71,6 +72,9 @@ def lib() -> ctypes.CDLL:
         L.qmm_profile_read_call.argtypes = [ctypes.c_long, P]
         L.moe_expert_stage_w4_iq4.restype = i32
         L.moe_expert_stage_w4_iq4.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+        L.moe_expert_stage_w4_iq4_ex.restype = i32
+        L.moe_expert_stage_w4_iq4_ex.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, sz,
+                                                 ctypes.c_uint, P]
         L.qmm_dbg_workspace_size.restype = sz
         L.qmm_dbg_workspace_size.argtypes = [i32, i32, i32, i32]
         L.qmm_dbg_gate_up_q8_1.restype = i32
@@ -213,9 +217,14 @@ def moe_expert_stage_workspace_layout(T: int, D: int, F: int, E: int, k: int) ->
     return dict(zip(WS_FIELD_NAMES, [int(v) for v in arr]))
 
 
-def moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, k: int, ws=None, Y=None):
+def moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, k: int, ws=None, Y=None,
+                            slots: bool = False):
     """The routed expert stage: route, W4 gate/up + SwiGLU + q8_1, IQ4_NL down,
-    weighted combine.  Returns Y [T, D] fp32 (and leaves intermediates in ws)."""
+    weighted combine.  Returns Y [T, D] fp32 (and leaves intermediates in ws).
+    slots=False: the combine is fused into the down product (fp32 atomic adds,
+    summation order not fixed); slots=True: per-row down outputs in the
+    workspace's Yslot, then the j-ordered combine (moe_expert_stage_w4_iq4_ex
+    with QMM_STAGE_SLOTS)."""
     T, D = X.shape
     E = logits.shape[1]
     F = Wgu_c.shape[1] // 2
@@ -233,9 +242,14 @@ def moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, k:
     if Y is None:
         Y = torch.empty((T, D), dtype=torch.float32, device=dev)
     _need(Y, "Y", (torch.float32,), (T, D))
-    st = lib().moe_expert_stage_w4_iq4(_ptr(X), _ptr(logits), T, D, F, E, k, _ptr(Wgu_c), _ptr(Wgu_s),
-                                       _ptr(gu_scale2), _ptr(Wd_idx), _ptr(Wd_s), _ptr(Y), _ptr(ws), ws.numel(),
-                                       _stream(dev))
+    if slots:
+        st = lib().moe_expert_stage_w4_iq4_ex(_ptr(X), _ptr(logits), T, D, F, E, k, _ptr(Wgu_c), _ptr(Wgu_s),
+                                              _ptr(gu_scale2), _ptr(Wd_idx), _ptr(Wd_s), _ptr(Y), _ptr(ws),
+                                              ws.numel(), QMM_STAGE_SLOTS, _stream(dev))
+    else:
+        st = lib().moe_expert_stage_w4_iq4(_ptr(X), _ptr(logits), T, D, F, E, k, _ptr(Wgu_c), _ptr(Wgu_s),
+                                           _ptr(gu_scale2), _ptr(Wd_idx), _ptr(Wd_s), _ptr(Y), _ptr(ws), ws.numel(),
+                                           _stream(dev))
     _check("moe_expert_stage_w4_iq4", st)
     return Y
 

@@ -172,6 +172,7 @@ void stage_layout(int T, int D, int F, int E, int k, size_t* off) {
         P * (F / 32) * 2,                           // Hs
         (size_t)max_tile_entries(T, E, k) * (F / 32) * 128 * 4,   // Hd32: fp32 d per tile entry
         P * D * 4,                                  // Yslot
+        P * 4,                                      // wrow: routing weight per routed row
     };
     size_t o = 0;
     for (int i = 0; i < QMM_WS_FIELDS - 1; ++i) {
@@ -388,11 +389,13 @@ static qmm_status run_gate_up(DeviceState* d, const uint16_t* Xp, int P, int D, 
     return QMM_OK;
 }
 
-// Down product Yslot [P][D] = IQ4_NL weights x q8_1 H (f16 codes Hq, fp32 d in
-// the per-128-row-entry layout Hd32), grouped by the 128-row tile list.
+// Down product over IQ4_NL weights x q8_1 H (f16 codes Hq, fp32 d in the
+// per-128-row-entry layout Hd32), grouped by the 128-row tile list.  Without a
+// combine: Yslot [P][D] per routed row.  With one (src, wrow given): the weighted
+// combine is fused in, Y [T][D] += wrow[r] * y_r at token src[r] (Y zeroed first).
 static qmm_status run_down(DeviceState* d, const __half* Hq, const float* Hd32, int P, int D, int F, int E,
                            const uint8_t* Wd_idx, const uint16_t* Wd_s, const int4* tiles, const int32_t* num_entries,
-                           int max_entries, float* Yslot, cudaStream_t stream) {
+                           int max_entries, float* out, const int32_t* src, const float* wrow, cudaStream_t stream) {
     qmm_status st;
     CUtensorMap ta, tb;
     if ((st = make_tmap(&ta, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
@@ -411,11 +414,13 @@ static qmm_status run_down(DeviceState* d, const __half* Hq, const float* Hd32, 
     q.max_entries = max_entries;
     q.dH32 = Hd32;
     q.dW = reinterpret_cast<const __half*>(Wd_s);
-    q.Y = Yslot;
+    q.src = src;
+    q.wrow = wrow;
+    q.Y = out;
     q.ydt = 0;
     q.ldy = D;
     q.err = d->err;
-    cudaError_t e = launch_iq4_down(ta, tb, q, d->sms, stream);
+    cudaError_t e = launch_iq4_down(ta, tb, q, d->sms, src != nullptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "expert stage: down launch");
     return QMM_OK;
 }
@@ -448,8 +453,17 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
                                    const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2,
                                    const uint8_t* Wd_idx, const uint16_t* Wd_s, float* Y, void* ws, size_t ws_bytes,
                                    cudaStream_t stream) {
+    return moe_expert_stage_w4_iq4_ex(X, logits, T, D, F, E, k, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, Y, ws, ws_bytes,
+                                      0u, stream);
+}
+
+qmm_status moe_expert_stage_w4_iq4_ex(const uint16_t* X, const float* logits, int T, int D, int F, int E, int k,
+                                      const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2,
+                                      const uint8_t* Wd_idx, const uint16_t* Wd_s, float* Y, void* ws, size_t ws_bytes,
+                                      unsigned flags, cudaStream_t stream) {
     qmm_status st = check_stage_shape(T, D, F, E, k);
     if (st != QMM_OK) return st;
+    if (flags & ~(unsigned)QMM_STAGE_SLOTS) return fail(QMM_ERR_INVALID_ARG, "moe_expert_stage_w4_iq4_ex: unknown flags");
     if (!Wgu_c || !Wgu_s || !gu_scale2 || !Wd_idx || !Wd_s || (T > 0 && (!X || !logits || !Y || !ws)))
         return fail(QMM_ERR_INVALID_ARG, "moe_expert_stage_w4_iq4: null pointer");
     if (!aligned16(X) || !aligned16(logits) || !aligned16(Wgu_c) || !aligned16(Wgu_s) || !aligned16(Wd_idx) ||
@@ -461,6 +475,7 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
     DeviceState* d = nullptr;
     if ((st = device_state(&d)) != QMM_OK) return st;
     if (T == 0) return QMM_OK;
+    const bool slots = (flags & QMM_STAGE_SLOTS) != 0;
 
     size_t off[QMM_WS_FIELDS];
     stage_layout(T, D, F, E, k, off);
@@ -476,6 +491,14 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
                  static_cast<int32_t*>(at(3)), static_cast<int32_t*>(at(4)), static_cast<int32_t*>(at(5)),
                  static_cast<int32_t*>(at(6)), static_cast<int4*>(at(7)), static_cast<int32_t*>(at(8)),
                  max_entries, static_cast<int4*>(at(9)), static_cast<int32_t*>(at(10)), max_entries2};
+    float* wrow = static_cast<float*>(at(17));
+    if (!slots) {
+        // the fused combine accumulates into Y: the top-k kernel zeroes it, the
+        // permutation records each routed row's weight
+        rb.wrow = wrow;
+        rb.yzero = Y;
+        rb.yzero_D = D;
+    }
     e = launch_route(logits, T, E, k, rb, stream);
     if (e != cudaSuccess) return cuda_fail(e, "expert stage: routing");
     if ((e = mark(d, 1, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
@@ -495,14 +518,17 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T
         return st;
     if ((e = mark(d, 3, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
-    // down (IQ4_NL weights on the MMA's M side, q8_1 H codes on its N side)
-    if ((st = run_down(d, Hq, Hd32, P, D, F, E, Wd_idx, Wd_s, rb.tiles, rb.num_entries, max_entries, Yslot, stream)) !=
-        QMM_OK)
+    // down (IQ4_NL weights on the MMA's M side, q8_1 H codes on its N side), with the
+    // weighted combine fused in, or to per-slot rows followed by the combine kernel
+    if ((st = run_down(d, Hq, Hd32, P, D, F, E, Wd_idx, Wd_s, rb.tiles, rb.num_entries, max_entries,
+                       slots ? Yslot : Y, slots ? nullptr : rb.src, slots ? nullptr : wrow, stream)) != QMM_OK)
         return st;
     if ((e = mark(d, 4, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
-    e = launch_combine(Yslot, P, rb.row, rb.w, T, k, D, Y, d->err, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "expert stage: combine");
+    if (slots) {
+        e = launch_combine(Yslot, P, rb.row, rb.w, T, k, D, Y, d->err, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "expert stage: combine");
+    }
     if ((e = mark(d, 5, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
     return QMM_OK;
 }
@@ -600,7 +626,8 @@ qmm_status qmm_dbg_down_iq4(const int8_t* Hq, const uint16_t* Hd, const int32_t*
         e = launch_hd_to_entries(reinterpret_cast<const __half*>(Hd), rb.tiles, rb.num_entries, rb.max_entries, F / 32,
                                  Hd32, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_dbg_down_iq4: operand layout");
-    return run_down(d, Hq16, Hd32, P, D, F, E, Wd_idx, Wd_s, rb.tiles, rb.num_entries, rb.max_entries, Yslot, stream);
+    return run_down(d, Hq16, Hd32, P, D, F, E, Wd_idx, Wd_s, rb.tiles, rb.num_entries, rb.max_entries, Yslot, nullptr,
+                    nullptr, stream);
 }
 
 qmm_status qmm_dbg_combine(const float* Yslot, int P, const int32_t* row, const float* w, int T, int k, int D,

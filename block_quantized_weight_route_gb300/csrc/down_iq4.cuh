@@ -118,7 +118,11 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t saddr) {
 // p.Y: Yslot [T*k][D] fp32 (p.ldy = D).
 // tmA: IQ4 codes as [E*D][F/2] bytes, box {32, 128}, 32-byte swizzle.
 // tmB: H codes as [T*k][F] f16, box {64, 128}, 128-byte swizzle.
-template <class C>
+// COMBINE = false: each routed row's outputs are stored to p.Y = Yslot [T*k][D];
+// COMBINE = true: the weighted combine is fused in: Y[src[r], n] += wrow[r] * y[r, n]
+// into p.Y = Y [T][D] (zeroed beforehand), with fp32 atomic adds (red.global.add),
+// so the order of a token's k contributions is not fixed.
+template <class C, bool COMBINE>
 __global__ void __launch_bounds__(C::THREADS, 1)
     down_iq4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -365,13 +369,39 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 sph ^= 1u;
             }
             if (!ok) break;
-            // Yslot[row, n] for this warp's token columns; lanes write consecutive n
-            float* out = static_cast<float*>(p.Y) + (long)g4.y * p.ldy + n0 + r;
             const int tok0 = cq * C::CPW;
+            if constexpr (!COMBINE) {
+                // Yslot[row, n] for this warp's token columns; lanes write consecutive n
+                float* out = static_cast<float*>(p.Y) + (long)g4.y * p.ldy + n0 + r;
 #pragma unroll
-            for (int j = 0; j < C::CPW / 2; ++j) {
-                if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = y[j].x;
-                if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = y[j].y;
+                for (int j = 0; j < C::CPW / 2; ++j) {
+                    if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = y[j].x;
+                    if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = y[j].y;
+                }
+            } else {
+                // Y[token, n] += weight * y for this warp's token columns: lane l holds the
+                // token and weight of columns l, l+32, ...; each column's pair is broadcast
+                // and the 32 lanes add 32 consecutive n (one 128-byte reduction)
+                constexpr int NC = C::CPW / 32;
+                int tk[NC];
+                float wt[NC];
+#pragma unroll
+                for (int i = 0; i < NC; ++i) {
+                    const int c = tok0 + 32 * i + lane;
+                    tk[i] = c < g4.z ? __ldg(p.src + g4.y + c) : 0;
+                    wt[i] = c < g4.z ? __ldg(p.wrow + g4.y + c) : 0.f;
+                }
+                float* out = static_cast<float*>(p.Y) + n0 + r;
+#pragma unroll
+                for (int j = 0; j < C::CPW / 2; ++j) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 2 * j + h;
+                        const int t = __shfl_sync(0xffffffffu, tk[c >> 5], c & 31);
+                        const float wc = __shfl_sync(0xffffffffu, wt[c >> 5], c & 31);
+                        if (tok0 + c < g4.z) atomicAdd(out + (long)t * p.ldy, wc * (h ? y[j].y : y[j].x));
+                    }
+                }
             }
             g4 = g4n;
         }

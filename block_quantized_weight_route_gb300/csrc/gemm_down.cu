@@ -5,13 +5,19 @@ namespace qmm {
 
 int smem_iq4_down() { return DownCfg::SMEM_BYTES; }
 
-cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
-                            cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(down_iq4_kernel<DownCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <bool COMBINE>
+static cudaError_t launch_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                               cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(down_iq4_kernel<DownCfg, COMBINE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DownCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    down_iq4_kernel<DownCfg><<<grid, DownCfg::THREADS, DownCfg::SMEM_BYTES, s>>>(tmA, tmB, p);
+    down_iq4_kernel<DownCfg, COMBINE><<<grid, DownCfg::THREADS, DownCfg::SMEM_BYTES, s>>>(tmA, tmB, p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid, bool combine,
+                            cudaStream_t s) {
+    return combine ? launch_down<true>(tmA, tmB, p, grid, s) : launch_down<false>(tmA, tmB, p, grid, s);
 }
 
 }  // namespace qmm

@@ -23,6 +23,8 @@ struct GemmParams {
     const float* blk_scale; // FP8: [N/128][K/128] block scales
     const float* dH32;      // down: fp32 d of H per 128-row tile entry, [entry][K/32][128]
     const __half* dW;       // down: IQ4_NL block scales, [E][N][K/32]
+    const int32_t* src;     // down with the combine fused: token of each routed row [P]
+    const float* wrow;      // down with the combine fused: routing weight of each routed row [P]
     void* Y;                // output (fp32 or bf16)
     int ydt;                // 0: fp32, 1: bf16
     long ldy;               // output row pitch in elements
@@ -61,7 +63,9 @@ TileShape w4_gate_up_shape();
 int fp8_tile_rows();
 cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                               cudaStream_t s);
-cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+// combine = false: per-slot rows p.Y [P][N] fp32; true: Y[src[r]] += wrow[r] * y_r
+// accumulated into p.Y [T][N] fp32 (which must start at zero).
+cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid, bool combine,
                             cudaStream_t s);
 
 int smem_iq4_down();
@@ -81,6 +85,9 @@ struct RouteBufs {
     int4* tiles2;         // [max_entries2] 256-row entries (optional, needs tiles)
     int32_t* num_entries2;
     int max_entries2;
+    float* wrow = nullptr;    // [T*k] weight of the pair at each routed row (optional)
+    float* yzero = nullptr;   // [T][yzero_D] fp32 rows set to zero by the top-k kernel (optional)
+    int yzero_D = 0;
 };
 constexpr int kRouteChunk = 256;   // tokens per grouping chunk
 cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBufs& b, cudaStream_t s);

@@ -23,12 +23,19 @@ constexpr int kMaxK = 16;
 
 // One warp per token.  Lane l holds logits l, l+32, ...; k rounds of a warp
 // arg-max (ties to the lower expert index) pick the experts in descending order.
+// With yz, the warp also sets row t of yz [T][D] fp32 to zero (the output the
+// down product then accumulates into, when the combine is fused into it).
 template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                         int32_t* __restrict__ ids, float* __restrict__ w) {
+                                                         int32_t* __restrict__ ids, float* __restrict__ w,
+                                                         float* __restrict__ yz, int D) {
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+        if (yz) {
+            float4* row = reinterpret_cast<float4*>(yz + (long)t * D);
+            for (int i = lane; i < D / 4; i += 32) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         float v[EPL];
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
@@ -193,11 +200,14 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int chunks, int E, int
 // One CTA per chunk (blockDim == kRouteChunk, one token per thread): the rank of
 // a pair among its expert's pairs inside the chunk is the number of earlier
 // tokens of the chunk whose bit is set in that expert's mask.
+// With wrow, also the routing weight of each routed row: wrow[row] = w[t][j].
 __global__ void __launch_bounds__(kRouteChunk) route_permute_kernel(const int32_t* __restrict__ ids, int T, int E,
                                                                     int k, const int32_t* __restrict__ chunk_base,
                                                                     const int32_t* __restrict__ offsets,
                                                                     int32_t* __restrict__ src,
-                                                                    int32_t* __restrict__ row) {
+                                                                    int32_t* __restrict__ row,
+                                                                    const float* __restrict__ w,
+                                                                    float* __restrict__ wrow) {
     constexpr int WORDS = kRouteChunk / 32;
     extern __shared__ uint32_t masks[];   // [E][WORDS]
     for (int i = threadIdx.x; i < E * WORDS; i += blockDim.x) masks[i] = 0;
@@ -225,6 +235,7 @@ __global__ void __launch_bounds__(kRouteChunk) route_permute_kernel(const int32_
                 const int r = offsets[e] + chunk_base[(long)blockIdx.x * E + e] + rank;
                 row[t * k + j] = r;
                 src[r] = (int32_t)t;
+                if (wrow) wrow[r] = w[t * k + j];
             }
         }
     }
@@ -238,7 +249,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBu
     switch (epl) {
 #define QMM_TOPK_CASE(N)                                                                    \
     case N:                                                                                 \
-        route_topk_kernel<N><<<grid_topk, 256, 0, s>>>(logits, T, E, k, b.ids, b.w);       \
+        route_topk_kernel<N><<<grid_topk, 256, 0, s>>>(logits, T, E, k, b.ids, b.w, b.yzero, b.yzero_D); \
         break;
         QMM_TOPK_CASE(1) QMM_TOPK_CASE(2) QMM_TOPK_CASE(3) QMM_TOPK_CASE(4) QMM_TOPK_CASE(5) QMM_TOPK_CASE(6)
         QMM_TOPK_CASE(7) QMM_TOPK_CASE(8) QMM_TOPK_CASE(9) QMM_TOPK_CASE(10) QMM_TOPK_CASE(11) QMM_TOPK_CASE(12)
@@ -252,7 +263,8 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, const RouteBu
     route_scan_kernel<<<1, 1024, 0, s>>>(chunks, E, b.chunk_hist, b.counts, b.offsets, b.tiles, b.num_entries,
                                          b.max_entries, b.tiles2, b.num_entries2, b.max_entries2);
     const size_t msmem = (size_t)E * (kRouteChunk / 32) * sizeof(uint32_t);
-    route_permute_kernel<<<chunks, kRouteChunk, msmem, s>>>(b.ids, T, E, k, b.chunk_hist, b.offsets, b.src, b.row);
+    route_permute_kernel<<<chunks, kRouteChunk, msmem, s>>>(b.ids, T, E, k, b.chunk_hist, b.offsets, b.src, b.row, b.w,
+                                                            b.wrow);
     return cudaGetLastError();
 }
 

@@ -144,12 +144,33 @@ qmm_status moe_route_permute(const float *logits, int T, int E, int k, int32_t *
  *   its regions (routing outputs, permuted X, H codes/scales, per-row down
  *   outputs) are listed by moe_expert_stage_workspace_layout().
  * Shapes: D % 128 == 0, F % 128 == 0, F <= 1024, 1 <= k <= 16, k <= E <= 512, T >= 0.
+ * The weighted combine is fused into the down product: each routed row's
+ * outputs are added, times its weight, into Y with fp32 atomic adds (Y is
+ * zeroed by the routing step), so the order in which a token's k terms are
+ * summed is not fixed and Y may differ between calls in the last bits (well
+ * inside the stage tolerance); moe_expert_stage_w4_iq4_ex with QMM_STAGE_SLOTS
+ * gives the j-ordered, reproducible sum instead.
  */
 size_t moe_expert_stage_workspace_size(int T, int D, int F, int E, int k);
 qmm_status moe_expert_stage_w4_iq4(const uint16_t *X, const float *logits, int T, int D, int F, int E, int k,
                                    const uint8_t *Wgu_c, const uint8_t *Wgu_s, const float *gu_scale2,
                                    const uint8_t *Wd_idx, const uint16_t *Wd_s, float *Y, void *ws, size_t ws_bytes,
                                    cudaStream_t stream);
+
+/*
+ * moe_expert_stage_w4_iq4_ex -- moe_expert_stage_w4_iq4 with options.
+ *   flags = 0: as moe_expert_stage_w4_iq4 (combine fused into the down product).
+ *   flags = QMM_STAGE_SLOTS: the down product writes every routed row's outputs to
+ *     the workspace region Yslot [T*k][D] fp32, and a separate combine kernel
+ *     forms Y[t] = sum_j w[t][j] * Yslot[row[t][j]] in ascending j: the same
+ *     result every call, and the per-row down outputs stay inspectable.
+ * Other flag bits: QMM_ERR_INVALID_ARG.
+ */
+#define QMM_STAGE_SLOTS 1u
+qmm_status moe_expert_stage_w4_iq4_ex(const uint16_t *X, const float *logits, int T, int D, int F, int E, int k,
+                                      const uint8_t *Wgu_c, const uint8_t *Wgu_s, const float *gu_scale2,
+                                      const uint8_t *Wd_idx, const uint16_t *Wd_s, float *Y, void *ws, size_t ws_bytes,
+                                      unsigned flags, cudaStream_t stream);
 
 /* Byte offsets, inside the expert-stage workspace, of its regions (for callers
  * that inspect intermediate results).  Writes QMM_WS_FIELDS offsets in this order:
@@ -159,9 +180,11 @@ qmm_status moe_expert_stage_w4_iq4(const uint16_t *X, const float *logits, int T
  *  11 X_perm [T*k][D] bf16   12 Hq [T*k][F] fp16: the q8_1 codes (integers in [-127, 127]) held
  *     exactly as f16, the operand type of the down product's tensor-core MMA
  *  13 Hd [T*k][F/32] fp16   14 Hs [T*k][F/32] fp16
- *  15 d of H as fp32 per 128-row tile (internal)   16 Yslot [T*k][D] fp32
- *  17 total size */
-#define QMM_WS_FIELDS 18
+ *  15 d of H as fp32 per 128-row tile (internal)
+ *  16 Yslot [T*k][D] fp32 (written with QMM_STAGE_SLOTS only)
+ *  17 wrow [T*k] fp32: the routing weight of each routed row (fused combine)
+ *  18 total size */
+#define QMM_WS_FIELDS 19
 qmm_status moe_expert_stage_workspace_layout(int T, int D, int F, int E, int k, size_t *offsets_out);
 
 /*
@@ -238,7 +261,8 @@ qmm_status moe_route_permute_noalloc(const float *logits, int T, int E, int k, i
  * Phase timing of the expert stage (for benchmarks).  With profiling on, each
  * moe_expert_stage_w4_iq4 call records CUDA events on its stream between its
  * phases: 0 routing (top-k, counts, scan, permutation), 1 row gather of X,
- * 2 gate/up + SwiGLU + q8_1, 3 down, 4 combine.  qmm_profile_read() waits for
+ * 2 gate/up + SwiGLU + q8_1, 3 down (with the fused combine), 4 the separate
+ * combine kernel (QMM_STAGE_SLOTS only; otherwise empty).  qmm_profile_read() waits for
  * the last profiled call's events and writes its QMM_PROFILE_PHASES phase times
  * in milliseconds; qmm_profile_read_call(i, ...) does the same for the i-th call
  * (0-based) since profiling was switched on, for the last QMM_PROFILE_RING such

@@ -87,6 +87,11 @@ def test_argument_checks_return_before_any_device_work(L):
     need = L.moe_route_workspace_size(1000, 128, 8)
     assert need >= 4 * 128 * 4
     assert L.moe_route_permute(P(256), 1000, 128, 8, *([P(256)] * 7), need - 1, None) == 4
+    # the stage with options: an unknown flag bit is rejected before any device work
+    L.moe_expert_stage_w4_iq4_ex.restype = ctypes.c_int
+    L.moe_expert_stage_w4_iq4_ex.argtypes = [P, P] + [ctypes.c_int] * 5 + [P] * 7 + [sz, ctypes.c_uint, P]
+    assert L.moe_expert_stage_w4_iq4_ex(P(256), P(256), 10, 256, 256, 8, 2, *([P(256)] * 7), 1 << 30, 2, None) == 1
+    assert b"flags" in L.qmm_last_error()
 
 
 def test_expert_stage_workspace_layout_is_consistent(L):
@@ -105,6 +110,7 @@ def test_expert_stage_workspace_layout_is_consistent(L):
         assert off[12] - off[11] >= P * D * 2         # X_perm
         assert off[13] - off[12] >= P * F * 2         # Hq (f16 codes)
         assert off[17] - off[16] >= P * D * 4         # Yslot
+        assert off[18] - off[17] >= P * 4             # wrow
     arr = (ctypes.c_size_t * QMM_WS_FIELDS)()
     assert L.moe_expert_stage_workspace_layout(10, 100, 128, 8, 2, arr) == 2     # D % 128
     assert L.moe_expert_stage_workspace_layout(10, 128, 2048, 8, 2, arr) == 2    # F > 1024

@@ -279,8 +279,12 @@ def run_stage(qlib, g, k):
     F = g["Wgu_c"].shape[1] // 2
     size = qlib.moe_expert_stage_workspace_size(T, D, F, E, k)
     ws = torch.empty(size, dtype=torch.uint8, device="cuda")
-    Y = qlib.moe_expert_stage_w4_iq4(bf16_dev(g["X"]), dev(g["logits"]), dev(g["Wgu_c"]), dev(g["Wgu_s"]),
-                                     dev(g["gu_scale2"]), dev(g["Wd_idx"]), dev(g["Wd_s"].view(np.int16)), k, ws=ws)
+    args = (bf16_dev(g["X"]), dev(g["logits"]), dev(g["Wgu_c"]), dev(g["Wgu_s"]), dev(g["gu_scale2"]),
+            dev(g["Wd_idx"]), dev(g["Wd_s"].view(np.int16)), k)
+    # the default stage (combine fused into the down product, fp32 atomics), then
+    # the per-slot stage, whose workspace keeps every routed row's down outputs
+    Yf = qlib.moe_expert_stage_w4_iq4(*args, ws=ws).cpu().numpy()
+    Y = qlib.moe_expert_stage_w4_iq4(*args, ws=ws, slots=True)
     torch.cuda.synchronize()
     qlib.qmm_check_status()
     lay = qlib.moe_expert_stage_workspace_layout(T, D, F, E, k)
@@ -289,7 +293,7 @@ def run_stage(qlib, g, k):
     # the q8_1 codes are held as f16; every one must be an integer in [-127, 127]
     hq16 = view("Hq", torch.float16, (P, F)).astype(np.float64)
     assert np.all(hq16 == np.round(hq16)) and np.all(np.abs(hq16) <= 127)
-    return dict(Y=Y.cpu().numpy(), Hq=hq16.astype(np.int8), Hd=view("Hd", torch.int16, (P, F // 32)),
+    return dict(Y=Y.cpu().numpy(), Yf=Yf, Hq=hq16.astype(np.int8), Hd=view("Hd", torch.int16, (P, F // 32)),
                 Yslot=view("Yslot", torch.float32, (P, D)), row=view("row", torch.int32, (T, k)),
                 src=view("src", torch.int32, (P,)), offsets=view("offsets", torch.int32, (E + 1,)))
 
@@ -310,9 +314,12 @@ def check_stage(qlib, g, k, tokens=None):
     ys = oracle.moe_down_iq4(gpu["Hq"][rows], gpu["Hd"][rows].view(np.uint16), r["offsets"], rows,
                              g["Wd_idx"], g["Wd_s"])
     assert rel_err(gpu["Yslot"][rows], ys) <= 1e-5
-    # the whole stage
+    # the whole stage, both forms of the combine; the fused one differs from the
+    # j-ordered sum only by the order of at most k fp32 additions per output
     toks = st["tokens"]
     assert rel_err(gpu["Y"][toks], st["Y"]) <= STAGE_TOL
+    assert rel_err(gpu["Yf"][toks], st["Y"]) <= STAGE_TOL
+    assert np.max(np.abs(gpu["Yf"] - gpu["Y"])) <= 1e-6 * np.max(np.abs(gpu["Y"]))
     return gpu, st
 
 

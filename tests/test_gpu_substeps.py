@@ -1,6 +1,6 @@
 """Parity of each expert-stage sub-step (the qmm_dbg_* calls of the C ABI) with
 the oracle, each step fed the oracle's own inputs for it, plus the check that
-the three steps chained on the GPU reproduce the fused stage bit for bit.
+the three steps chained on the GPU reproduce the per-slot stage bit for bit.
 
 Tolerances: q8_1 codes of H >= 99.9% equal and the rest off by one, d of H
 within one fp16 ulp (the fp32 h feeding the block maximum is summed in another
@@ -122,14 +122,17 @@ def test_dbg_combine_matches_oracle(qlib, T, k, D):
 
 def test_dbg_chain_reproduces_fused_stage(qlib):
     """route (from the stage's workspace) -> gate/up -> down -> combine through the
-    sub-step calls gives the fused stage's Y bit for bit (same kernels)."""
+    sub-step calls gives the per-slot stage's Y (QMM_STAGE_SLOTS) bit for bit (same
+    kernels), and the default stage, whose down product adds into Y with fp32
+    atomics, agrees with it up to the order of the k terms."""
     T, D, F, E, k = 333, 256, 256, 16, 4
     g = wl.gen_moe(T, D, F, E, k, 1.0 / 128, 1.0, seed=25)
     size = qlib.moe_expert_stage_workspace_size(T, D, F, E, k)
     ws = torch.empty(size, dtype=torch.uint8, device="cuda")
     Xd = dev(g["X"].view(np.int16)).view(torch.bfloat16)
     args = (dev(g["Wgu_c"]), dev(g["Wgu_s"]), dev(g["gu_scale2"]), dev(g["Wd_idx"]), dev(g["Wd_s"].view(np.int16)))
-    Y = qlib.moe_expert_stage_w4_iq4(Xd, dev(g["logits"]), *args, k, ws=ws)
+    Yf = qlib.moe_expert_stage_w4_iq4(Xd, dev(g["logits"]), *args, k, ws=ws)
+    Y = qlib.moe_expert_stage_w4_iq4(Xd, dev(g["logits"]), *args, k, ws=ws, slots=True)
     qlib.qmm_check_status()
     lay = qlib.moe_expert_stage_workspace_layout(T, D, F, E, k)
     P = T * k
@@ -141,6 +144,7 @@ def test_dbg_chain_reproduces_fused_stage(qlib):
     Y2 = qlib.qmm_dbg_combine(Ys, row, w)
     qlib.qmm_check_status()
     assert torch.equal(Y, Y2)
+    assert float((Yf - Y).abs().max()) <= 1e-6 * float(Y.abs().max())
 
 
 def test_dbg_bad_offsets_are_reported(qlib):
