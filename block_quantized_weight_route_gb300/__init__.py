@@ -83,6 +83,10 @@ def lib() -> ctypes.CDLL:
         L.qmm_dbg_down_iq4.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, sz, P]
         L.qmm_dbg_combine.restype = i32
         L.qmm_dbg_combine.argtypes = [P, i32, P, P, i32, i32, i32, P, P]
+        L.qmm_q8_0_q8_1_workspace_size.restype = sz
+        L.qmm_q8_0_q8_1_workspace_size.argtypes = [i32, i32, i32]
+        L.qmm_q8_0_q8_1.restype = i32
+        L.qmm_q8_0_q8_1.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
         L.qmm_dbg_wait_timeout.restype = i32
         L.qmm_dbg_wait_timeout.argtypes = [ctypes.c_uint, P]
         _lib = L
@@ -177,6 +181,34 @@ def qmm_fp8_blk128(X, W, S, Y=None, ws=None):
                                  _ptr(ws) if ws is not None else None, nws, _stream(X.device))
     _check("qmm_fp8_blk128", st)
     return Y
+
+
+def qmm_q8_0_q8_1_workspace_size(M: int, K: int, N: int) -> int:
+    return int(lib().qmm_q8_0_q8_1_workspace_size(M, K, N))
+
+
+def qmm_q8_0_q8_1(Xq, Xd, Wq, Wd, ws=None, fp32_out: bool = False) -> dict:
+    """Dense Q8_0 x q8_1 projection with its output rounded to q8_1 blocks.
+    Xq int8 [M, K], Xd fp16 bits [M, K/32]; Wq int8 [N, K], Wd fp16 bits [N, K/32].
+    Returns Yq int8 [M, N], Yd / Ys fp16 bits [M, N/32] and, with fp32_out, the
+    fp32 rows Y [M, N] before the rounding."""
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    _need(Xq, "Xq", _U8, (M, K))
+    _need(Xd, "Xd", _F16, (M, K // 32))
+    _need(Wq, "Wq", _U8, (N, K))
+    _need(Wd, "Wd", _F16, (N, K // 32))
+    dev = Xq.device
+    if ws is None:
+        ws = torch.empty(max(qmm_q8_0_q8_1_workspace_size(M, K, N), 256), dtype=torch.uint8, device=dev)
+    _need(ws, "ws", _U8)
+    Yq = torch.empty((M, N), dtype=torch.int8, device=dev)
+    Yd = torch.empty((M, N // 32), dtype=torch.int16, device=dev)
+    Ys = torch.empty((M, N // 32), dtype=torch.int16, device=dev)
+    Y = torch.empty((M, N), dtype=torch.float32, device=dev) if fp32_out else None
+    _check("qmm_q8_0_q8_1", lib().qmm_q8_0_q8_1(_ptr(Xq), _ptr(Xd), M, K, N, _ptr(Wq), _ptr(Wd), _ptr(Yq), _ptr(Yd),
+                                                _ptr(Ys), _ptr(Y), _ptr(ws), ws.numel(), _stream(dev)))
+    return dict(Yq=Yq, Yd=Yd, Ys=Ys, Y=Y)
 
 
 def moe_route_workspace_size(T: int, E: int, k: int) -> int:

@@ -312,6 +312,83 @@ qmm_status qmm_fp8_blk128_ws(const uint16_t* X, int M, int K, int N, const uint8
     return QMM_OK;
 }
 
+// ---------------------------------------------------------------- dense Q8_0 x q8_1
+
+// Workspace of qmm_q8_0_q8_1: f16 activation codes [M][K], the activations' d per
+// 128-row tile [entries][K/32][128] fp32, the tile list and its count.
+static void q8_layout(int M, int K, size_t* off) {
+    const int entries = (M + 127) / 128;
+    const size_t sz[4] = {(size_t)M * K * 2, (size_t)entries * (K / 32) * 128 * 4, (size_t)entries * 16, 16};
+    size_t o = 0;
+    for (int i = 0; i < 4; ++i) {
+        off[i] = o;
+        o = align_up(o + sz[i], 256);
+    }
+    off[4] = o;
+}
+
+size_t qmm_q8_0_q8_1_workspace_size(int M, int K, int N) {
+    (void)N;
+    if (M < 1 || K < 256 || K % 256) return 0;
+    size_t off[5];
+    q8_layout(M, K, off);
+    return off[4];
+}
+
+qmm_status qmm_q8_0_q8_1(const int8_t* Xq, const uint16_t* Xd, int M, int K, int N, const int8_t* Wq,
+                         const uint16_t* Wd, int8_t* Yq, uint16_t* Yd, uint16_t* Ys, float* Y, void* ws,
+                         size_t ws_bytes, cudaStream_t stream) {
+    if (M < 1 || K < 256 || K % 256 || N < 128 || N % 128)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE, "qmm_q8_0_q8_1: need M >= 1, K %% 256 == 0, N %% 128 == 0 (M=%d K=%d N=%d)",
+                    M, K, N);
+    if (!Xq || !Xd || !Wq || !Wd || !Yq || !Yd || !Ys || !ws)
+        return fail(QMM_ERR_INVALID_ARG, "qmm_q8_0_q8_1: null pointer");
+    if (!aligned16(Xq) || !aligned16(Xd) || !aligned16(Wq) || !aligned16(Wd) || !aligned16(Yq) || !aligned16(Yd) ||
+        !aligned16(Ys) || (Y && !aligned16(Y)) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return fail(QMM_ERR_INVALID_ARG, "qmm_q8_0_q8_1: buffers must be 16-byte aligned (workspace 256-byte aligned)");
+    const size_t need = qmm_q8_0_q8_1_workspace_size(M, K, N);
+    if (ws_bytes < need) return fail(QMM_ERR_WORKSPACE, "qmm_q8_0_q8_1: workspace %zu < %zu bytes", ws_bytes, need);
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    size_t off[5];
+    q8_layout(M, K, off);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    __half* X16 = reinterpret_cast<__half*>(base + off[0]);
+    float* dX32 = reinterpret_cast<float*>(base + off[1]);
+    int4* tiles = reinterpret_cast<int4*>(base + off[2]);
+    int32_t* count = reinterpret_cast<int32_t*>(base + off[3]);
+    const int entries = (M + 127) / 128;
+    cudaError_t e = launch_dense_tiles(M, tiles, count, stream);
+    if (e == cudaSuccess) e = launch_codes_i8_to_f16(Xq, X16, (long)M * K, stream);
+    if (e == cudaSuccess)
+        e = launch_hd_to_entries(reinterpret_cast<const __half*>(Xd), tiles, count, entries, K / 32, dX32, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_q8_0_q8_1: operand layout");
+    CUtensorMap ta, tb, tw;
+    if ((st = make_tmap(&ta, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) != QMM_OK)
+        return st;
+    if ((st = make_tmap(&tb, X16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, M, (uint64_t)K * 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
+        return st;
+    if ((st = make_tmap(&tw, Wd, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K / 32, N, K / 16, 8, 128,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != QMM_OK)
+        return st;
+    GemmParams p{};
+    p.N = N;
+    p.K = K;
+    p.n_tiles = N / 128;
+    p.n_step = 128;
+    p.tiles = tiles;
+    p.num_entries = count;
+    p.max_entries = entries;
+    p.dH32 = dX32;
+    p.err = d->err;
+    e = launch_q8_dense(ta, tb, tw, p, Yq, reinterpret_cast<__half*>(Yd), reinterpret_cast<__half*>(Ys), Y, M, d->sms,
+                        stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_q8_0_q8_1 launch");
+    return QMM_OK;
+}
+
 size_t moe_route_workspace_size(int T, int E, int k) {
     (void)k;
     if (T < 0 || E < 1) return 0;

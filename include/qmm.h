@@ -104,6 +104,28 @@ qmm_status qmm_fp8_blk128_ws(const uint16_t *X, int M, int K, int N, const uint8
                              void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * qmm_q8_0_q8_1 -- dense projection with Q8_0 weights and q8_1 activations,
+ * the output rounded to q8_1 blocks ("Run Edge0-145B Q3_K on AMD HIP (Linux,
+ * gfx1100)", commit 17c02cd: the D and U projections of a latent layer as
+ * Q8_0 x q8_1 integer dots, D re-quantising its products to q8_1 and writing the
+ * fp32 rows too when asked):
+ *   y[m,n] = sum_b fp16(Xd[m][b]) * fp16(Wd[n][b]) * sum_{k in block b} Xq[m][k] * Wq[n][k]
+ *   (one exact integer dot per block of 32, folded in fp32), then per row m and
+ *   32 consecutive n: d = max|y|/127, q = round-half-away(y/d) in [-127, 127],
+ *   Yq = q, Yd = fp16(d), Ys = fp16(d * sum q)  (all zero for an all-zero block).
+ *   Xq [M][K] int8, Xd [M][K/32] fp16 (the q8_1 activations' d);
+ *   Wq [N][K] int8, Wd [N][K/32] fp16 (Q8_0: 32 codes and one scale per block);
+ *   Yq [M][N] int8, Yd / Ys [M][N/32] fp16; Y [M][N] fp32 before the rounding, or NULL.
+ *   ws: device scratch of at least qmm_q8_0_q8_1_workspace_size(M, K, N) bytes,
+ *   256-byte aligned (the activation codes as f16 and per-tile d tables).
+ * Shapes: M >= 1, K % 256 == 0, N % 128 == 0.
+ */
+size_t qmm_q8_0_q8_1_workspace_size(int M, int K, int N);
+qmm_status qmm_q8_0_q8_1(const int8_t *Xq, const uint16_t *Xd, int M, int K, int N, const int8_t *Wq,
+                         const uint16_t *Wd, int8_t *Yq, uint16_t *Yd, uint16_t *Ys, float *Y, void *ws,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/*
  * moe_route_permute -- top-k routing and per-expert grouping of T tokens.
  * For each token t: ids[t][0..k) are the k largest logits (descending; a tie
  * goes to the lower expert index) and w[t][j] = exp(l_j - l_max) / sum over the

@@ -87,6 +87,16 @@ def test_argument_checks_return_before_any_device_work(L):
     need = L.moe_route_workspace_size(1000, 128, 8)
     assert need >= 4 * 128 * 4
     assert L.moe_route_permute(P(256), 1000, 128, 8, *([P(256)] * 7), need - 1, None) == 4
+    # the dense Q8_0 x q8_1 projection: K not a multiple of 256, N not of 128, null pointers
+    L.qmm_q8_0_q8_1.restype = ctypes.c_int
+    L.qmm_q8_0_q8_1.argtypes = [P, P] + [ctypes.c_int] * 3 + [P] * 7 + [sz, P]
+    assert L.qmm_q8_0_q8_1(*([P(256)] * 2), 64, 200, 128, *([P(256)] * 7), 1 << 30, None) == 2
+    assert L.qmm_q8_0_q8_1(*([P(256)] * 2), 64, 256, 100, *([P(256)] * 7), 1 << 30, None) == 2
+    assert L.qmm_q8_0_q8_1(None, None, 64, 256, 128, *([None] * 7), 1 << 30, None) == 1
+    L.qmm_q8_0_q8_1_workspace_size.restype = sz
+    L.qmm_q8_0_q8_1_workspace_size.argtypes = [ctypes.c_int] * 3
+    assert L.qmm_q8_0_q8_1_workspace_size(2048, 5120, 8064) >= 2048 * 5120 * 2
+    assert L.qmm_q8_0_q8_1_workspace_size(2048, 100, 8064) == 0
     # the stage with options: an unknown flag bit is rejected before any device work
     L.moe_expert_stage_w4_iq4_ex.restype = ctypes.c_int
     L.moe_expert_stage_w4_iq4_ex.argtypes = [P, P] + [ctypes.c_int] * 5 + [P] * 7 + [sz, ctypes.c_uint, P]
