@@ -83,6 +83,12 @@ def lib() -> ctypes.CDLL:
         L.qmm_dbg_down_iq4.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, sz, P]
         L.qmm_dbg_combine.restype = i32
         L.qmm_dbg_combine.argtypes = [P, i32, P, P, i32, i32, i32, P, P]
+        L.moe_expert_table_size.restype = sz
+        L.moe_expert_table_size.argtypes = [i32]
+        L.moe_expert_table_build.restype = i32
+        L.moe_expert_table_build.argtypes = [i32, i32, i32, P, P, P, P, P, sz, P]
+        L.moe_expert_stage_w4_iq4_table.restype = i32
+        L.moe_expert_stage_w4_iq4_table.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, sz, ctypes.c_uint, P]
         L.qmm_q8_0_q8_1_workspace_size.restype = sz
         L.qmm_q8_0_q8_1_workspace_size.argtypes = [i32, i32, i32]
         L.qmm_q8_0_q8_1.restype = i32
@@ -283,6 +289,53 @@ def moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, k:
                                            _ptr(gu_scale2), _ptr(Wd_idx), _ptr(Wd_s), _ptr(Y), _ptr(ws), ws.numel(),
                                            _stream(dev))
     _check("moe_expert_stage_w4_iq4", st)
+    return Y
+
+
+def moe_expert_table_build(Wgu_c, Wgu_s, Wd_idx, Wd_s) -> torch.Tensor:
+    """A pointer table over per-expert weight tensors (lists of E CUDA tensors:
+    [2F, D/2] and [2F, D/16] uint8, [D, F/2] uint8, [D, F/32] fp16 bits).  Returns
+    the table (a uint8 device tensor); the weight tensors must outlive its use."""
+    E = len(Wgu_c)
+    if not (len(Wgu_s) == len(Wd_idx) == len(Wd_s) == E) or E < 1:
+        raise ValueError("four lists of E per-expert tensors")
+    F2, D2 = Wgu_c[0].shape
+    F, D = F2 // 2, D2 * 2
+    for e in range(E):
+        _need(Wgu_c[e], "Wgu_c[e]", _U8, (2 * F, D // 2))
+        _need(Wgu_s[e], "Wgu_s[e]", _U8, (2 * F, D // 16))
+        _need(Wd_idx[e], "Wd_idx[e]", _U8, (D, F // 2))
+        _need(Wd_s[e], "Wd_s[e]", _F16, (D, F // 32))
+    dev = Wgu_c[0].device
+    n = int(lib().moe_expert_table_size(E))
+    table = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    arr = lambda ts: (ctypes.c_void_p * E)(*[t.data_ptr() for t in ts])  # noqa: E731
+    _check("moe_expert_table_build",
+           lib().moe_expert_table_build(D, F, E, arr(Wgu_c), arr(Wgu_s), arr(Wd_idx), arr(Wd_s), _ptr(table),
+                                        table.numel(), _stream(dev)))
+    return table
+
+
+def moe_expert_stage_w4_iq4_table(X, logits, gu_scale2, table, F: int, k: int, ws=None, Y=None, slots: bool = False):
+    """moe_expert_stage_w4_iq4 over a pointer table of per-expert weights
+    (moe_expert_table_build)."""
+    T, D = X.shape
+    E = logits.shape[1]
+    _need(X, "X", _BF16, (T, D))
+    _need(logits, "logits", (torch.float32,), (T, E))
+    _need(gu_scale2, "gu_scale2", (torch.float32,), (E,))
+    _need(table, "table", _U8)
+    dev = X.device
+    if ws is None:
+        ws = torch.empty(max(moe_expert_stage_workspace_size(T, D, F, E, k), 256), dtype=torch.uint8, device=dev)
+    _need(ws, "ws", _U8)
+    if Y is None:
+        Y = torch.empty((T, D), dtype=torch.float32, device=dev)
+    _need(Y, "Y", (torch.float32,), (T, D))
+    _check("moe_expert_stage_w4_iq4_table",
+           lib().moe_expert_stage_w4_iq4_table(_ptr(X), _ptr(logits), T, D, F, E, k, _ptr(gu_scale2), _ptr(table),
+                                               _ptr(Y), _ptr(ws), ws.numel(), QMM_STAGE_SLOTS if slots else 0,
+                                               _stream(dev)))
     return Y
 
 

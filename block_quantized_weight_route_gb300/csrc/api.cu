@@ -5,6 +5,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/qmm.h"
 #include "ptx.cuh"
@@ -430,9 +431,29 @@ qmm_status moe_route_permute(const float* logits, int T, int E, int k, int32_t* 
 // Gate/up + SwiGLU + q8_1 over permuted rows Xp [P][D], grouped by the 256-row
 // tile list: 256 token rows x (64 gate + 64 up weight rows) per tile, clusters
 // of CTAs sharing the token rows.  Writes Hq (f16 codes), Hd, Hs, Hd32.
+// Pointer-table form of the expert weights (moe_expert_table_build): E tensor
+// maps of the gate/up codes, E of the down indices, then the E gate/up scale and
+// E down scale pointers.
+struct TableView {
+    const CUtensorMap* gu_maps;
+    const CUtensorMap* dn_maps;
+    const uint8_t* const* gu_scales;
+    const __half* const* dn_scales;
+};
+static size_t table_bytes(int E) { return align_up((size_t)E * (2 * sizeof(CUtensorMap) + 2 * sizeof(void*)), 256); }
+static TableView table_view(const void* table, int E) {
+    const uint8_t* b = static_cast<const uint8_t*>(table);
+    TableView v;
+    v.gu_maps = reinterpret_cast<const CUtensorMap*>(b);
+    v.dn_maps = v.gu_maps + E;
+    v.gu_scales = reinterpret_cast<const uint8_t* const*>(b + (size_t)2 * E * sizeof(CUtensorMap));
+    v.dn_scales = reinterpret_cast<const __half* const*>(v.gu_scales + E);
+    return v;
+}
+
 static qmm_status run_gate_up(DeviceState* d, const uint16_t* Xp, int P, int D, int F, int E, const uint8_t* Wgu_c,
-                              const uint8_t* Wgu_s, const float* gu_scale2, const RouteBufs& rb, __half* Hq,
-                              __half* Hd, __half* Hs, float* Hd32, cudaStream_t stream) {
+                              const uint8_t* Wgu_s, const TableView* tab, const float* gu_scale2, const RouteBufs& rb,
+                              __half* Hq, __half* Hd, __half* Hs, float* Hd32, cudaStream_t stream) {
     qmm_status st;
     // sh.rows token rows x (sh.bn / 2 gate + sh.bn / 2 up) weight rows per tile
     const TileShape sh = w4_gate_up_shape();
@@ -443,10 +464,17 @@ static qmm_status run_gate_up(DeviceState* d, const uint16_t* Xp, int P, int D, 
     if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, sh.rows / gu_cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
-    if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32, hstep,
-                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+    if (tab) {
+        memset(&tb, 0, sizeof tb);   // not read: every expert has its own map in the table
+    } else if ((st = make_tmap(&tb, Wgu_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)E * 2 * F, D / 2, 32,
+                               hstep, CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK) {
         return st;
+    }
     GemmParams g{};
+    if (tab) {
+        g.wmaps = tab->gu_maps;
+        g.wscale_tab = tab->gu_scales;
+    }
     g.K = D;
     g.F = F;
     g.n_tiles = F / hstep;
@@ -471,13 +499,17 @@ static qmm_status run_gate_up(DeviceState* d, const uint16_t* Xp, int P, int D, 
 // combine: Yslot [P][D] per routed row.  With one (src, wrow given): the weighted
 // combine is fused in, Y [T][D] += wrow[r] * y_r at token src[r] (Y zeroed first).
 static qmm_status run_down(DeviceState* d, const __half* Hq, const float* Hd32, int P, int D, int F, int E,
-                           const uint8_t* Wd_idx, const uint16_t* Wd_s, const int4* tiles, const int32_t* num_entries,
-                           int max_entries, float* out, const int32_t* src, const float* wrow, cudaStream_t stream) {
+                           const uint8_t* Wd_idx, const uint16_t* Wd_s, const TableView* tab, const int4* tiles,
+                           const int32_t* num_entries, int max_entries, float* out, const int32_t* src,
+                           const float* wrow, cudaStream_t stream) {
     qmm_status st;
     CUtensorMap ta, tb;
-    if ((st = make_tmap(&ta, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
-                        CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+    if (tab) {
+        memset(&ta, 0, sizeof ta);   // not read: every expert has its own map in the table
+    } else if ((st = make_tmap(&ta, Wd_idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)E * D, F / 2, 32, 128,
+                               CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK) {
         return st;
+    }
     if ((st = make_tmap(&tb, Hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, F, P, (uint64_t)F * 2, 64, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)
         return st;
@@ -491,6 +523,10 @@ static qmm_status run_down(DeviceState* d, const __half* Hq, const float* Hd32, 
     q.max_entries = max_entries;
     q.dH32 = Hd32;
     q.dW = reinterpret_cast<const __half*>(Wd_s);
+    if (tab) {
+        q.wmaps = tab->dn_maps;
+        q.dW_tab = tab->dn_scales;
+    }
     q.src = src;
     q.wrow = wrow;
     q.Y = out;
@@ -526,22 +562,29 @@ qmm_status moe_expert_stage_workspace_layout(int T, int D, int F, int E, int k, 
     return QMM_OK;
 }
 
+static qmm_status expert_stage(const uint16_t* X, const float* logits, int T, int D, int F, int E, int k,
+                               const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2, const uint8_t* Wd_idx,
+                               const uint16_t* Wd_s, const TableView* tab, float* Y, void* ws, size_t ws_bytes,
+                               unsigned flags, cudaStream_t stream);
+
 qmm_status moe_expert_stage_w4_iq4(const uint16_t* X, const float* logits, int T, int D, int F, int E, int k,
                                    const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2,
                                    const uint8_t* Wd_idx, const uint16_t* Wd_s, float* Y, void* ws, size_t ws_bytes,
                                    cudaStream_t stream) {
-    return moe_expert_stage_w4_iq4_ex(X, logits, T, D, F, E, k, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, Y, ws, ws_bytes,
-                                      0u, stream);
+    return expert_stage(X, logits, T, D, F, E, k, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, nullptr, Y, ws, ws_bytes, 0u,
+                        stream);
 }
 
-qmm_status moe_expert_stage_w4_iq4_ex(const uint16_t* X, const float* logits, int T, int D, int F, int E, int k,
-                                      const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2,
-                                      const uint8_t* Wd_idx, const uint16_t* Wd_s, float* Y, void* ws, size_t ws_bytes,
-                                      unsigned flags, cudaStream_t stream) {
+// The expert stage over contiguous [E][...] weights (tab == nullptr) or over a
+// pointer table of per-expert weights.
+static qmm_status expert_stage(const uint16_t* X, const float* logits, int T, int D, int F, int E, int k,
+                               const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2, const uint8_t* Wd_idx,
+                               const uint16_t* Wd_s, const TableView* tab, float* Y, void* ws, size_t ws_bytes,
+                               unsigned flags, cudaStream_t stream) {
     qmm_status st = check_stage_shape(T, D, F, E, k);
     if (st != QMM_OK) return st;
     if (flags & ~(unsigned)QMM_STAGE_SLOTS) return fail(QMM_ERR_INVALID_ARG, "moe_expert_stage_w4_iq4_ex: unknown flags");
-    if (!Wgu_c || !Wgu_s || !gu_scale2 || !Wd_idx || !Wd_s || (T > 0 && (!X || !logits || !Y || !ws)))
+    if (!gu_scale2 || (!tab && (!Wgu_c || !Wgu_s || !Wd_idx || !Wd_s)) || (T > 0 && (!X || !logits || !Y || !ws)))
         return fail(QMM_ERR_INVALID_ARG, "moe_expert_stage_w4_iq4: null pointer");
     if (!aligned16(X) || !aligned16(logits) || !aligned16(Wgu_c) || !aligned16(Wgu_s) || !aligned16(Wd_idx) ||
         !aligned16(Wd_s) || !aligned16(Y) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(ws) & 255u))
@@ -591,13 +634,13 @@ qmm_status moe_expert_stage_w4_iq4_ex(const uint16_t* X, const float* logits, in
     float* Yslot = static_cast<float*>(at(16));
 
     // gate/up + SwiGLU + q8_1
-    if ((st = run_gate_up(d, Xp, P, D, F, E, Wgu_c, Wgu_s, gu_scale2, rb, Hq, Hd, Hs, Hd32, stream)) != QMM_OK)
+    if ((st = run_gate_up(d, Xp, P, D, F, E, Wgu_c, Wgu_s, tab, gu_scale2, rb, Hq, Hd, Hs, Hd32, stream)) != QMM_OK)
         return st;
     if ((e = mark(d, 3, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
 
     // down (IQ4_NL weights on the MMA's M side, q8_1 H codes on its N side), with the
     // weighted combine fused in, or to per-slot rows followed by the combine kernel
-    if ((st = run_down(d, Hq, Hd32, P, D, F, E, Wd_idx, Wd_s, rb.tiles, rb.num_entries, max_entries,
+    if ((st = run_down(d, Hq, Hd32, P, D, F, E, Wd_idx, Wd_s, tab, rb.tiles, rb.num_entries, max_entries,
                        slots ? Yslot : Y, slots ? nullptr : rb.src, slots ? nullptr : wrow, stream)) != QMM_OK)
         return st;
     if ((e = mark(d, 4, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
@@ -608,6 +651,77 @@ qmm_status moe_expert_stage_w4_iq4_ex(const uint16_t* X, const float* logits, in
     }
     if ((e = mark(d, 5, stream)) != cudaSuccess) return cuda_fail(e, "profiling event");
     return QMM_OK;
+}
+
+qmm_status moe_expert_stage_w4_iq4_ex(const uint16_t* X, const float* logits, int T, int D, int F, int E, int k,
+                                      const uint8_t* Wgu_c, const uint8_t* Wgu_s, const float* gu_scale2,
+                                      const uint8_t* Wd_idx, const uint16_t* Wd_s, float* Y, void* ws, size_t ws_bytes,
+                                      unsigned flags, cudaStream_t stream) {
+    return expert_stage(X, logits, T, D, F, E, k, Wgu_c, Wgu_s, gu_scale2, Wd_idx, Wd_s, nullptr, Y, ws, ws_bytes, flags,
+                        stream);
+}
+
+// ---------------------------------------------------------------- per-expert pointer tables
+
+size_t moe_expert_table_size(int E) {
+    if (E < 1 || E > 512) return 0;
+    return table_bytes(E);
+}
+
+qmm_status moe_expert_table_build(int D, int F, int E, const uint8_t* const* Wgu_c, const uint8_t* const* Wgu_s,
+                                  const uint8_t* const* Wd_idx, const uint16_t* const* Wd_s, void* table,
+                                  size_t table_size, cudaStream_t stream) {
+    if (E < 1 || E > 512 || D < 128 || D % 128 || F < 128 || F % 128 || F > 1024)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE,
+                    "moe_expert_table_build: need 1 <= E <= 512, D %% 128 == 0, F %% 128 == 0, F <= 1024");
+    if (!Wgu_c || !Wgu_s || !Wd_idx || !Wd_s || !table)
+        return fail(QMM_ERR_INVALID_ARG, "moe_expert_table_build: null pointer");
+    if (reinterpret_cast<uintptr_t>(table) & 255u)
+        return fail(QMM_ERR_INVALID_ARG, "moe_expert_table_build: table must be 256-byte aligned");
+    if (table_size < table_bytes(E))
+        return fail(QMM_ERR_WORKSPACE, "moe_expert_table_build: table %zu < %zu bytes", table_size, table_bytes(E));
+    for (int e = 0; e < E; ++e) {
+        if (!Wgu_c[e] || !Wgu_s[e] || !Wd_idx[e] || !Wd_s[e])
+            return fail(QMM_ERR_INVALID_ARG, "moe_expert_table_build: null pointer for expert %d", e);
+        if (!aligned16(Wgu_c[e]) || !aligned16(Wgu_s[e]) || !aligned16(Wd_idx[e]) || !aligned16(Wd_s[e]))
+            return fail(QMM_ERR_INVALID_ARG, "moe_expert_table_build: expert %d's buffers must be 16-byte aligned", e);
+    }
+    DeviceState* d = nullptr;
+    qmm_status st = device_state(&d);
+    if (st != QMM_OK) return st;
+    // the table on the host, then one copy into the caller's device buffer
+    std::vector<uint8_t> host(table_bytes(E), 0);
+    CUtensorMap* gu = reinterpret_cast<CUtensorMap*>(host.data());
+    CUtensorMap* dn = gu + E;
+    const void** gus = reinterpret_cast<const void**>(host.data() + (size_t)2 * E * sizeof(CUtensorMap));
+    const void** dns = gus + E;
+    const int hstep = w4_gate_up_shape().bn / 2;
+    for (int e = 0; e < E; ++e) {
+        // the expert's gate/up codes [2F][D/2] and down indices [D][F/2], boxes as in the
+        // contiguous form
+        if ((st = make_tmap(&gu[e], Wgu_c[e], CU_TENSOR_MAP_DATA_TYPE_UINT8, D / 2, (uint64_t)2 * F, D / 2, 32, hstep,
+                            CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+            return st;
+        if ((st = make_tmap(&dn[e], Wd_idx[e], CU_TENSOR_MAP_DATA_TYPE_UINT8, F / 2, (uint64_t)D, F / 2, 32, 128,
+                            CU_TENSOR_MAP_SWIZZLE_32B)) != QMM_OK)
+            return st;
+        gus[e] = Wgu_s[e];
+        dns[e] = Wd_s[e];
+    }
+    cudaError_t e = cudaMemcpyAsync(table, host.data(), host.size(), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_expert_table_build: copy");
+    return QMM_OK;
+}
+
+qmm_status moe_expert_stage_w4_iq4_table(const uint16_t* X, const float* logits, int T, int D, int F, int E, int k,
+                                         const float* gu_scale2, const void* table, float* Y, void* ws,
+                                         size_t ws_bytes, unsigned flags, cudaStream_t stream) {
+    if (!table || (reinterpret_cast<uintptr_t>(table) & 255u))
+        return fail(QMM_ERR_INVALID_ARG, "moe_expert_stage_w4_iq4_table: table null or not 256-byte aligned");
+    const TableView tab = table_view(table, E);
+    return expert_stage(X, logits, T, D, F, E, k, nullptr, nullptr, gu_scale2, nullptr, nullptr, &tab, Y, ws, ws_bytes,
+                        flags, stream);
 }
 
 // ---------------------------------------------------------------- sub-step entry points
@@ -677,7 +791,7 @@ qmm_status qmm_dbg_gate_up_q8_1(const uint16_t* X_perm, const int32_t* offsets, 
     if ((st = dbg_tiles(d, offsets, P, E, base, off, &rb, stream)) != QMM_OK) return st;
     __half* Hq16 = reinterpret_cast<__half*>(base + off[4]);
     float* Hd32 = reinterpret_cast<float*>(base + off[5]);
-    if ((st = run_gate_up(d, X_perm, P, D, F, E, Wgu_c, Wgu_s, gu_scale2, rb, Hq16, reinterpret_cast<__half*>(Hd),
+    if ((st = run_gate_up(d, X_perm, P, D, F, E, Wgu_c, Wgu_s, nullptr, gu_scale2, rb, Hq16, reinterpret_cast<__half*>(Hd),
                           reinterpret_cast<__half*>(Hs), Hd32, stream)) != QMM_OK)
         return st;
     cudaError_t e = launch_codes_f16_to_i8(Hq16, Hq, (long)P * F, stream);
@@ -703,8 +817,8 @@ qmm_status qmm_dbg_down_iq4(const int8_t* Hq, const uint16_t* Hd, const int32_t*
         e = launch_hd_to_entries(reinterpret_cast<const __half*>(Hd), rb.tiles, rb.num_entries, rb.max_entries, F / 32,
                                  Hd32, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_dbg_down_iq4: operand layout");
-    return run_down(d, Hq16, Hd32, P, D, F, E, Wd_idx, Wd_s, rb.tiles, rb.num_entries, rb.max_entries, Yslot, nullptr,
-                    nullptr, stream);
+    return run_down(d, Hq16, Hd32, P, D, F, E, Wd_idx, Wd_s, nullptr, rb.tiles, rb.num_entries, rb.max_entries, Yslot,
+                    nullptr, nullptr, stream);
 }
 
 qmm_status qmm_dbg_combine(const float* Yslot, int P, const int32_t* row, const float* w, int T, int k, int D,

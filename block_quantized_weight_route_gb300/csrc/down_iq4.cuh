@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
+        if (!p.wmaps) tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
@@ -198,14 +198,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int entry = t / p.n_tiles;
                 const int n0 = (t - entry * p.n_tiles) * C::BM;
                 const int4 g = p.tiles[entry];
+                // the expert's IQ4 codes: its own tensor map (pointer-table form) at rows
+                // n0.., or the kernel parameter over the contiguous [E*D] rows
+                const CUtensorMap* amap = p.wmaps ? p.wmaps + g.x : &tmA;
+                const int arow = (p.wmaps ? 0 : g.x * p.N) + n0;
+                if (p.wmaps) tensormap_acquire(amap);
                 // this tile's d_H and d_W values
                 const bool got_s = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
                 if (__any_sync(0xffffffffu, !got_s)) break;
                 if (lane == 31) {
                     uint8_t* sst = sstage + ss * C::SSTAGE_BYTES;
+                    const __half* dw = p.dW_tab ? p.dW_tab[g.x] + (long)n0 * groups : p.dW + ((long)g.x * p.N + n0) * groups;
                     mbar_arrive_expect_tx(&full_s[ss], dh_bytes + dw_bytes);
                     bulk_load(sst, p.dH32 + (long)entry * groups * C::BN, dh_bytes, &full_s[ss]);
-                    bulk_load(sst + C::DH_BYTES, p.dW + ((long)g.x * p.N + n0) * groups, dw_bytes, &full_s[ss]);
+                    bulk_load(sst + C::DH_BYTES, dw, dw_bytes, &full_s[ss]);
                 }
                 __syncwarp();
                 ++s_issued;
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
                     __syncwarp();
                     if (lane == l0)
-                        tma_load_2d(st, &tmA, &full_t[s], kb * 32, g.x * p.N + n0);
+                        tma_load_2d(st, amap, &full_t[s], kb * 32, arow);
                     else if (lane == l0 + 1)
                         tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
                     __syncwarp();

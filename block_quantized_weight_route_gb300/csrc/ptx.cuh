@@ -139,6 +139,13 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// Make a tensor map in global memory, written before this kernel (by a copy or
+// another kernel), visible to the TMA unit before this thread's first use of it.
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
+                 : "memory");
+}
+
 // As tma_load_2d, but the box lands at the same shared-memory offset in every
 // CTA of the cluster named by cta_mask, and each of those CTAs' mbarriers at
 // `bar`'s offset receives the completed bytes.

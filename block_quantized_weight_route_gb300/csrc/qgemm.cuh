@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
+        if (!p.wmaps) tma_prefetch_desc(&tmB);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
@@ -491,6 +491,10 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             for (int t = cid; t < num_tiles && ok; t += ncl) {
                 const TileInfo ti = ti_next;                 // read one tile ahead
                 if (t + ncl < num_tiles) ti_next = decode_tile<C>(p, t + ncl, crank);
+                // the weight codes' tensor map: the expert's own (pointer-table form), or
+                // the kernel parameter over the contiguous [E][...] array
+                const CUtensorMap* bmap = p.wmaps ? p.wmaps + ti.expert : &tmB;
+                if (p.wmaps) tensormap_acquire(bmap);
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                     const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
                     if (__any_sync(0xffffffffu, !got)) {
@@ -517,14 +521,15 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                         uint8_t* bdst = st + C::A_RAW_BYTES;
                         const int kx = kb * C::B_ROW_BYTES;
                         if constexpr (C::EPI == Epi::SWIGLU_Q81) {
-                            // gate rows e*2F + n0 .. +BN/2 (lane l0+1), up rows e*2F + F + n0 .. +BN/2 (lane l0+2)
-                            const int base = ti.expert * 2 * p.F + ti.n0;
+                            // gate rows n0 .. +BN/2 (lane l0+1), up rows F + n0 .. +BN/2 (lane l0+2) of
+                            // the expert's [2F] rows (row e*2F + ... of the contiguous array)
+                            const int base = (p.wmaps ? 0 : ti.expert * 2 * p.F) + ti.n0;
                             if (lane == l0 + 1)
-                                tma_load_2d(bdst, &tmB, &full_t[s], kx, base);
+                                tma_load_2d(bdst, bmap, &full_t[s], kx, base);
                             else
-                                tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, &tmB, &full_t[s], kx, base + p.F);
+                                tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, bmap, &full_t[s], kx, base + p.F);
                         } else if (lane == l0 + 1) {
-                            tma_load_2d(bdst, &tmB, &full_t[s], kx, ti.expert * p.N + ti.n0);
+                            tma_load_2d(bdst, bmap, &full_t[s], kx, (p.wmaps ? 0 : ti.expert * p.N) + ti.n0);
                         }
                     }
                     __syncwarp();
@@ -828,14 +833,16 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         // W4 scales: 16-byte loads covering 4 K blocks, one chunk ahead (K % 256 == 0),
         // else one 4-byte load per K block.
         const bool vec_scales = (p.K % 256) == 0;
-        auto scale_row = [&](const TileInfo& tt, bool& in_range) -> long {
+        // this thread's weight row of a tile: its E4M3 scale row (K/16 bytes)
+        auto scale_row = [&](const TileInfo& tt, bool& in_range) -> const uint8_t* {
             if constexpr (C::EPI == Epi::SWIGLU_Q81) {
                 const int hr = (crow < C::BN / 2) ? (tt.n0 + crow) : (p.F + tt.n0 + crow - C::BN / 2);
                 in_range = true;
-                return (long)tt.expert * 2 * p.F + hr;
+                if (p.wscale_tab) return p.wscale_tab[tt.expert] + (long)hr * (p.K / 16);
+                return p.w_scale + ((long)tt.expert * 2 * p.F + hr) * (p.K / 16);
             } else {
                 in_range = (long)tt.n0 + crow < p.N;
-                return (long)tt.n0 + crow;
+                return p.w_scale + ((long)tt.n0 + crow) * (p.K / 16);
             }
         };
         // Scale prefetch two 4-K-block chunks ahead, through a cursor that walks
@@ -853,8 +860,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             uint4 v = make_uint4(0, 0, 0, 0);
             if (pf_t < num_tiles) {
                 bool in_range;
-                const long wrow = scale_row(pf_ti, in_range);
-                if (in_range) v = ldg_nc_v4(p.w_scale + wrow * (p.K / 16) + pf_ch * 16);
+                const uint8_t* srow = scale_row(pf_ti, in_range);
+                if (in_range) v = ldg_nc_v4(srow + pf_ch * 16);
                 if (++pf_ch == pf_ti.kb1 / 4) {
                     pf_t += ncl;
                     if (pf_t < num_tiles) {
@@ -928,8 +935,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     uint32_t sbytes = 0;
                     if constexpr (C::B == BMode::W4) {
                         bool in_range;
-                        const long wrow = scale_row(ti, in_range);
-                        sbytes = in_range ? __ldg(reinterpret_cast<const uint32_t*>(p.w_scale + wrow * (p.K / 16) + kb * 4))
+                        const uint8_t* srow = scale_row(ti, in_range);
+                        sbytes = in_range ? __ldg(reinterpret_cast<const uint32_t*>(srow + kb * 4))
                                           : 0u;
                     }
                     if (!convert_step(sbytes)) ok = false;

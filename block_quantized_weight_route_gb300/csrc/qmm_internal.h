@@ -23,6 +23,11 @@ struct GemmParams {
     const float* blk_scale; // FP8: [N/128][K/128] block scales
     const float* dH32;      // down: fp32 d of H per 128-row tile entry, [entry][K/32][128]
     const __half* dW;       // down: IQ4_NL block scales, [E][N][K/32]
+    // per-expert weights (pointer-table form of the expert stage; null: the
+    // contiguous [E][...] arrays through tmB / tmA, w_scale and dW above)
+    const CUtensorMap* wmaps;          // [E] tensor maps of each expert's weight codes
+    const uint8_t* const* wscale_tab;  // gate/up: [E] E4M3 scale matrices [2F][D/16]
+    const __half* const* dW_tab;       // down: [E] IQ4_NL scale matrices [D][F/32]
     const int32_t* src;     // down with the combine fused: token of each routed row [P]
     const float* wrow;      // down with the combine fused: routing weight of each routed row [P]
     void* Y;                // output (fp32 or bf16)

@@ -194,6 +194,35 @@ qmm_status moe_expert_stage_w4_iq4_ex(const uint16_t *X, const float *logits, in
                                       const uint8_t *Wd_idx, const uint16_t *Wd_s, float *Y, void *ws, size_t ws_bytes,
                                       unsigned flags, cudaStream_t stream);
 
+/*
+ * Per-expert pointer tables: the expert stage over weights held in one
+ * allocation per expert, as the routed-MoE grouped GEMMs of "perf: strix-hip
+ * BF16 GEMMs via hipBLASLt" take them (per-expert pointer tables), with no
+ * copy of the weights.
+ * moe_expert_table_size(E): bytes of the table for E experts (0 if E is not in 1..512).
+ * moe_expert_table_build: Wgu_c, Wgu_s, Wd_idx, Wd_s are HOST arrays of E DEVICE
+ *   pointers, expert e's matrices in the layouts of moe_expert_stage_w4_iq4
+ *   without the leading [E]: Wgu_c[e] [2F][D/2], Wgu_s[e] [2F][D/16],
+ *   Wd_idx[e] [D][F/2], Wd_s[e] [D][F/32] fp16; each 16-byte aligned.  Writes
+ *   into the caller's device buffer `table` (256-byte aligned, at least
+ *   moe_expert_table_size(E) bytes) one TMA tensor map per expert for its
+ *   gate/up codes and one for its down indices, and the scale pointers; this is
+ *   a set-up call: it copies from the host and synchronises `stream`.  The
+ *   table stays valid as long as the experts' buffers do.
+ *   Shapes: 1 <= E <= 512, D % 128 == 0, F % 128 == 0, F <= 1024.
+ * moe_expert_stage_w4_iq4_table: moe_expert_stage_w4_iq4_ex with each expert's
+ *   weights taken from the table (same results, bit for bit with
+ *   QMM_STAGE_SLOTS, as the contiguous call on the same values); the kernels
+ *   read the expert's tensor map from the table when a tile of that expert starts.
+ */
+size_t moe_expert_table_size(int E);
+qmm_status moe_expert_table_build(int D, int F, int E, const uint8_t *const *Wgu_c, const uint8_t *const *Wgu_s,
+                                  const uint8_t *const *Wd_idx, const uint16_t *const *Wd_s, void *table,
+                                  size_t table_size, cudaStream_t stream);
+qmm_status moe_expert_stage_w4_iq4_table(const uint16_t *X, const float *logits, int T, int D, int F, int E, int k,
+                                         const float *gu_scale2, const void *table, float *Y, void *ws,
+                                         size_t ws_bytes, unsigned flags, cudaStream_t stream);
+
 /* Byte offsets, inside the expert-stage workspace, of its regions (for callers
  * that inspect intermediate results).  Writes QMM_WS_FIELDS offsets in this order:
  *   0 ids [T*k] i32     1 w [T*k] f32       2 counts [E] i32    3 offsets [E+1] i32
