@@ -233,8 +233,8 @@ qmm_status qmm_w4a16_ws(const uint16_t* X, int M, int K, int N, const uint8_t* W
     if (!aligned16(X) || !aligned16(Wc) || !aligned16(Ws) || !aligned16(Y))
         return fail(QMM_ERR_INVALID_ARG, "qmm_w4a16: buffers must be 16-byte aligned");
     if (ydt != QMM_F32 && ydt != QMM_BF16) return fail(QMM_ERR_INVALID_ARG, "qmm_w4a16: bad output type");
-    if (M < 1 || K < 64 || N < 32 || K % 64 || N % 32)
-        return fail(QMM_ERR_UNSUPPORTED_SHAPE, "qmm_w4a16: need M >= 1, K %% 64 == 0, N %% 32 == 0 (M=%d K=%d N=%d)",
+    if (M < 1 || K < 32 || N < 32 || K % 32 || N % 32)
+        return fail(QMM_ERR_UNSUPPORTED_SHAPE, "qmm_w4a16: need M >= 1, K %% 32 == 0, N %% 32 == 0 (M=%d K=%d N=%d)",
                     M, K, N);
     GemmParams p{};
     qmm_status st = split_workspace("qmm_w4a16", ws, ws_bytes, &p);

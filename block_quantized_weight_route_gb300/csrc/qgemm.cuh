@@ -149,7 +149,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int g, int 
         // index of the first 128-row routing entry the tile covers (two per tile when MSUB == 2)
         ti.entry = (C::MSUB == 2) ? e4.w : entry;
         ti.kb0 = 0;
-        ti.kb1 = p.K / C::BK;
+        ti.kb1 = (p.K + C::BK - 1) / C::BK;
         ti.split = -1;
         ti.s = 0;
     } else {
@@ -167,7 +167,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int g, int 
         ti.rows = min(C::BM, p.M - ti.row0);
         ti.n0 = nt * p.n_step;
         ti.entry = mt;
-        const int kblocks = p.K / C::BK;
+        const int kblocks = (p.K + C::BK - 1) / C::BK;   // K % 64 == 32: a last half block
         if (split >= 0) {
             const int nch = kblocks / 4;
             ti.kb0 = 4 * (s * nch / p.split_S);
@@ -936,8 +936,20 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     if constexpr (C::B == BMode::W4) {
                         bool in_range;
                         const uint8_t* srow = scale_row(ti, in_range);
-                        sbytes = in_range ? __ldg(reinterpret_cast<const uint32_t*>(srow + kb * 4))
-                                          : 0u;
+                        if (!in_range) {
+                            sbytes = 0u;
+                        } else if ((p.K & 63) == 0) {
+                            sbytes = __ldg(reinterpret_cast<const uint32_t*>(srow + kb * 4));
+                        } else {
+                            // K % 64 == 32: scale rows are not 4-byte aligned, and the last K
+                            // block has two scale bytes (its other 32 K are zero-filled codes,
+                            // given scale 0 so that no NaN scale byte of the next row enters)
+                            const int nsc = p.K / 16;
+                            sbytes = 0u;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                if (kb * 4 + i < nsc) sbytes |= (uint32_t)__ldg(srow + kb * 4 + i) << (8 * i);
+                        }
                     }
                     if (!convert_step(sbytes)) ok = false;
                 }
@@ -1004,7 +1016,7 @@ cudaError_t launch_qgemm(const CUtensorMap& tmA, const CUtensorMap& tmB, GemmPar
         const int kblocks = p.K / C::BK;
         const int full = items / clusters * clusters, rem = items - full;
         p.split_from = items;
-        if (p.split_part && kblocks % 4 == 0 && rem > 0 && 2 * rem <= clusters) {
+        if (p.split_part && p.K % 256 == 0 && rem > 0 && 2 * rem <= clusters) {
             int S = clusters / rem;
             if (S > 8) S = 8;
             if (S > kblocks / 8) S = kblocks / 8;

@@ -65,7 +65,7 @@ qmm_status qmm_check_status(cudaStream_t stream);
  *   Wc  [N][K/2]  packed e2m1 codes (bit 3 sign, bits 0-2 index {0,.5,1,1.5,2,3,4,6})
  *   Ws  [N][K/16] OCP E4M3 scale bytes
  *   Y   [M][N]    fp32 (ydt = QMM_F32) or bf16 rounded to nearest even (QMM_BF16)
- * fp32 accumulation.  Shapes: M >= 1, K % 64 == 0, N % 32 == 0.
+ * fp32 accumulation.  Shapes: M >= 1, K % 32 == 0, N % 32 == 0.
  */
 qmm_status qmm_w4a16(const uint16_t *X, int M, int K, int N, const uint8_t *Wc, const uint8_t *Ws, float scale2,
                      void *Y, qmm_dtype ydt, cudaStream_t stream);

@@ -53,8 +53,9 @@ def test_argument_checks_return_before_any_device_work(L):
     assert L.qmm_w4a16(None, 64, 512, 512, None, None, 1.0, None, 0, None) == 1
     # misaligned
     assert L.qmm_w4a16(P(16), 64, 512, 512, P(17), P(32), 1.0, P(48), 0, None) == 1
-    # shapes: K not a multiple of 64, N not a multiple of 32
+    # shapes: K not a multiple of 32, N not a multiple of 32
     assert L.qmm_w4a16(P(256), 64, 100, 512, P(256), P(256), 1.0, P(256), 0, None) == 2
+    assert L.qmm_w4a16(P(256), 64, 16, 512, P(256), P(256), 1.0, P(256), 0, None) == 2
     assert L.qmm_w4a16(P(256), 64, 512, 500, P(256), P(256), 1.0, P(256), 0, None) == 2
     L.qmm_fp8_blk128.restype = ctypes.c_int
     L.qmm_fp8_blk128.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P]

@@ -114,7 +114,48 @@ def test_w4a16_k_split_integer_inputs_are_exact(qlib):
     assert np.array_equal(Y.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("M,K,N", [(64, 512, 512), (1, 64, 32), (129, 192, 96), (300, 1024, 544), (40, 4096, 256)])
+def test_w4a16_half_last_k_block_integer_inputs_are_exact(qlib):
+    """K % 64 == 32: the last 64-wide K block is half outside the operands (zero-filled
+    by the copies, its scale bytes masked); with unit scales and small-integer X the
+    result is an exact integer matmul."""
+    rng = np.random.default_rng(5)
+    M, K, N = 150, 2080, 288
+    Xi = rng.integers(-20, 21, size=(M, K)).astype(np.float32)
+    X = torch.from_numpy(Xi).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    Wc = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    Ws = np.full((N, K // 16), 0x38, np.uint8)
+    Y = qlib.qmm_w4a16(bf16_dev(X), dev(Wc), dev(Ws), 1.0).cpu().numpy()
+    assert np.array_equal(Y.astype(np.float64), oracle.w4a16(X, Wc, Ws, 1.0))
+
+
+def test_w4a16_wide_tiles_k_split_integer_inputs_are_exact(qlib):
+    """M=2048, N=20480: 256 x 256 tiles are chosen and their last wave (the column
+    tiles from 19456 on) is split along K over several CTAs with fp32 partials in
+    the workspace.  Unit scales and small-integer X make every partial exact, so the
+    split result equals the oracle and the unsplit call exactly."""
+    rng = np.random.default_rng(6)
+    M, K, N = 2048, 1024, 20480
+    Xi = rng.integers(-20, 21, size=(M, K)).astype(np.float32)
+    X = torch.from_numpy(Xi).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    Wc = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    Ws = np.full((N, K // 16), 0x38, np.uint8)
+    Xd, Wcd, Wsd = bf16_dev(X), dev(Wc), dev(Ws)
+    assert qlib.qmm_dense_workspace_size(M, K, N) > 0
+    Y_split = qlib.qmm_w4a16(Xd, Wcd, Wsd, 1.0)
+    Y_plain = torch.empty_like(Y_split)
+    st = qlib.lib().qmm_w4a16(qlib._ptr(Xd), M, K, N, qlib._ptr(Wcd), qlib._ptr(Wsd), 1.0, qlib._ptr(Y_plain), 0,
+                              qlib._stream(Xd.device))
+    assert st == 0
+    qlib.qmm_check_status()
+    assert torch.equal(Y_split, Y_plain)
+    rows = np.concatenate([np.arange(0, M, 16), [255, 256, 2047]])
+    cols = np.concatenate([np.arange(19456, N), np.arange(0, 19456, 311)])
+    ref = oracle.w4a16(X, Wc, Ws, 1.0, rows=rows, cols=cols)
+    assert np.array_equal(Y_split.cpu().numpy().astype(np.float64)[np.ix_(rows, cols)], ref)
+
+
+@pytest.mark.parametrize("M,K,N", [(64, 512, 512), (1, 64, 32), (129, 192, 96), (300, 1024, 544), (40, 4096, 256),
+                                   (64, 96, 128), (130, 32, 64), (257, 5152, 96)])
 def test_w4a16_matches_oracle(qlib, M, K, N):
     g = wl.gen_w4a16(M, K, N, 1.0 / 64, seed=M + K + N)
     Y = qlib.qmm_w4a16(bf16_dev(g["X"]), dev(g["Wc"]), dev(g["Ws"]), float(g["scale2"])).cpu().numpy()
