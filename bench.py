@@ -39,11 +39,38 @@ GEMM_W4 = "w4a16_m2048_k5120_n17408"
 GEMM_FP8 = "fp8blk128_m2048_k5120_n5120"
 GEMM_ROUTER = "w4a16_router_m2048_k2560_n512"
 METRIC = "MoE expert-stage prefill tokens/s; quant-GEMM TFLOP/s vs GB300 tensor peak"
-# DRAM bytes (read + write) per launch of each stage kernel on the 5268-token
-# workload, from one ncu capture of the kernel as it stands (profiles/); None
-# once a kernel changes after its capture.
-DRAM_TRAFFIC = {"down": 182.84e6 + 289.72e6, "gate_up": 472.55e6 + 61.48e6}
+GEMM_TINY = "w4a16_m64_k512_n512"
+STAGE_LARGE = "moe_t21504_d2560_f1024_e256_k8_zipf"
+# the dense Q8_0 x q8_1 projection: a latent layer's D projection at M = 2048
+# (41.3M multiply-adds per row: K = 5120, N = 8064)
+Q8_SHAPE = (2048, 5120, 8064)
+# DRAM bytes (read + write) per launch of a stage kernel on the 5268-token
+# workload, from one ncu capture (profiles/), with the SHA-256 of the kernel's
+# sources at the time of the capture: the figure is reported only while the
+# sources are unchanged (else null).
+DRAM_TRAFFIC = {}
+KERNEL_SOURCES = {
+    "down": ["csrc/down_iq4.cuh", "csrc/gemm_down.cu", "csrc/qgemm.cuh", "csrc/ptx.cuh"],
+    "gate_up": ["csrc/qgemm.cuh", "csrc/gemm_w4.cu", "csrc/ptx.cuh"],
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def sources_sha(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES.get(kernel, []):
+        with open(os.path.join(ROOT, "block_quantized_weight_route_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str):
+    """The captured per-launch DRAM bytes of `kernel`, or None if its sources changed since."""
+    t = DRAM_TRAFFIC.get(kernel)
+    if not t or t["sources_sha"] != sources_sha(kernel):
+        return None
+    return t["bytes"]
 
 
 def load_peaks():
@@ -204,23 +231,77 @@ def run_reference(args, world, rank):
 
 # --------------------------------------------------------------------------- GPU arm
 
-def stage_units(w):
+def stage_work(w):
+    """Algorithmic work of one expert-stage call: the two grouped GEMMs' flops, the
+    down product's fold (one multiply and one FMA per output and 32-K block, on
+    the FP32 lanes), the bytes the stage must move (every expert's weights, X, the
+    logits, the q8_1 H written and read once, Y), and per-phase bytes of the
+    data-movement kernels."""
     P = w.T * w.k
     flops = {"gate_up": 2.0 * P * w.D * 2 * w.F, "down": 2.0 * P * w.F * w.D}
-    # the down product's fp32 fold: per output and 32-K block one multiply (I * d_H)
-    # and one FMA (* d_W + y), 3 flops, on the CUDA cores
-    fold_flops = 3.0 * P * w.D * (w.F // 32)
-    bytes_ = {
-        "route": w.T * w.E * 4 + 4 * P * 4,                          # logits in; ids, w, src, row out
+    fold_ops = 2.0 * P * w.D * (w.F // 32)
+    weights = w.E * (2 * w.F * w.D // 2 + 2 * w.F * w.D // 16 + w.D * w.F // 2 + w.D * (w.F // 32) * 2 + 4)
+    h_bytes = P * w.F + P * (w.F // 32) * 4
+    total = weights + w.T * w.D * 2 + w.T * w.E * 4 + 2 * h_bytes + w.T * w.D * 4
+    phase_bytes = {
+        "route": w.T * w.E * 4 + 4 * P * 4 + P * 4 + w.T * w.D * 4,   # logits in; ids, w, src, row, wrow out; Y zeroed
         "gather": w.T * w.D * 2 + P * w.D * 2,                       # X read once, X_perm written
-        "combine": P * w.D * 4 + w.T * w.D * 4 + P * 8,              # Yslot read, Y written, row/w
+        "combine": P * w.D * 4 + w.T * w.D * 4 + P * 8,              # (per-slot form) Yslot read, Y written
     }
-    return flops, bytes_, fold_flops
+    return flops, fold_ops, total, phase_bytes
 
 
-def fp32_peak_tflops(sm_mhz: float, sms: int = 152) -> float:
-    """FP32 FMA peak: 128 lanes per SM, 2 flops per FMA, at the sampled SM clock."""
-    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+def fp32_lane_ops_peak(sm_mhz: float, sms: int = 152) -> float:
+    """FP32 lane operations per second (one FMA or multiply per lane per clock):
+    128 lanes per SM at the sampled SM clock, in T/s."""
+    return sms * 128 * sm_mhz * 1e6 / 1e12
+
+
+def stage_roofline(w, ms: float, peaks: dict, sm_mhz: float, sms: int) -> dict:
+    """Roofline time of the stage = max(tensor flops / bf16 peak + fold ops / FP32
+    lane peak, bytes / HBM bandwidth); fraction = roofline time / measured time."""
+    flops, fold_ops, total, _ = stage_work(w)
+    t_tensor = sum(flops.values()) / (peaks["bf16_tflops"] * 1e12) * 1e3
+    t_fold = fold_ops / (fp32_lane_ops_peak(sm_mhz, sms) * 1e12) * 1e3
+    t_hbm = total / (peaks["hbm_gbs"] * 1e9) * 1e3
+    roof = max(t_tensor + t_fold, t_hbm)
+    return {"measured_ms": ms, "roofline_ms": roof, "frac": roof / ms, "tensor_ms": t_tensor, "fold_ms": t_fold,
+            "hbm_ms": t_hbm, "flops": sum(flops.values()), "fold_ops": fold_ops, "bytes": total,
+            "peaks": "bf16 burst and HBM copy of MEASURED_PEAKS.json; FP32 lanes 152 x 128 x sampled SM clock"}
+
+
+def phase_rooflines(w, phases: dict, peaks: dict, peak_src: str, sm_mhz: float, sms: int) -> dict:
+    flops, fold_ops, _, pbytes = stage_work(w)
+    pk_t = peaks["bf16_tflops"]
+    out = {}
+    for name, ms in phases.items():
+        if name in flops:
+            ach = flops[name] / (ms * 1e-3) / 1e12
+            r = {"ms": ms, "bound": "tensor", "achieved": ach, "peak": pk_t, "unit": "TFLOP/s", "frac": ach / pk_t,
+                 "peak_source": f"{peak_src} (burst bf16)"}
+            if name == "down":
+                # the exact integer block dots run on the f16 tensor pipe; the fp32 fold
+                # of every 32-K block's dot runs on the FP32 lanes beside it
+                pk_f = fp32_lane_ops_peak(sm_mhz, sms)
+                fa = fold_ops / (ms * 1e-3) / 1e12
+                r["fold"] = {"ops": fold_ops, "achieved": fa, "peak": pk_f, "unit": "T lane-ops/s", "frac": fa / pk_f}
+            out[name] = r
+        elif ms > 0.005:
+            ach = pbytes[name] / (ms * 1e-3) / 1e9
+            out[name] = {"ms": ms, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"]}
+        else:
+            out[name] = {"ms": ms, "note": "empty: the combine runs inside the down product"}
+    return out
+
+
+def expert_histogram(q, ws, w) -> dict:
+    """Rows per expert of the last stage call (the workspace's counts region)."""
+    import torch
+    lay = q.moe_expert_stage_workspace_layout(w.T, w.D, w.F, w.E, w.k)
+    c = q.workspace_view(ws, lay, "counts", torch.int32, (w.E,)).cpu().numpy()
+    return {"max": int(c.max()), "mean": float(c.mean()), "min": int(c.min()), "max_over_mean": float(c.max() / c.mean()),
+            "experts_under_128_rows": int((c < 128).sum()), "empty_experts": int((c == 0).sum())}
 
 
 def run_gpu(args, world, rank, local):
@@ -277,35 +358,35 @@ def run_gpu(args, world, rank, local):
     value = w.T * world * args.steps / total_s
 
     phases = {k: statistics.mean(p[k] for p in phase_ms) for k in q.PROFILE_PHASES}
-    flops, bytes_, fold_flops = stage_units(w)
-    pk_t = peaks["bf16_tflops_sustained"]
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    pk_alu = fp32_peak_tflops(clk.get("sm_mhz") or 2070.0, sms)
-    phase_roof = {}
-    for name, ms in phases.items():
-        if name == "down":
-            # bound by the fp32 fold on the CUDA cores (its exact integer block dots
-            # run on the f16 tensor pipe, reported beside it)
-            ach = fold_flops / (ms * 1e-3) / 1e12
-            tens = flops[name] / (ms * 1e-3) / 1e12
-            phase_roof[name] = {"ms": ms, "bound": "alu", "achieved": ach, "peak": pk_alu, "unit": "TFLOP/s",
-                                "frac": ach / pk_alu, "peak_source": "152 SMs x 128 FP32 lanes x 2 x sampled SM clock",
-                                "tensor_view": {"achieved": tens, "peak": pk_t, "frac": tens / pk_t}}
-        elif name in flops:
-            ach = flops[name] / (ms * 1e-3) / 1e12
-            phase_roof[name] = {"ms": ms, "bound": "tensor", "achieved": ach, "peak": pk_t, "unit": "TFLOP/s",
-                                "frac": ach / pk_t}
-        else:
-            ach = bytes_[name] / (ms * 1e-3) / 1e9
-            phase_roof[name] = {"ms": ms, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"]}
-    dom = max(phases, key=phases.get)
-    roof = dict(phase_roof[dom])
-    roof.pop("ms")
+    sm_mhz = clk.get("sm_mhz") or 2070.0
+    phase_roof = phase_rooflines(w, phases, peaks, peak_src, sm_mhz, sms)
+    # the dominant kernel: on the tensor pipe against the burst bf16 peak (a kernel
+    # of a ~1 ms step), the down product's fold beside it
+    dom = max((n for n in phases if "bound" in phase_roof[n]), key=phases.get)
+    roof = {k: v for k, v in phase_roof[dom].items() if k != "ms"}
     roof["kernel"] = dom
-    roof["traffic"] = DRAM_TRAFFIC.get(dom)
-    if roof["bound"] != "alu":
-        roof["peak_source"] = f"{peak_src} ({'sustained' if roof['bound'] == 'tensor' else 'copy'})"
+    roof["traffic"] = dram_traffic(dom)
+    roof["traffic_note"] = ("DRAM read + write bytes per launch from the ncu capture of these sources"
+                            if roof["traffic"] is not None else "no ncu capture of the kernel's current sources")
+    stage_roof = stage_roofline(w, 1e3 * total_s / (args.steps * world), peaks, sm_mhz, sms)
+    hist = expert_histogram(q, ws, w)
+
+    # the per-slot form of the stage (QMM_STAGE_SLOTS: separate j-ordered combine,
+    # reproducible bit for bit), timed the same way as context
+    for _ in range(2):
+        q.moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, s2, Wd_idx, Wd_s, w.k, ws=ws, Y=Y, slots=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nsl = max(3, min(20, args.steps))
+    a.record(stream)
+    for _ in range(nsl):
+        q.moe_expert_stage_w4_iq4(X, logits, Wgu_c, Wgu_s, s2, Wd_idx, Wd_s, w.k, ws=ws, Y=Y, slots=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    slots_ms = a.elapsed_time(b) / nsl
+    step()                         # leave the default form's Y for the end-to-end check
+    torch.cuda.synchronize()
 
     # ---- end to end through the public API: every step copies its own inputs in
     # from pinned host memory and its Y back out.  Double-buffered the way a
@@ -363,7 +444,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.empty_cache()
 
     quant = {} if args.no_gemm else bench_dense(q, torch, device, args, peaks, peak_src)
-    other = {} if args.no_gemm else bench_other_stage(q, torch, device, args)
+    other = {} if args.no_gemm else bench_other_stage(q, torch, device, args, peaks, peak_src, sms)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -374,8 +455,10 @@ def run_gpu(args, world, rank, local):
                    "l2": "inputs larger than L2 (340 MB of expert weights read per step)",
                    "timing": "CUDA events per step; phase events between the stage's kernels inside the timed steps "
                              "(the e2e loop records none)"},
-        "roofline": roof, "phases": phase_roof, "quant_gemm": quant, "other_stage": other, "e2e": e2e, "clocks": clk,
-        "gpu_launches": 8 * args.steps, "wall_s": wall,
+        "roofline": roof, "stage_roofline": stage_roof, "phases": phase_roof, "expert_counts": hist,
+        "stage_slots_ms": slots_ms, "quant_gemm": quant, "other_stage": other, "e2e": e2e, "clocks": clk,
+        # per step: top-k, histogram, scan, permutation, gather, gate/up, down (combine fused)
+        "gpu_launches": 7 * args.steps, "wall_s": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(g, w.k)
@@ -383,12 +466,10 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(line))
 
 
-STAGE_LARGE = "moe_t21504_d2560_f1024_e256_k8_zipf"
-
-
-def bench_other_stage(q, torch, device, args):
-    """The larger stage configuration (skewed expert popularity), timed the same
-    way as the headline stage but for a few steps: context, not the metric."""
+def bench_other_stage(q, torch, device, args, peaks, peak_src, sms):
+    """The larger stage configuration (T=21504, D=2560, F=1024, E=256, Zipf(1.1)
+    expert popularity: load imbalance and tail experts), timed like the headline
+    stage: CUDA events per step, phase events, roofline, per-expert counts."""
     w = wl.WORKLOADS[STAGE_LARGE]
     g = wl.generate(w)
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
@@ -400,17 +481,27 @@ def bench_other_stage(q, torch, device, args):
     for _ in range(3):
         q.moe_expert_stage_w4_iq4(X, L, *args_, w.k, ws=ws, Y=Y)
     torch.cuda.synchronize()
-    n = max(3, min(20, args.steps // 10))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(n):
+    n = max(3, min(20, args.steps))
+    q.qmm_profile_enable(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    for i in range(n):
+        ev[i][0].record(stream)
         q.moe_expert_stage_w4_iq4(X, L, *args_, w.k, ws=ws, Y=Y)
-    b.record(stream)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
+    ph = [q.qmm_profile_read_call(i) for i in range(n)]
+    q.qmm_profile_enable(False)
     q.qmm_check_status()
-    ms = a.elapsed_time(b) / n
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    phases = {k: statistics.mean(p[k] for p in ph) for k in q.PROFILE_PHASES}
+    sm_mhz = clk.get("sm_mhz") or 2070.0
     out = {STAGE_LARGE: {"ms": ms, "tokens_per_s": w.T / (ms * 1e-3), "tflops": w.flops() / (ms * 1e-3) / 1e12,
-                         "steps": n}}
+                         "steps": n, "stage_roofline": stage_roofline(w, ms, peaks, sm_mhz, sms),
+                         "phases": phase_rooflines(w, phases, peaks, peak_src, sm_mhz, sms),
+                         "expert_counts": expert_histogram(q, ws, w), "clocks": clk}}
     del ws, Y, X, L, args_
     torch.cuda.empty_cache()
     return out
@@ -421,7 +512,7 @@ def bench_dense(q, torch, device, args, peaks, peak_src):
     out = {}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
-    for name in (GEMM_W4, GEMM_FP8, GEMM_ROUTER):
+    for name in (GEMM_TINY, GEMM_W4, GEMM_FP8, GEMM_ROUTER):
         w = wl.WORKLOADS[name]
         g = wl.generate(w)
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
@@ -455,8 +546,40 @@ def bench_dense(q, torch, device, args, peaks, peak_src):
         tfl = w.flops() / (ms * 1e-3) / 1e12
         out[name] = {"ms": ms, "tflops": tfl, "peak": peaks["bf16_tflops"], "frac": tfl / peaks["bf16_tflops"],
                      "peak_source": f"{peak_src} (burst bf16)", "l2": "flushed before each launch"}
+        if name == GEMM_TINY:
+            # latency-bound: also the bytes it must move (X, codes, scales, Y) against HBM
+            nbytes = w.M * w.K * 2 + w.N * w.K // 2 + w.N * w.K // 16 + w.M * w.N * 4
+            out[name].update({"us": ms * 1e3, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                              "bound": "latency (reported, not targeted)"})
         del X, Y, dws
         torch.cuda.empty_cache()
+    # the dense Q8_0 x q8_1 projection re-quantised to q8_1 (a latent layer's D)
+    M, K, N = Q8_SHAPE
+    g = wl.gen_q8_0_q8_1(M, K, N, seed=6)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+    Xq, Xd, Wq, Wd = d(g["Xq"]), d(g["Xd"].view(np.int16)), d(g["Wq"]), d(g["Wd"].view(np.int16))
+    qws = torch.empty(q.qmm_q8_0_q8_1_workspace_size(M, K, N), dtype=torch.uint8, device=device)
+    for _ in range(max(3, args.warmup)):
+        q.qmm_q8_0_q8_1(Xq, Xd, Wq, Wd, ws=qws)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        q.qmm_q8_0_q8_1(Xq, Xd, Wq, Wd, ws=qws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    q.qmm_check_status()
+    ms = statistics.mean(times)
+    tfl = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    out[f"q8_0_q8_1_m{M}_k{K}_n{N}"] = {"ms": ms, "tflops": tfl, "peak": peaks["bf16_tflops"],
+                                          "frac": tfl / peaks["bf16_tflops"], "peak_source": f"{peak_src} (burst bf16)",
+                                          "l2": "flushed before each launch",
+                                          "note": "exact int8 block dots on the f16 tensor path + fp32 fold"}
+    del Xq, Xd, Wq, Wd, qws
+    torch.cuda.empty_cache()
     return out
 
 
@@ -468,8 +591,8 @@ def run_case(args):
     q.build_library()
     dev = torch.device("cuda", 0)
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
-    if args.case == "stage":
-        w = wl.WORKLOADS[STAGE]
+    if args.case in ("stage", "stage_large"):
+        w = wl.WORKLOADS[STAGE if args.case == "stage" else STAGE_LARGE]
         g = wl.generate(w)
         X, L = d(g["X"].view(np.int16)), d(g["logits"])
         args_ = (d(g["Wgu_c"]), d(g["Wgu_s"]), d(g["gu_scale2"]), d(g["Wd_idx"]), d(g["Wd_s"].view(np.int16)))
@@ -480,6 +603,11 @@ def run_case(args):
         g = wl.generate(w)
         X, Wc, Ws = d(g["X"].view(np.int16)), d(g["Wc"]), d(g["Ws"])
         call = lambda: q.qmm_w4a16(X, Wc, Ws, float(g["scale2"]), out_dtype=torch.bfloat16)  # noqa: E731
+    elif args.case == "q8":
+        M, K, N = Q8_SHAPE
+        g = wl.gen_q8_0_q8_1(M, K, N, seed=6)
+        Xq, Xd, Wq, Wd = d(g["Xq"]), d(g["Xd"].view(np.int16)), d(g["Wq"]), d(g["Wd"].view(np.int16))
+        call = lambda: q.qmm_q8_0_q8_1(Xq, Xd, Wq, Wd)  # noqa: E731
     else:
         w = wl.WORKLOADS[GEMM_FP8]
         g = wl.generate(w)
@@ -504,7 +632,7 @@ def main():
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--no-gemm", action="store_true", help="skip the dense GEMM measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["stage", "w4a16", "fp8"], default=None,
+    ap.add_argument("--case", choices=["stage", "stage_large", "w4a16", "fp8", "q8"], default=None,
                     help="run one op only (for profiler captures); prints no JSON line")
     ap.add_argument("--warmup-case", type=int, default=1, help="untimed runs before --steps in --case mode")
     args = ap.parse_args()
