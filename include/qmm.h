@@ -22,6 +22,10 @@
  *    returns QMM_ERR_TIMEOUT for it.
  *  - The library runs only on compute capability 10.3 (GB300); any other device
  *    gives QMM_ERR_UNSUPPORTED_DEVICE.  There is no fallback path.
+ *  - Device addresses the library looks up once per device (its device error
+ *    word, the fixed scratch of moe_route_permute_noalloc) are kept for the
+ *    life of the process: they do not survive cudaDeviceReset, after which the
+ *    library must not be called again in that process.
  */
 #ifndef QMM_H
 #define QMM_H

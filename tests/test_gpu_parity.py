@@ -61,7 +61,8 @@ def check_bf16_output(got, ref, tol=GEMM_TOL):
     e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
     assert np.all(np.abs(got - ref) <= tol * np.max(a) + np.exp2(e - 8))
     rounded = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
-    assert np.mean(got == rounded) >= 0.99
+    # observed on GB300: >= 99.86% equal (the K = 5120 sample; >= 99.99% at K <= 2048)
+    assert np.mean(got == rounded) >= 0.995
 
 
 # ---------------------------------------------------------------- dense W4A16
@@ -274,14 +275,28 @@ def test_fp8_blk128_full_size_sampled(qlib):
 
 # ---------------------------------------------------------------- routing
 
+# Routing weights: the GPU computes w_j = e_j / sum_i e_i in fp32 with e_i =
+# expf(l_i - l_max) (within 2 ulp each), a sum of at most 16 terms and one
+# division, the oracle in fp64 rounded once: at most ~2 + 15 * 1/2 + 1/2 ulps of
+# accumulated rounding, so 16 ulps of the oracle's fp32 value bound it (observed
+# on GB300: at most 8 ulps, at T = 21504).
+ROUTE_W_ULPS = 16
+
+
+def max_ulps(got, ref):
+    ref32 = np.asarray(ref, np.float32)
+    return float(np.max(np.abs(np.asarray(got, np.float64) - ref32.astype(np.float64)) /
+                        np.spacing(np.abs(ref32)).astype(np.float64)))
+
+
 def check_route(qlib, logits, k):
     r = oracle.route(logits, k)
     out = qlib.moe_route_permute(dev(logits), k)
     for key in ("ids", "counts", "offsets", "src", "row"):
         got = out[key].cpu().numpy().reshape(r[key].shape)
         assert np.array_equal(got, r[key]), key
-    w = out["w"].cpu().numpy()
-    assert np.max(np.abs(w - r["w"])) <= 2 ** -21
+    w = out["w"].cpu().numpy().reshape(r["w"].shape)
+    assert max_ulps(w, r["w"]) <= ROUTE_W_ULPS
     return r
 
 
@@ -380,16 +395,30 @@ def test_expert_stage_k_equals_e(qlib):
     check_stage(qlib, g, 4)
 
 
-def test_expert_stage_t5268_sampled(qlib):
+def every_expert_tokens(logits, k):
+    """Tokens whose routed rows include the first and the last row of every
+    expert's group (so every expert, the Zipf tail included, and both ends of
+    every group are checked), plus the first and last token."""
+    r = oracle.route(logits, k)
+    toks = {0, logits.shape[0] - 1}
+    for e in range(logits.shape[1]):
+        o0, o1 = int(r["offsets"][e]), int(r["offsets"][e + 1])
+        if o1 > o0:
+            toks.add(int(r["src"][o0]))
+            toks.add(int(r["src"][o1 - 1]))
+    return np.array(sorted(toks), np.int32)
+
+
+def test_expert_stage_t5268_every_expert(qlib):
     w = wl.WORKLOADS["moe_t5268_d2048_f768_e128_k8"]
     g = wl.generate(w)
-    check_stage(qlib, g, w.k, tokens=np.array([0, 1, 77, 2600, 5266, 5267]))
+    check_stage(qlib, g, w.k, tokens=every_expert_tokens(g["logits"], w.k))
 
 
-def test_expert_stage_t21504_zipf_sampled(qlib):
+def test_expert_stage_t21504_zipf_every_expert(qlib):
     w = wl.WORKLOADS["moe_t21504_d2560_f1024_e256_k8_zipf"]
     g = wl.generate(w)
-    check_stage(qlib, g, w.k, tokens=np.array([0, 9999, 21503]))
+    check_stage(qlib, g, w.k, tokens=every_expert_tokens(g["logits"], w.k))
 
 
 def test_expert_stage_at_the_shape_limits(qlib):
