@@ -40,6 +40,9 @@ namespace qmm {
 #ifndef QMM_DOWN_CSTAGES
 #define QMM_DOWN_CSTAGES 2
 #endif
+#ifndef QMM_DOWN_PAIR
+#define QMM_DOWN_PAIR 1
+#endif
 template <int EPI_WARPS_, int CONV_WARPS_, int TSTAGES_>
 struct DownCfgT {
     static constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16, GROUP_K = 32;
@@ -50,7 +53,14 @@ struct DownCfgT {
     static constexpr int CW = (EPI_WARPS_ == 16 && CONV_WARPS_ == 4) ? 16 : 32;
     static constexpr int NCH = CPW / CW;
     static constexpr int W2 = EPI_BASE + EPI_WARPS;           // first warp after the epilogue (sub-partition 0)
-    static constexpr int THREADS = 32 * (CONV_WARPS == 2 ? W2 : W2 + 3);
+    // 8 epilogue warps and 4 converters: 16 warps launched at 128 registers a
+    // thread, the two epilogue warpgroups raised to 168 (their running sums and
+    // two 32-column loads) and the other two lowered to 88 - the shares add up
+    // to exactly the launch's 16 x 128
+    static constexpr bool REG_SPLIT = (EPI_WARPS_ == 8 && CONV_WARPS_ == 4);
+    static constexpr int REGS_LAUNCH = 128, REGS_EPI = 168, REGS_OTHER = 88;
+    static_assert(!REG_SPLIT || 8 * REGS_EPI + 8 * REGS_OTHER == 16 * REGS_LAUNCH, "register shares = launch registers");
+    static constexpr int THREADS = REG_SPLIT ? 512 : 32 * (CONV_WARPS == 2 ? W2 : W2 + 3);
     static constexpr int CONV_THREADS = 32 * CONV_WARPS;
     static constexpr int MMA_WARP = 2;                        // sub-partition 2; TMEM is allocated by warp 1
     __device__ static int conv_slot(int warp) {
@@ -65,6 +75,10 @@ struct DownCfgT {
     static_assert(EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue width");
     static_assert(CONV_WARPS == 2 || CONV_WARPS == 4, "converter count");
     static constexpr int TSTAGES = TSTAGES_, CSTAGES = QMM_DOWN_CSTAGES, SSTAGES = 2, NBUF = 4;
+    // PAIR: the accumulators of a 64-K step's two blocks are handed over together
+    // (one commit / wait / release per pair instead of per block)
+    static constexpr bool PAIR = QMM_DOWN_PAIR != 0;
+    static constexpr int NHAND = PAIR ? NBUF / 2 : NBUF;        // hand-off barriers
     static constexpr int TMA_GROUPS = TSTAGES_;   // producer lane pairs (IQ4 codes, H codes)
     static_assert(2 * TMA_GROUPS <= 31, "producer lanes: pairs below lane 31");
     static constexpr int KG_MAX = 32;                         // K <= 1024
@@ -76,7 +90,7 @@ struct DownCfgT {
     static constexpr int DW_BYTES = BM * KG_MAX * 2;          // d_W of one tile, [row][block] fp16
     static constexpr int SSTAGE_BYTES = DH_BYTES + DW_BYTES;
     static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, false);
-    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * SSTAGES + 2 * NBUF + 1;
+    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * SSTAGES + 2 * NBUF + 1;   // (NHAND <= NBUF)
     static constexpr int SMEM_BYTES = 1024 + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES +
                                       SSTAGES * SSTAGE_BYTES + BAR_COUNT * 8 + 64;
     static_assert(A_RAW_BYTES % 1024 == 0 && TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0 &&
@@ -84,14 +98,17 @@ struct DownCfgT {
                   "align");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
-// Measured on the 5268-token stage: 8 epilogue warps (64 token columns each,
-// both TMEM loads of a block issued before one wait), 2 converters, 5 TMA and
-// 2 converted stages: 0.447 ms, against 0.475 ms with 16 epilogue warps.
+// Measured on the 5268-token stage (down with the fused combine): 8 epilogue
+// warps (64 token columns each, both TMEM loads of a block issued before one
+// wait), 4 converters under the register split, accumulators handed over in
+// pairs, 5 TMA and 2 converted stages: 0.506 ms, against 0.519 ms with 2
+// converters and 0.530 ms with 2 converters and one hand-off per block (16
+// epilogue warps were slower still).
 #ifndef QMM_DOWN_EPI_WARPS
 #define QMM_DOWN_EPI_WARPS 8
 #endif
 #ifndef QMM_DOWN_CONV_WARPS
-#define QMM_DOWN_CONV_WARPS 2
+#define QMM_DOWN_CONV_WARPS 4
 #endif
 #ifndef QMM_DOWN_TSTAGES
 #define QMM_DOWN_TSTAGES 5
@@ -138,8 +155,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t* full_s = empty_c + C::CSTAGES;
     uint64_t* empty_s = full_s + C::SSTAGES;
     uint64_t* acc_full = empty_s + C::SSTAGES;
-    uint64_t* acc_empty = acc_full + C::NBUF;
-    uint64_t* drain_bar = acc_empty + C::NBUF;
+    uint64_t* acc_empty = acc_full + C::NHAND;
+    uint64_t* drain_bar = acc_empty + C::NHAND;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -158,7 +175,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&full_s[i], 1);
             mbar_init(&empty_s[i], C::EPI_WARPS);
         }
-        for (int i = 0; i < C::NBUF; ++i) {
+        for (int i = 0; i < C::NHAND; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], C::EPI_WARPS);
         }
@@ -181,127 +198,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int entries = min(*p.num_entries, p.max_entries);
     const int num_tiles = entries * p.n_tiles;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer (one warp)
-        // A thread has one TMA copy executing at a time (~0.8-0.9k cycles each on
-        // GB300, whatever the size), so the two copies of stage s come from lanes
-        // 2*(s % TMA_GROUPS) and 2*(s % TMA_GROUPS) + 1, and the per-tile scale
-        // copies from lane 31: copies of different stages overlap.
-        {
-            int s = 0, ss = 0;
-            uint32_t ph = 0, sph = 0;
-            long issued = 0, s_issued = 0;
-            bool ok = true;
-            const uint32_t dh_bytes = (uint32_t)(groups * C::BN * 4);
-            const uint32_t dw_bytes = (uint32_t)(C::BM * groups * 2);
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const int entry = t / p.n_tiles;
-                const int n0 = (t - entry * p.n_tiles) * C::BM;
-                const int4 g = p.tiles[entry];
-                // the expert's IQ4 codes: its own tensor map (pointer-table form) at rows
-                // n0.., or the kernel parameter over the contiguous [E*D] rows
-                const CUtensorMap* amap = p.wmaps ? p.wmaps + g.x : &tmA;
-                const int arow = (p.wmaps ? 0 : g.x * p.N) + n0;
-                if (p.wmaps) tensormap_acquire(amap);
-                // this tile's d_H and d_W values
-                const bool got_s = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
-                if (__any_sync(0xffffffffu, !got_s)) break;
-                if (lane == 31) {
-                    uint8_t* sst = sstage + ss * C::SSTAGE_BYTES;
-                    const __half* dw = p.dW_tab ? p.dW_tab[g.x] + (long)n0 * groups : p.dW + ((long)g.x * p.N + n0) * groups;
-                    mbar_arrive_expect_tx(&full_s[ss], dh_bytes + dw_bytes);
-                    bulk_load(sst, p.dH32 + (long)entry * groups * C::BN, dh_bytes, &full_s[ss]);
-                    bulk_load(sst + C::DH_BYTES, dw, dw_bytes, &full_s[ss]);
-                }
-                __syncwarp();
-                ++s_issued;
-                if (++ss == C::SSTAGES) {
-                    ss = 0;
-                    sph ^= 1u;
-                }
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
-                    if (__any_sync(0xffffffffu, !got)) {
-                        ok = false;
-                        break;
-                    }
-                    const int l0 = 2 * (s % C::TMA_GROUPS);
-                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                    if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
-                    __syncwarp();
-                    if (lane == l0)
-                        tma_load_2d(st, amap, &full_t[s], kb * 32, arow);
-                    else if (lane == l0 + 1)
-                        tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
-                    __syncwarp();
-                    ++issued;
-                    if (++s == C::TSTAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            if (lane == 0) {
-                drain_ring(full_t, issued, C::TSTAGES, p.err);
-                drain_ring(full_s, s_issued, C::SSTAGES, p.err);
-            }
-        }
-        __syncwarp();
-    } else if (warp == C::MMA_WARP) {
-        // ------------------------------------------------------------ MMA issuer (one lane)
-        // A single thread runs the whole issue loop: no per-MMA election or warp
-        // votes, so each K block costs a few dozen instructions on this warp.
-        if (lane == 0) {
-            int cs = 0, ts = 0, buf = 0;
-            uint32_t cph = 0, bph = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < kblocks && ok; ++kb) {
-                    // expanded weights ready: the converters arrive on full_c only after they saw
-                    // the TMA stage (IQ4 codes and H codes) complete, so full_c orders the H
-                    // codes of the same stage too
-                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
-                        ok = false;
-                        break;
-                    }
-                    // (no tcgen05 fence here: the operands are ordered by the mbarriers and the
-                    // writers' proxy fence; a tcgen05 fence per K block would drain the MMA pipe)
-                    const uint32_t a_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
-                    const uint32_t b_base = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
-#pragma unroll
-                    for (int h = 0; h < C::BK / C::GROUP_K; ++h) {
-                        // one 32-K block: two K=16 MMAs into its own accumulator
-                        if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::BN);
-                        const uint32_t off = (uint32_t)(h * C::GROUP_K * 2);
-                        tc_mma_f16(dtmem, smem_desc_sw128(a_base + off), smem_desc_sw128(b_base + off), C::IDESC, 0u);
-                        tc_mma_f16(dtmem, smem_desc_sw128(a_base + off + 32), smem_desc_sw128(b_base + off + 32),
-                                   C::IDESC, 1u);
-                        tc_commit(&acc_full[buf]);
-                        if (++buf == C::NBUF) {
-                            buf = 0;
-                            bph ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                    tc_commit(&empty_c[cs]);
-                    tc_commit(&empty_t[ts]);
-                    if (++cs == C::CSTAGES) {
-                        cs = 0;
-                        cph ^= 1u;
-                    }
-                    if (++ts == C::TSTAGES) ts = 0;
-                }
-            }
-            tc_commit(drain_bar);
-            drain_ring(drain_bar, 1, 1, p.err);
-        }
-        __syncwarp();
-    } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
+    // Roles.  With the register split, each warpgroup runs exactly one setmaxnreg
+    // (the epilogue warpgroups the inc, the others the dec), at the top of the
+    // code it governs.
+    if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
+        if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::REGS_EPI>();
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int cq = (warp - C::EPI_BASE) >> 2;              // this warp's block of CPW token columns
@@ -326,15 +227,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             float2 y[C::CPW / 2];
 #pragma unroll
             for (int j = 0; j < C::CPW / 2; ++j) y[j] = make_float2(0.f, 0.f);
-            for (int g = 0; g < groups; ++g) {
-                if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+            // fold this warp's CPW columns of block g from accumulator buffer b
+            auto fold_block = [&](int g, int b, bool release, int hand) {
                 const float dwf = __half2float(__ushort_as_half((unsigned short)lds_u16(dw_addr + g * 2)));
                 const float2 dw2 = make_float2(dwf, dwf);
-                const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + cq * C::CPW);
+                const uint32_t acc = lane_addr + (uint32_t)(b * C::BN + cq * C::CPW);
                 // all of this warp's accumulator columns for the block: loads issued
                 // together, one wait, the buffer handed back before the fold
                 uint32_t v[C::NCH][C::CW];
@@ -344,9 +241,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     else tmem_ld16(acc + c * C::CW, v[c]);
                 }
                 tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                if (release) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[hand]);
+                }
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
 #pragma unroll
@@ -363,7 +262,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         y23 = __ffma2_rn(__fmul2_rn(i23, d23), dw2, y23);
                     }
                 }
-                if (++buf == C::NBUF) {
+            };
+            for (int g = 0; g < groups; g += (C::PAIR ? 2 : 1)) {
+                if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if constexpr (C::PAIR) {
+                    fold_block(g, 2 * buf, false, buf);
+                    fold_block(g + 1, 2 * buf + 1, true, buf);
+                } else {
+                    fold_block(g, buf, true, buf);
+                }
+                if (++buf == C::NHAND) {
                     buf = 0;
                     bph ^= 1u;
                 }
@@ -411,36 +323,183 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             g4 = g4n;
         }
-    } else if (C::conv_slot(warp) >= 0) {
-        // ------------------------------------------------------------ converters (IQ4 indices -> f16)
-        const int ct = C::conv_slot(warp) * 32 + lane;
-        int ts = 0, cs = 0;
-        uint32_t tph = 0, cph = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
-                    !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY)) {
-                    ok = false;
-                    break;
+    } else {
+        if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
+        if (warp == 0) {
+            // ------------------------------------------------------------ producer (one warp)
+            // A thread has one TMA copy executing at a time (~0.8-0.9k cycles each on
+            // GB300, whatever the size), so the two copies of stage s come from lanes
+            // 2*(s % TMA_GROUPS) and 2*(s % TMA_GROUPS) + 1, and the per-tile scale
+            // copies from lane 31: copies of different stages overlap.
+            {
+                int s = 0, ss = 0;
+                uint32_t ph = 0, sph = 0;
+                long issued = 0, s_issued = 0;
+                bool ok = true;
+                const uint32_t dh_bytes = (uint32_t)(groups * C::BN * 4);
+                const uint32_t dw_bytes = (uint32_t)(C::BM * groups * 2);
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    const int entry = t / p.n_tiles;
+                    const int n0 = (t - entry * p.n_tiles) * C::BM;
+                    const int4 g = p.tiles[entry];
+                    // the expert's IQ4 codes: its own tensor map (pointer-table form) at rows
+                    // n0.., or the kernel parameter over the contiguous [E*D] rows
+                    const CUtensorMap* amap = p.wmaps ? p.wmaps + g.x : &tmA;
+                    const int arow = (p.wmaps ? 0 : g.x * p.N) + n0;
+                    if (p.wmaps) tensormap_acquire(amap);
+                    // this tile's d_H and d_W values
+                    const bool got_s = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                    if (__any_sync(0xffffffffu, !got_s)) break;
+                    if (lane == 31) {
+                        uint8_t* sst = sstage + ss * C::SSTAGE_BYTES;
+                        const __half* dw = p.dW_tab ? p.dW_tab[g.x] + (long)n0 * groups : p.dW + ((long)g.x * p.N + n0) * groups;
+                        mbar_arrive_expect_tx(&full_s[ss], dh_bytes + dw_bytes);
+                        bulk_load(sst, p.dH32 + (long)entry * groups * C::BN, dh_bytes, &full_s[ss]);
+                        bulk_load(sst + C::DH_BYTES, dw, dw_bytes, &full_s[ss]);
+                    }
+                    __syncwarp();
+                    ++s_issued;
+                    if (++ss == C::SSTAGES) {
+                        ss = 0;
+                        sph ^= 1u;
+                    }
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                        if (__any_sync(0xffffffffu, !got)) {
+                            ok = false;
+                            break;
+                        }
+                        const int l0 = 2 * (s % C::TMA_GROUPS);
+                        uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                        if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                        __syncwarp();
+                        if (lane == l0)
+                            tma_load_2d(st, amap, &full_t[s], kb * 32, arow);
+                        else if (lane == l0 + 1)
+                            tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
+                        __syncwarp();
+                        ++issued;
+                        if (++s == C::TSTAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
                 }
-                const uint32_t traw = smem_u32(tstage + ts * C::TSTAGE_BYTES);
-                const uint32_t cbase = smem_u32(cstage + cs * C::CSTAGE_BYTES);
-#pragma unroll
-                for (int rr = ct; rr < C::BM; rr += C::CONV_THREADS) convert_iq4_row(traw, cbase, rr);
-                fence_proxy_async_smem();
-                __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&full_c[cs]);
-                    mbar_arrive(&empty_t[ts]);
+                    drain_ring(full_t, issued, C::TSTAGES, p.err);
+                    drain_ring(full_s, s_issued, C::SSTAGES, p.err);
                 }
-                if (++ts == C::TSTAGES) {
-                    ts = 0;
-                    tph ^= 1u;
+            }
+            __syncwarp();
+        } else if (warp == C::MMA_WARP) {
+            // ------------------------------------------------------------ MMA issuer (one lane)
+            // A single thread runs the whole issue loop: no per-MMA election or warp
+            // votes, so each K block costs a few dozen instructions on this warp.
+            if (lane == 0) {
+                int cs = 0, ts = 0, buf = 0;
+                uint32_t cph = 0, bph = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    for (int kb = 0; kb < kblocks && ok; ++kb) {
+                        // expanded weights ready: the converters arrive on full_c only after they saw
+                        // the TMA stage (IQ4 codes and H codes) complete, so full_c orders the H
+                        // codes of the same stage too
+                        if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                            ok = false;
+                            break;
+                        }
+                        // (no tcgen05 fence here: the operands are ordered by the mbarriers and the
+                        // writers' proxy fence; a tcgen05 fence per K block would drain the MMA pipe)
+                        const uint32_t a_base = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+                        const uint32_t b_base = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
+                        if constexpr (C::PAIR) {
+                            // the step's two 32-K blocks into the two buffers of hand-off pair buf
+                            if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+    #pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const uint32_t dtmem = tmem_base + (uint32_t)((2 * buf + h) * C::BN);
+                                const uint32_t off = (uint32_t)(h * C::GROUP_K * 2);
+                                tc_mma_f16(dtmem, smem_desc_sw128(a_base + off), smem_desc_sw128(b_base + off), C::IDESC,
+                                           0u);
+                                tc_mma_f16(dtmem, smem_desc_sw128(a_base + off + 32), smem_desc_sw128(b_base + off + 32),
+                                           C::IDESC, 1u);
+                            }
+                            tc_commit(&acc_full[buf]);
+                            if (++buf == C::NHAND) {
+                                buf = 0;
+                                bph ^= 1u;
+                            }
+                        } else {
+    #pragma unroll
+                            for (int h = 0; h < C::BK / C::GROUP_K; ++h) {
+                                // one 32-K block: two K=16 MMAs into its own accumulator
+                                if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::BN);
+                                const uint32_t off = (uint32_t)(h * C::GROUP_K * 2);
+                                tc_mma_f16(dtmem, smem_desc_sw128(a_base + off), smem_desc_sw128(b_base + off), C::IDESC,
+                                           0u);
+                                tc_mma_f16(dtmem, smem_desc_sw128(a_base + off + 32), smem_desc_sw128(b_base + off + 32),
+                                           C::IDESC, 1u);
+                                tc_commit(&acc_full[buf]);
+                                if (++buf == C::NBUF) {
+                                    buf = 0;
+                                    bph ^= 1u;
+                                }
+                            }
+                        }
+                        if (!ok) break;
+                        tc_commit(&empty_c[cs]);
+                        tc_commit(&empty_t[ts]);
+                        if (++cs == C::CSTAGES) {
+                            cs = 0;
+                            cph ^= 1u;
+                        }
+                        if (++ts == C::TSTAGES) ts = 0;
+                    }
                 }
-                if (++cs == C::CSTAGES) {
-                    cs = 0;
-                    cph ^= 1u;
+                tc_commit(drain_bar);
+                drain_ring(drain_bar, 1, 1, p.err);
+            }
+            __syncwarp();
+        } else if (C::conv_slot(warp) >= 0) {
+            // ------------------------------------------------------------ converters (IQ4 indices -> f16)
+            const int ct = C::conv_slot(warp) * 32 + lane;
+            int ts = 0, cs = 0;
+            uint32_t tph = 0, cph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
+                        !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t traw = smem_u32(tstage + ts * C::TSTAGE_BYTES);
+                    const uint32_t cbase = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+    #pragma unroll
+                    for (int rr = ct; rr < C::BM; rr += C::CONV_THREADS) convert_iq4_row(traw, cbase, rr);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&full_c[cs]);
+                        mbar_arrive(&empty_t[ts]);
+                    }
+                    if (++ts == C::TSTAGES) {
+                        ts = 0;
+                        tph ^= 1u;
+                    }
+                    if (++cs == C::CSTAGES) {
+                        cs = 0;
+                        cph ^= 1u;
+                    }
                 }
             }
         }

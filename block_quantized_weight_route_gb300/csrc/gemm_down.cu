@@ -11,6 +11,15 @@ static cudaError_t launch_down(const CUtensorMap& tmA, const CUtensorMap& tmB, c
     cudaError_t e = cudaFuncSetAttribute(down_iq4_kernel<DownCfg, COMBINE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DownCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    if constexpr (DownCfg::REG_SPLIT) {
+        // the warpgroups' register shares add up to 128 a thread: launch only if
+        // the kernel is allocated exactly that many (more shares than the pool
+        // would leave a setmaxnreg.inc waiting)
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, down_iq4_kernel<DownCfg, COMBINE>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != DownCfg::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
+    }
     down_iq4_kernel<DownCfg, COMBINE><<<grid, DownCfg::THREADS, DownCfg::SMEM_BYTES, s>>>(tmA, tmB, p);
     return cudaGetLastError();
 }

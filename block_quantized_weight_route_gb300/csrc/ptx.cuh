@@ -277,6 +277,19 @@ __host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, bool bf16) {
            ((uint32_t)(M >> 4) << 24);
 }
 
+// Register split between warpgroups: the four warps of a warpgroup give back
+// registers to (dec) or take them from (inc) the pool the block was launched
+// with, down or up to N per thread.  An inc waits until the pool holds enough,
+// so the shares must add up to no more than the launch's registers.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
