@@ -11,12 +11,17 @@ namespace qmm {
 // converter warps expand two weight rows per thread.
 template <int CN>
 using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 2, 16, 4, 4, false, CN, 2>;
+// CTA pair: 256 x 256 tiles, each CTA 128 token rows and 128 weight rows (one
+// 128 x 128 scale block), the fold over its 128 rows x both CTAs' columns.
+using CfgFp8Pair = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 2, 16, 5, 4, false, 2, 1, true>;
+static_assert(CfgFp8<1>::TILE_M == CfgFp8Pair::TILE_M, "one routing of rows for both forms");
 
-int fp8_tile_rows() { return CfgFp8<1>::BM; }
+int fp8_tile_rows() { return CfgFp8<1>::TILE_M; }
 
 cudaError_t launch_fp8_blk128(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                               cudaStream_t s) {
     const int items = p.m_tiles * (p.n_tiles / cn);
+    if (QMM_PAIR && cn == 2) return launch_qgemm<CfgFp8Pair>(tmA, tmB, p, items, s);
     switch (cn) {
         case 4: return launch_qgemm<CfgFp8<4>>(tmA, tmB, p, items, s);
         case 2: return launch_qgemm<CfgFp8<2>>(tmA, tmB, p, items, s);

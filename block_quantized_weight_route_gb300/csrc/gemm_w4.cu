@@ -25,11 +25,24 @@ using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 128, 8, 4, 4, 3, false, CN, 2>
 // Gate/up: 256 token rows x (64 gate + 64 up) weight rows per tile.
 template <int CN>
 using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, QMM_GU_TSTAGES, QMM_GU_CSTAGES, true, CN, 2>;
+// CTA-pair forms (clusters of 2): 256 token rows x 256 weight rows per pair,
+// each CTA 128 token rows and 128 weight rows (gate/up: 64 gate + 64 up).
+#ifndef QMM_PAIR_TSTAGES
+#define QMM_PAIR_TSTAGES 6
+#endif
+#ifndef QMM_PAIR_CSTAGES
+#define QMM_PAIR_CSTAGES 4
+#endif
+using CfgW4DensePair = GemmCfg<BMode::W4, Epi::STORE, 128, 8, 4, QMM_PAIR_TSTAGES, QMM_PAIR_CSTAGES, false, 2, 1, true>;
+using CfgW4GateUpPair = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, QMM_PAIR_TSTAGES, QMM_PAIR_CSTAGES, true, 2, 1, true>;
+static_assert(CfgW4GateUp<1>::TILE_M == CfgW4GateUpPair::TILE_M, "one routing of rows for both forms");
 
 // Wide tiles do a tile's work in about 1.75x the time of a narrow one (measured:
 // 0.305 against 0.349 ms at M=2048, K=5120, N=17408), so they win unless their
 // coarser waves leave more SMs idle.
 TileShape w4_dense_shape(int M, int N, int sms) {
+    // CTA pairs: narrow per-CTA tiles (the pair's tile is 256 x 256)
+    if (QMM_PAIR && ((N + 127) / 128) % 2 == 0) return TileShape{256, 128};
     const long wide = (long)((M + 255) / 256) * ((N + 255) / 256);
     const long narrow = (long)((M + 255) / 256) * ((N + 127) / 128);
     const long wide_waves = (wide + sms - 1) / sms, narrow_waves = (narrow + sms - 1) / sms;
@@ -60,6 +73,7 @@ cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, c
             default: return launch_qgemm<CfgW4DenseWide<1>>(tmA, tmB, p, items, s);
         }
     }
+    if (QMM_PAIR && cn == 2) return launch_qgemm<CfgW4DensePair>(tmA, tmB, p, items, s);
     switch (cn) {
         case 4: return launch_qgemm<CfgW4Dense<4>>(tmA, tmB, p, items, s);
         case 2: return launch_qgemm<CfgW4Dense<2>>(tmA, tmB, p, items, s);
@@ -69,6 +83,7 @@ cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, c
 
 cudaError_t launch_w4_gate_up_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                      cudaStream_t s) {
+    if (QMM_PAIR && cn == 2) return launch_qgemm<CfgW4GateUpPair>(tmA, tmB, p, 0, s);
     switch (cn) {
         case 4: return launch_qgemm<CfgW4GateUp<4>>(tmA, tmB, p, 0, s);
         case 2: return launch_qgemm<CfgW4GateUp<2>>(tmA, tmB, p, 0, s);

@@ -95,23 +95,62 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
+// Cluster-scope forms, for a barrier that threads of another CTA of the cluster
+// arrive on (remote arrivals with release.cluster): the completed phase then
+// also orders that CTA's earlier shared-memory writes before this thread's
+// later operations.
+__device__ __forceinline__ bool mbar_test_wait_cl(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Arrive once on the mbarrier at `bar`'s offset in CTA `rank` of the cluster
+// (this CTA included), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank) {
+    asm volatile(
+        "{\n\t.reg .b32 ra;\n\t"
+        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(rank)
+        : "memory");
+}
+
 // Wait for phase `parity` of `bar` to complete.  Returns false (after setting
 // *err to `code` if no error was recorded yet, and raising the CTA-wide abort
 // flag) when the wait times out or another role of the CTA has aborted.
 // After a first poll the thread sleeps in try_wait (woken on completion, or
 // after at most 2 us) rather than spinning: polling warps slow the warps that
 // do the work.  The wall clock (slow to read) is consulted every 64 sleeps.
+// CLUSTER: cluster-scope acquire (a barrier with arrivals from another CTA).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               uint32_t* err, uint32_t code, uint64_t limit_ns) {
 #ifndef QMM_WAIT_TEST_FIRST
 #define QMM_WAIT_TEST_FIRST 1
 #endif
-    if (QMM_WAIT_TEST_FIRST ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if constexpr (CLUSTER) {
+        if (mbar_test_wait_cl(bar, parity)) return true;
+    } else {
+        if (QMM_WAIT_TEST_FIRST ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    }
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
+        for (int i = 0; i < 64; ++i) {
+            if constexpr (CLUSTER) {
+                // (polled: a sleeping cluster-scope wait was no faster)
+                if (mbar_test_wait_cl(bar, parity)) return true;
+            } else {
+                if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
+            }
+        }
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             atomicCAS(err, 0u, code);
@@ -123,7 +162,11 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, vo
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* err, uint32_t code) {
-    return mbar_wait_for(bar, parity, abort_flag, err, code, kWaitTimeoutNs);
+    return mbar_wait_for<false>(bar, parity, abort_flag, err, code, kWaitTimeoutNs);
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             uint32_t* err, uint32_t code) {
+    return mbar_wait_for<true>(bar, parity, abort_flag, err, code, kWaitTimeoutNs);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -196,6 +239,18 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// CTA-pair (cta_group::2) allocation: one warp of each of the two CTAs of the
+// pair executes it; both CTAs receive the same TMEM address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_slot, uint32_t ncols) {   // whole warp, both CTAs
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {   // whole warp, both CTAs
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -212,6 +267,30 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// CTA-pair MMA, issued by one thread of the even CTA of the pair: M = 256 rows,
+// rows [0, 128) from A at the descriptor's address in the even CTA's shared
+// memory and rows [128, 256) from the same address in the odd CTA's; of the N
+// columns, [0, N/2) come from B in the even CTA and [N/2, N) from B in the odd
+// one.  Each CTA's TMEM receives its own 128 rows, all N columns, at d_tmem.
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at `bar`'s offset in every CTA of cta_mask when the
+// pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "h"(cta_mask)
+                 : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.

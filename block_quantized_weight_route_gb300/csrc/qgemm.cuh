@@ -36,13 +36,29 @@
 
 namespace qmm {
 
+// CTA-pair (cta_group::2) GEMMs wherever a launch forms clusters of 2.
+#ifndef QMM_PAIR
+#define QMM_PAIR 0
+#endif
+
 enum class BMode { W4, FP8 };
 enum class Epi { STORE, SWIGLU_Q81, FOLD_FP8 };
 
 template <BMode B_, Epi E_, int BN_, int CONV_WARPS_, int EPI_WARPS_, int TSTAGES_, int CSTAGES_, bool GROUPED_,
-          int CLUSTER_N_ = 1, int MSUB_ = 1>
+          int CLUSTER_N_ = 1, int MSUB_ = 1, bool PAIR_ = false>
 struct GemmCfg {
     static constexpr BMode B = B_;
+    // CTA pair (cta_group::2): the two CTAs of a cluster of 2 compute one
+    // 256 x 2*BN tile with M = 256 MMAs issued by the even CTA.  Each CTA holds
+    // 128 activation rows and converts BN weight rows (its half of the MMA's N);
+    // its TMEM receives its 128 rows x all 2*BN columns.  Every MMA then reads
+    // half of each operand from each CTA's shared memory, which halves the
+    // shared-memory operand traffic per FLOP against a one-CTA M = 128 MMA.
+    static constexpr bool PAIR = PAIR_;
+    static_assert(!PAIR || (CLUSTER_N_ == 2 && MSUB_ == 1), "CTA pair: a cluster of 2, one 128-row tile per CTA");
+    // accumulator columns per row sub-tile, and rows of the tile a work item covers
+    static constexpr int ACC_N = PAIR_ ? 2 * BN_ : BN_;
+    static constexpr int TILE_M = PAIR_ ? 256 : 128 * MSUB_;
     // MSUB row blocks of 128 share every converted weight tile: each K step
     // issues MSUB MMAs (one per 128-row sub-tile) against the same B operand,
     // which divides the conversion work per FLOP by MSUB.
@@ -51,7 +67,7 @@ struct GemmCfg {
     // tiles; each loads 1/CLUSTER_N of the activation tile and multicasts it to
     // all, so the activations cross L2 once per cluster instead of once per CTA.
     static constexpr int CLUSTER_N = CLUSTER_N_;
-    static constexpr int A_SLICE_ROWS = 128 * MSUB_ / CLUSTER_N_;
+    static constexpr int A_SLICE_ROWS = PAIR_ ? 128 : 128 * MSUB_ / CLUSTER_N_;
     static constexpr Epi EPI = E_;
     static constexpr bool GROUPED = GROUPED_;
     static constexpr int BM = 128 * MSUB_, BN = BN_, BK = 64, UMMA_K = 16;
@@ -70,9 +86,15 @@ struct GemmCfg {
     static constexpr int MAXNREG_RAW = 16384 / (WARPS_PER_SMSP * 32) / 8 * 8;
     static constexpr int MAXNREG = MAXNREG_RAW > 255 ? 255 : MAXNREG_RAW;
     // fold epilogue: token columns per warp, and the TMEM load width
-    static constexpr int FOLD_CPW = 128 / (EPI_WARPS_ >= 8 ? EPI_WARPS_ / 4 : 1);
+    static constexpr int FOLD_CPW = ACC_N / (EPI_WARPS_ >= 8 ? EPI_WARPS_ / 4 : 1);
     static constexpr int FOLD_LDW = (EPI_WARPS_ == 16) ? 16 : 32;
     static constexpr int TSTAGES = TSTAGES_, CSTAGES = CSTAGES_;
+    // converted stages handed over per proxy fence (at most CSTAGES / 2, so that
+    // the MMA always holds a batch while the converters fill the next)
+#ifndef QMM_CONV_BATCH
+#define QMM_CONV_BATCH 1
+#endif
+    static constexpr int CONV_BATCH = (QMM_CONV_BATCH < CSTAGES_ / 2) ? QMM_CONV_BATCH : (CSTAGES_ / 2 > 0 ? CSTAGES_ / 2 : 1);
     // producer lane groups (4 lanes each: activation copy, one or two weight copies)
     static constexpr int TMA_GROUPS = TSTAGES_;
     static_assert(TMA_GROUPS * 4 <= 32, "producer lane groups fit one warp");
@@ -87,19 +109,20 @@ struct GemmCfg {
     static constexpr bool FOLD = (E_ == Epi::FOLD_FP8);
     static constexpr int GROUP_K = FOLD ? 128 : 0;   // 0: whole K
     static_assert(GROUP_K == 0 || GROUP_K == 2 * BK, "fold groups span two K blocks");
-    static constexpr int NBUF = 512 / (BN * MSUB_);
-    static constexpr uint32_t IDESC = idesc_kind_f16(128, BN, true);
+    static constexpr int NBUF = 512 / (ACC_N * MSUB_);
+    static constexpr uint32_t IDESC = PAIR_ ? idesc_kind_f16(256, 2 * BN_, true) : idesc_kind_f16(128, BN_, true);
+    static_assert(ACC_N <= 256, "MMA N");
     // converter threads per weight row, or weight rows per converter thread
     static constexpr int TPR = (CONV_WARPS_ * 32 >= BN_) ? CONV_WARPS_ * 32 / BN_ : 1;
     static constexpr int RPT = (CONV_WARPS_ * 32 >= BN_) ? 1 : BN_ / (CONV_WARPS_ * 32);
-    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * NBUF + 1;
+    static constexpr int BAR_COUNT = 2 * TSTAGES + 3 * CSTAGES + 2 * NBUF + 1;
     static constexpr int SMEM_BYTES =
         1024 /*align slack*/ + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES + BAR_COUNT * 8 + 64;
     static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
     static_assert(!FOLD || EPI_WARPS == 8 || EPI_WARPS == 16, "fold epilogue: two or four warps per lane quarter");
     static_assert(!FOLD || FOLD_CPW % 8 == 0, "fold columns per warp: whole 16-byte runs");
-    static_assert(GROUPED_ || 128 * MSUB_ * BN_ <= 65536, "split partial tile at most 256 x 256");
+    static_assert(GROUPED_ || 128 * MSUB_ * ACC_N <= 65536, "split partial tile at most 256 x 256");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
     static_assert(TPR == 1 || (TPR == 2 && B_ == BMode::W4), "one or (W4) two converter threads per weight row");
     static_assert(CONV_WARPS * 32 * RPT == TPR * BN, "converters cover the weight rows");
@@ -111,6 +134,22 @@ struct GemmCfg {
     static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4) ||
                       (EPI_WARPS == 16 && CONV_WARPS == 2),
                   "warp layout");
+    // relay threads of a pair's odd CTA: lane 0 of the MMA warp (slot 0) and of the
+    // warps without a role (slots 1, 2: warps 5 and 9 with 4 epilogue warps)
+#ifndef QMM_RELAYS
+#define QMM_RELAYS 3
+#endif
+    static constexpr int RELAYS = (PAIR_ && EPI_WARPS_ == 4) ? QMM_RELAYS : 1;
+    // a relay waits on a converted stage's barrier only after forwarding the stage
+    // RELAYS before it, which completes the barrier's previous phase only if
+    // RELAYS <= CSTAGES (a parity wait two phases ahead would pass at once)
+    static_assert(RELAYS >= 1 && RELAYS <= 3 && (!PAIR_ || RELAYS <= CSTAGES_), "relay threads");
+    __device__ static int relay_slot(int warp) {
+        if (warp == 1) return 0;
+        if (EPI_WARPS == 4 && RELAYS >= 2 && warp == 5) return 1;
+        if (EPI_WARPS == 4 && RELAYS >= 3 && warp == 9) return 2;
+        return -1;
+    }
     // converter slot of a warp, -1 if it is not a converter:
     //   4 epilogue warps (12..15):  converters on warps 2,3,4,6,7,8,10,11
     //   8 epilogue warps (4..11):   converters on warps 2,3,12,14
@@ -143,11 +182,18 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int g, int 
         const int entry = g / n_groups, nt = (g - entry * n_groups) * C::CLUSTER_N + crank;
         const int4 e4 = p.tiles[entry];
         ti.expert = e4.x;
-        ti.row0 = e4.y;
-        ti.rows = e4.z;
+        if constexpr (C::PAIR) {
+            // the 256-row tile's half held by this CTA of the pair (rows may be 0)
+            ti.row0 = e4.y + crank * 128;
+            ti.rows = max(0, min(128, e4.z - crank * 128));
+            ti.entry = e4.w + crank;
+        } else {
+            ti.row0 = e4.y;
+            ti.rows = e4.z;
+            // index of the first 128-row routing entry the tile covers (two per tile when MSUB == 2)
+            ti.entry = (C::MSUB == 2) ? e4.w : entry;
+        }
         ti.n0 = nt * p.n_step;
-        // index of the first 128-row routing entry the tile covers (two per tile when MSUB == 2)
-        ti.entry = (C::MSUB == 2) ? e4.w : entry;
         ti.kb0 = 0;
         ti.kb1 = (p.K + C::BK - 1) / C::BK;
         ti.split = -1;
@@ -163,8 +209,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int g, int 
         }
         const int mt = tile % p.m_tiles, nt = (tile / p.m_tiles) * C::CLUSTER_N + crank;
         ti.expert = 0;
-        ti.row0 = mt * C::BM;
-        ti.rows = min(C::BM, p.M - ti.row0);
+        if constexpr (C::PAIR) {
+            ti.row0 = mt * C::TILE_M + crank * 128;
+            ti.rows = max(0, min(128, p.M - ti.row0));
+        } else {
+            ti.row0 = mt * C::BM;
+            ti.rows = min(C::BM, p.M - ti.row0);
+        }
         ti.n0 = nt * p.n_step;
         ti.entry = mt;
         const int kblocks = (p.K + C::BK - 1) / C::BK;   // K % 64 == 32: a last half block
@@ -383,8 +434,11 @@ __device__ __forceinline__ void store_out32(const GemmParams& p, long grow, int 
 
 // K splits of the last wave: out[tile rows, tile columns] = scale x (sum of the
 // S partial tiles in split order), one thread per 4 consecutive columns; rows
-// and columns outside [M, N) are not written.  Partials as in GemmParams.
-static __global__ void __launch_bounds__(256) split_reduce_kernel(GemmParams p, int BM, int BN, int CN, int rem, float scale) {
+// and columns outside [M, N) are not written.  Partials as in GemmParams: one
+// BM x BN partial per CTA, the CTAs of a cluster on consecutive column tiles,
+// or (pair) on the two 128-row halves of a 256-row tile with all BN columns.
+static __global__ void __launch_bounds__(256) split_reduce_kernel(GemmParams p, int BM, int BN, int CN, int rem, float scale,
+                                                                  bool cta_pair) {
     const long per_tile = (long)BM * (BN / 4);
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)rem * CN * per_tile) return;
@@ -393,9 +447,10 @@ static __global__ void __launch_bounds__(256) split_reduce_kernel(GemmParams p, 
     const int r = within / (BN / 4), c4 = within - r * (BN / 4);
     const int j = pair / CN, crank = pair - j * CN;
     const int tile = p.split_from + j;
-    const int mt = tile % p.m_tiles, nt = (tile / p.m_tiles) * CN + crank;
-    const long grow = (long)mt * BM + r;
-    const int col = nt * p.n_step + c4 * 4;
+    const int mt = tile % p.m_tiles;
+    const long grow = cta_pair ? (long)mt * 256 + crank * 128 + r : (long)mt * BM + r;
+    const int col =
+        cta_pair ? (tile / p.m_tiles) * CN * p.n_step + c4 * 4 : ((tile / p.m_tiles) * CN + crank) * p.n_step + c4 * 4;
     if (grow >= p.M || col >= p.N) return;
     const float4* src = reinterpret_cast<const float4*>(p.split_part + (long)pair * p.split_S * BM * BN + (long)r * BN) + c4;
     const long sstride = (long)BM * BN / 4;
@@ -433,7 +488,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     uint64_t* acc_full = empty_c + C::CSTAGES;
     uint64_t* acc_empty = acc_full + C::NBUF;
     uint64_t* drain_bar = acc_empty + C::NBUF;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    uint64_t* conv_done = drain_bar + 1;   // pair, odd CTA: its converters' local hand-off to the relay
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(conv_done + C::CSTAGES);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -441,16 +497,21 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::TSTAGES; ++i) {
             mbar_init(&full_t[i], 1);
-            // released by the MMA commit of every CTA of the cluster (each read the multicast tile)
-            mbar_init(&empty_t[i], C::CLUSTER_N);
+            // released by the MMA commit of every CTA of the cluster (each read the multicast
+            // tile), or (pair) by the pair's one MMA commit
+            mbar_init(&empty_t[i], C::PAIR ? 1 : C::CLUSTER_N);
         }
+        // pair: the MMA issuer (even CTA) waits on its own full_c, which its converters
+        // arrive on and, once per stage, the odd CTA's relay thread; and on its own
+        // acc_empty, which the epilogue warps of both CTAs arrive on
         for (int i = 0; i < C::CSTAGES; ++i) {
-            mbar_init(&full_c[i], C::CONV_WARPS);
+            mbar_init(&full_c[i], C::PAIR ? C::CONV_WARPS + 1 : C::CONV_WARPS);
             mbar_init(&empty_c[i], 1);
+            mbar_init(&conv_done[i], C::CONV_WARPS);
         }
         for (int i = 0; i < C::NBUF; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], C::EPI_WARPS);
+            mbar_init(&acc_empty[i], (C::PAIR ? 2 : 1) * C::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -460,7 +521,12 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         tma_prefetch_desc(&tmA);
         if (!p.wmaps) tma_prefetch_desc(&tmB);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    if (warp == 1) {
+        if constexpr (C::PAIR)
+            tmem_alloc_pair(tmem_slot, 512);
+        else
+            tmem_alloc(tmem_slot, 512);
+    }
     tc_fence_before();
     __syncthreads();
     if constexpr (C::CLUSTER_N > 1) cluster_sync();   // peers' barriers are initialised before any multicast
@@ -468,6 +534,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     const uint32_t tmem_base = *tmem_slot;
 
     const int crank = (C::CLUSTER_N > 1) ? (int)cluster_ctarank() : 0;
+    // the pair's MMA issuer and the owner of the barriers both CTAs arrive on
+    const bool pair_leader = !C::PAIR || crank == 0;
     const int cid = (C::CLUSTER_N > 1) ? (int)cluster_id_x() : (int)blockIdx.x;
     const int ncl = (C::CLUSTER_N > 1) ? (int)cluster_count_x() : (int)gridDim.x;
     int num_tiles;   // work items (one per cluster step)
@@ -478,6 +546,28 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         const int items = p.m_tiles * (p.n_tiles / C::CLUSTER_N);
         num_tiles = (p.split_S > 1) ? p.split_from + (items - p.split_from) * p.split_S : items;
     }
+
+    // Relay r of the odd CTA of a pair (r < RELAYS): the converted stages with
+    // global index i = r (mod RELAYS), each once all of that CTA's converters have
+    // handed it over (conv_done), to the even CTA's full_c with a cluster-scope
+    // release.  Several relay threads forward consecutive stages concurrently.
+    auto relay_stages = [&](int r) {
+        long i = 0;
+        bool ok = true;
+        for (int t = cid; t < num_tiles && ok; t += ncl) {
+            const TileInfo ri = decode_tile<C>(p, t, crank);
+            for (int kb = ri.kb0; kb < ri.kb1; ++kb, ++i) {
+                if (i % C::RELAYS != r) continue;
+                const int cs = (int)(i % C::CSTAGES);
+                const uint32_t cph = (uint32_t)((i / C::CSTAGES) & 1);
+                if (!mbar_wait(&conv_done[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_cluster(&full_c[cs], 0);
+            }
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -509,7 +599,10 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
                     __syncwarp();
                     if (lane == l0) {
-                        if constexpr (C::CLUSTER_N > 1) {
+                        if constexpr (C::PAIR) {
+                            // this CTA's 128 rows of the pair's 256-row tile
+                            tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
+                        } else if constexpr (C::CLUSTER_N > 1) {
                             // this CTA's slice of the activation tile, written into every CTA of the cluster
                             tma_load_2d_multicast(st + crank * C::A_SLICE_ROWS * 128, &tmA, &full_t[s], kb * C::BK,
                                                   ti.row0 + crank * C::A_SLICE_ROWS,
@@ -547,8 +640,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         // ------------------------------------------------------------ MMA issuer (one lane)
         // One thread runs the whole issue loop: the descriptors of a K block are
         // built once and advanced by constants, and there is no election or warp
-        // synchronisation between MMAs.
-        if (lane == 0) {
+        // synchronisation between MMAs.  Pair: the even CTA issues for both.
+        if (lane == 0 && pair_leader) {
             int ts = 0, cs = 0, buf = 0;
             uint32_t cph = 0, bph = 0;
             bool ok = true;
@@ -565,7 +658,10 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     // Only the converted weights are waited on: the converters arrive on
                     // full_c after they saw this stage's TMA copies complete (full_t), so
                     // full_c also orders the activation tile.
-                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                    // (pair: both CTAs' converters arrive here, after their own TMA stage)
+                    const bool got_c = C::PAIR ? mbar_wait_cl(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)
+                                               : mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
+                    if (!got_c) {
                         ok = false;
                         break;
                     }
@@ -580,7 +676,10 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                         last = kb == mi.kb1 - 1;
                     }
                     if (first) {
-                        if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                        const bool got_a =
+                            C::PAIR ? mbar_wait_cl(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)
+                                    : mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY);
+                        if (!got_a) {
                             ok = false;
                             break;
                         }
@@ -592,27 +691,44 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     // (32 bytes), +1024 per 128-row sub-tile (16 KB)
                     const uint64_t ad = smem_desc_sw128(smem_u32(tstage + ts * C::TSTAGE_BYTES));
                     const uint64_t bd = smem_desc_sw128(smem_u32(cstage + cs * C::CSTAGE_BYTES));
-                    const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::MSUB * C::BN);
+                    const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::MSUB * C::ACC_N);
+                    if constexpr (C::PAIR) {
+                        // M = 256 over the pair, N = 2 * BN: both CTAs' stages at the same offsets
 #pragma unroll
-                    for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-#pragma unroll
-                        for (int m = 0; m < C::MSUB; ++m)
-                            if (m < nsub)
-                                tc_mma_f16(dtmem + (uint32_t)(m * C::BN), ad + (uint64_t)(m * 1024 + kk * 2),
-                                           bd + (uint64_t)(kk * 2), C::IDESC, (first && kk == 0) ? 0u : 1u);
-                    }
-                    if (last) {
-                        tc_commit(&acc_full[buf]);
-                        if (++buf == C::NBUF) {
-                            buf = 0;
-                            bph ^= 1u;
+                        for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk)
+                            tc_mma_f16_pair(dtmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), C::IDESC,
+                                            (first && kk == 0) ? 0u : 1u);
+                        if (last) {
+                            tc_commit_pair(&acc_full[buf], 3);
+                            if (++buf == C::NBUF) {
+                                buf = 0;
+                                bph ^= 1u;
+                            }
                         }
+                        tc_commit_pair(&empty_c[cs], 3);
+                        tc_commit_pair(&empty_t[ts], 3);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+#pragma unroll
+                            for (int m = 0; m < C::MSUB; ++m)
+                                if (m < nsub)
+                                    tc_mma_f16(dtmem + (uint32_t)(m * C::BN), ad + (uint64_t)(m * 1024 + kk * 2),
+                                               bd + (uint64_t)(kk * 2), C::IDESC, (first && kk == 0) ? 0u : 1u);
+                        }
+                        if (last) {
+                            tc_commit(&acc_full[buf]);
+                            if (++buf == C::NBUF) {
+                                buf = 0;
+                                bph ^= 1u;
+                            }
+                        }
+                        tc_commit(&empty_c[cs]);
+                        if constexpr (C::CLUSTER_N > 1)
+                            tc_commit_multicast(&empty_t[ts], (uint16_t)((1u << C::CLUSTER_N) - 1));
+                        else
+                            tc_commit(&empty_t[ts]);
                     }
-                    tc_commit(&empty_c[cs]);
-                    if constexpr (C::CLUSTER_N > 1)
-                        tc_commit_multicast(&empty_t[ts], (uint16_t)((1u << C::CLUSTER_N) - 1));
-                    else
-                        tc_commit(&empty_t[ts]);
                     if (++ts == C::TSTAGES) ts = 0;
                     if (++cs == C::CSTAGES) {
                         cs = 0;
@@ -621,8 +737,14 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 }
             }
             // Teardown: wait until every MMA issued has completed before TMEM is freed.
-            tc_commit(drain_bar);
+            if constexpr (C::PAIR)
+                tc_commit_pair(drain_bar, 1);
+            else
+                tc_commit(drain_bar);
             drain_ring(drain_bar, 1, 1, p.err);
+        }
+        if constexpr (C::PAIR) {
+            if (lane == 0 && !pair_leader) relay_stages(0);
         }
         __syncwarp();
     } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
@@ -633,13 +755,15 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         int buf = 0;
         uint32_t bph = 0;
         bool ok = true;
-        // K splits: this CTA's partial tile of split s, [BM][BN] fp32
-        constexpr long kTileFloats = (long)C::BM * C::BN;
+        // K splits: this CTA's partial tile of split s, [BM][ACC_N] fp32
+        constexpr long kTileFloats = (long)C::BM * C::ACC_N;
         auto split_part = [&](const TileInfo& tt, int s_) -> float* {
             return p.split_part + ((long)(tt.split * C::CLUSTER_N + crank) * p.split_S + s_) * kTileFloats;
         };
         for (int t = cid; t < num_tiles && ok; t += ncl) {
             const TileInfo ti = decode_tile<C>(p, t, crank);
+            // first output column of the tile's accumulator (pair: the even CTA's weight rows)
+            const int n0p = C::PAIR ? ti.n0 - crank * p.n_step : ti.n0;
             if constexpr (!C::FOLD) {
                 if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                     ok = false;
@@ -652,21 +776,21 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     // row sub-tile m: rows m*128 + lane of this warp's quarter
                     const bool valid = m * 128 + row < ti.rows;
                     const long grow = (long)ti.row0 + m * 128 + row;
-                    const uint32_t acc = lane_addr + (uint32_t)(buf * C::MSUB * C::BN + m * C::BN);
+                    const uint32_t acc = lane_addr + (uint32_t)(buf * C::MSUB * C::ACC_N + m * C::ACC_N);
                     if constexpr (C::EPI == Epi::STORE) {
     #pragma unroll 1
-                        for (int c = 0; c < C::BN / 32; ++c) {
+                        for (int c = 0; c < C::ACC_N / 32; ++c) {
                             uint32_t r[32];
                             tmem_ld32(acc + c * 32, r);
                             tmem_ld_wait();
                             float v[32];
     #pragma unroll
                             for (int jj = 0; jj < 32; ++jj) v[jj] = __uint_as_float(r[jj]);
-                            const int col = ti.n0 + c * 32;
+                            const int col = n0p + c * 32;
                             if (ti.split >= 0) {
                                 // K split: the unscaled partial, every row and column of the tile
                                 float4* dst = reinterpret_cast<float4*>(split_part(ti, ti.s) +
-                                                                        (long)(m * 128 + row) * C::BN + c * 32);
+                                                                        (long)(m * 128 + row) * C::ACC_N + c * 32);
     #pragma unroll
                                 for (int jj = 0; jj < 8; ++jj)
                                     dst[jj] = make_float4(v[4 * jj], v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
@@ -674,13 +798,14 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                                 store_out32(p, grow, col, v, p.scale2_dense);
                             }
                         }
-                    } else {   // SWIGLU_Q81: columns [0, BN/2) gate, [BN/2, BN) up
+                    } else {   // SWIGLU_Q81: per BN columns (one CTA's weight rows), [0, BN/2) gate, [BN/2, BN) up
                         const float s2 = p.scale2[ti.expert];
     #pragma unroll 1
-                        for (int c = 0; c < C::BN / 64; ++c) {
+                        for (int cc = 0; cc < C::ACC_N / 64; ++cc) {
+                            const int hh = cc / (C::BN / 64), c = cc - hh * (C::BN / 64);
                             uint32_t g[32], u[32];
-                            tmem_ld32(acc + c * 32, g);
-                            tmem_ld32(acc + C::BN / 2 + c * 32, u);
+                            tmem_ld32(acc + hh * C::BN + c * 32, g);
+                            tmem_ld32(acc + hh * C::BN + C::BN / 2 + c * 32, u);
                             tmem_ld_wait();
                             if (valid) {
                                 float h[32];
@@ -721,7 +846,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     #pragma unroll
                                     for (int j = 0; j < 16; ++j) packed[j] = 0;
                                 }
-                                const int col = ti.n0 + c * 32;
+                                const int col = n0p + hh * (C::BN / 2) + c * 32;
                                 uint4* hq = reinterpret_cast<uint4*>(p.Hq + grow * p.F + col);
     #pragma unroll
                                 for (int j = 0; j < 4; ++j)
@@ -738,7 +863,12 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                if (lane == 0) {
+                    if constexpr (C::PAIR)
+                        mbar_arrive_cluster(&acc_empty[buf], 0);
+                    else
+                        mbar_arrive(&acc_empty[buf]);
+                }
                 if (++buf == C::NBUF) {
                     buf = 0;
                     bph ^= 1u;
@@ -755,8 +885,11 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 for (int m = 0; m < C::MSUB; ++m)
 #pragma unroll
                     for (int j = 0; j < CPW; ++j) sum[m][j] = 0.f;
+                // this warp's columns lie in one 128-wide weight block (pair: either CTA's)
+                const int wblk = (n0p + cq * CPW) / 128;
+                const bool wblk_ok = wblk < p.N / 128;
                 for (int g = ti.kb0 / 2; g < ti.kb1 / 2; ++g) {
-                    const float s = __ldg(p.blk_scale + (long)(ti.n0 / 128) * groups + g);
+                    const float s = wblk_ok ? __ldg(p.blk_scale + (long)wblk * groups + g) : 0.f;
                     if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                         ok = false;
                         break;
@@ -765,7 +898,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
 #pragma unroll
                     for (int m = 0; m < C::MSUB; ++m) {
                         if (m < nsub) {
-                            const uint32_t acc = lane_addr + (uint32_t)(buf * C::MSUB * C::BN + m * C::BN + cq * CPW);
+                            const uint32_t acc = lane_addr + (uint32_t)(buf * C::MSUB * C::ACC_N + m * C::ACC_N + cq * CPW);
 #pragma unroll
                             for (int c = 0; c < CPW / LDW; ++c) {
                                 uint32_t r[LDW];
@@ -780,7 +913,12 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                    if (lane == 0) {
+                        if constexpr (C::PAIR)
+                            mbar_arrive_cluster(&acc_empty[buf], 0);
+                        else
+                            mbar_arrive(&acc_empty[buf]);
+                    }
                     if (++buf == C::NBUF) {
                         buf = 0;
                         bph ^= 1u;
@@ -794,7 +932,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     for (int m = 0; m < C::MSUB; ++m) {
                         if (m < nsub) {
                             float4* dst = reinterpret_cast<float4*>(split_part(ti, ti.s) +
-                                                                    (long)(m * 128 + row) * C::BN + cq * CPW);
+                                                                    (long)(m * 128 + row) * C::ACC_N + cq * CPW);
 #pragma unroll
                             for (int j = 0; j < CPW / 4; ++j)
                                 dst[j] = make_float4(sum[m][4 * j], sum[m][4 * j + 1], sum[m][4 * j + 2], sum[m][4 * j + 3]);
@@ -806,7 +944,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 for (int m = 0; m < C::MSUB; ++m) {
                     if (m < nsub && m * 128 + row < ti.rows) {
                         const long grow = (long)ti.row0 + m * 128 + row;
-                        const int col = ti.n0 + cq * CPW;
+                        const int col = n0p + cq * CPW;
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.Y) + grow * p.ldy + col);
 #pragma unroll
                         for (int j = 0; j < CPW / 8; ++j) {
@@ -879,8 +1017,30 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 sc_next2 = next_chunk();
             }
         }
+        // Converted stages are handed to the MMA CONV_BATCH at a time: one proxy
+        // fence (and, for a pair, one cluster-scope release) per batch.  Each costs
+        // a few hundred cycles of the converter's own time, which would otherwise
+        // be paid per K block on the pipeline's critical path.
+        int pend = 0, pend_first = 0;
+        auto flush = [&]() {
+            if (pend == 0) return;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                for (int i = 0, c = pend_first; i < pend; ++i, c = (c + 1 == C::CSTAGES) ? 0 : c + 1) {
+                    // (pair, odd CTA: to the relay thread, which forwards the stage to the
+                    // even CTA's barrier with a cluster-scope release; a converter's own
+                    // cluster-scope release would wait for its scale loads in flight)
+                    if (C::PAIR && crank != 0)
+                        mbar_arrive(&conv_done[c]);
+                    else
+                        mbar_arrive(&full_c[c]);
+                }
+            }
+            pend = 0;
+        };
         // one K block: wait for its raw codes and a free converted stage, expand,
-        // hand the stage to the MMA; false if a wait timed out
+        // hand the stage to the MMA (with its batch); false if a wait timed out
         auto convert_step = [&](uint32_t sbytes) -> bool {
             if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
                 !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY))
@@ -895,9 +1055,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             } else {
                 convert_fp8_rows<C::RPT>(braw, bconv, crow, C::BN / C::RPT);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full_c[cs]);
+            if (pend++ == 0) pend_first = cs;
+            if (pend == C::CONV_BATCH) flush();
             if (++ts == C::TSTAGES) {
                 ts = 0;
                 tph ^= 1u;
@@ -955,6 +1114,9 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 }
             }
         }
+        flush();
+    } else if (C::PAIR && C::RELAYS > 1 && C::relay_slot(warp) > 0) {
+        if (lane == 0 && !pair_leader) relay_stages(C::relay_slot(warp));
     }
 
     __syncthreads();
@@ -963,7 +1125,10 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     if constexpr (C::CLUSTER_N > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 512);
+        if constexpr (C::PAIR)
+            tmem_dealloc_pair(tmem_base, 512);
+        else
+            tmem_dealloc(tmem_base, 512);
     }
 }
 
@@ -1020,7 +1185,7 @@ cudaError_t launch_qgemm(const CUtensorMap& tmA, const CUtensorMap& tmB, GemmPar
             int S = clusters / rem;
             if (S > 8) S = 8;
             if (S > kblocks / 8) S = kblocks / 8;
-            if (S >= 2 && (long)rem * C::CLUSTER_N * S * C::BM * C::BN <= p.split_part_cap) {
+            if (S >= 2 && (long)rem * C::CLUSTER_N * S * C::BM * C::ACC_N <= p.split_part_cap) {
                 p.split_from = full;
                 p.split_S = S;
             }
@@ -1033,9 +1198,10 @@ cudaError_t launch_qgemm(const CUtensorMap& tmA, const CUtensorMap& tmB, GemmPar
     if (e != cudaSuccess) return e;
     if (p.split_S > 1) {
         const int rem = (p.m_tiles * (p.n_tiles / C::CLUSTER_N)) - p.split_from;
-        const long threads = (long)rem * C::CLUSTER_N * C::BM * (C::BN / 4);
+        const long threads = (long)rem * C::CLUSTER_N * C::BM * (C::ACC_N / 4);
         const float scale = (C::EPI == Epi::STORE) ? p.scale2_dense : 1.0f;
-        split_reduce_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, C::BM, C::BN, C::CLUSTER_N, rem, scale);
+        split_reduce_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, C::BM, C::ACC_N, C::CLUSTER_N, rem, scale,
+                                                                             C::PAIR);
     }
     return cudaGetLastError();
 }
