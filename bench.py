@@ -48,7 +48,10 @@ Q8_SHAPE = (2048, 5120, 8064)
 # workload, from one ncu capture (profiles/), with the SHA-256 of the kernel's
 # sources at the time of the capture: the figure is reported only while the
 # sources are unchanged (else null).
-DRAM_TRAFFIC = {}
+DRAM_TRAFFIC = {
+    "down": {"bytes": 243982080 + 30502912, "sources_sha": "a6c76a1e6d02090a"},
+    "gate_up": {"bytes": 399371008 + 63362304, "sources_sha": "34417d211160a7ea"},
+}
 KERNEL_SOURCES = {
     "down": ["csrc/down_iq4.cuh", "csrc/gemm_down.cu", "csrc/qgemm.cuh", "csrc/ptx.cuh"],
     "gate_up": ["csrc/qgemm.cuh", "csrc/gemm_w4.cu", "csrc/ptx.cuh"],
