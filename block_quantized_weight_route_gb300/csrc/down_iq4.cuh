@@ -43,6 +43,9 @@ namespace qmm {
 #ifndef QMM_DOWN_PAIR
 #define QMM_DOWN_PAIR 1
 #endif
+#ifndef QMM_DOWN_CONV4
+#define QMM_DOWN_CONV4 2
+#endif
 template <int EPI_WARPS_, int CONV_WARPS_, int TSTAGES_>
 struct DownCfgT {
     static constexpr int BM = 128, BN = 128, BK = 64, UMMA_K = 16, GROUP_K = 32;
@@ -68,7 +71,7 @@ struct DownCfgT {
         if (warp == 3) return 1;
         if (CONV_WARPS == 4) {
             if (warp == W2) return 2;
-            if (warp == W2 + 2) return 3;
+            if (warp == W2 + QMM_DOWN_CONV4) return 3;
         }
         return -1;
     }
@@ -89,10 +92,21 @@ struct DownCfgT {
     static constexpr int DH_BYTES = KG_MAX * BN * 4;          // d_H of one tile, [block][token] fp32
     static constexpr int DW_BYTES = BM * KG_MAX * 2;          // d_W of one tile, [row][block] fp16
     static constexpr int SSTAGE_BYTES = DH_BYTES + DW_BYTES;
+    // Fused combine, staged: the epilogue leaves a finished tile's y [token][row]
+    // fp32 in shared memory and goes on to the next tile; two combine warps (the
+    // warps without a role under the register split, 13 and 15) add weight x y into
+    // Y[token] with 16-byte reductions while the next tile is folded.
+    static constexpr bool STAGE_Y = REG_SPLIT;
+    static constexpr int YS_BYTES = STAGE_Y ? BN * BM * 4 : 0;
+    __device__ static int comb_slot(int warp) {
+        if (!STAGE_Y) return -1;
+        return warp == W2 + 1 ? 0 : (warp == W2 + 3 ? 1 : -1);
+    }
+    static_assert(!STAGE_Y || QMM_DOWN_CONV4 == 2, "combine warps: the warps after the epilogue without a converter");
     static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, false);
-    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * SSTAGES + 2 * NBUF + 1;   // (NHAND <= NBUF)
+    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * SSTAGES + 2 * NBUF + 3;   // (NHAND <= NBUF)
     static constexpr int SMEM_BYTES = 1024 + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES +
-                                      SSTAGES * SSTAGE_BYTES + BAR_COUNT * 8 + 64;
+                                      SSTAGES * SSTAGE_BYTES + YS_BYTES + BAR_COUNT * 8 + 64;
     static_assert(A_RAW_BYTES % 1024 == 0 && TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0 &&
                       SSTAGE_BYTES % 1024 == 0,
                   "align");
@@ -111,7 +125,7 @@ struct DownCfgT {
 #define QMM_DOWN_CONV_WARPS 4
 #endif
 #ifndef QMM_DOWN_TSTAGES
-#define QMM_DOWN_TSTAGES 5
+#define QMM_DOWN_TSTAGES 4
 #endif
 using DownCfg = DownCfgT<QMM_DOWN_EPI_WARPS, QMM_DOWN_CONV_WARPS, QMM_DOWN_TSTAGES>;
 
@@ -121,6 +135,11 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
                      smem_u32(smem_dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
+}
+
+// p[0..3] += {a, b, c, d} as one 16-byte fp32 reduction in L2 (p 16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t saddr) {
@@ -147,7 +166,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint8_t* tstage = smem;
     uint8_t* cstage = tstage + C::TSTAGES * C::TSTAGE_BYTES;
     uint8_t* sstage = cstage + C::CSTAGES * C::CSTAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sstage + C::SSTAGES * C::SSTAGE_BYTES);
+    float* ystage = reinterpret_cast<float*>(sstage + C::SSTAGES * C::SSTAGE_BYTES);   // [token][row], STAGE_Y
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sstage + C::SSTAGES * C::SSTAGE_BYTES + C::YS_BYTES);
     uint64_t* full_t = bars;
     uint64_t* empty_t = full_t + C::TSTAGES;
     uint64_t* full_c = empty_t + C::TSTAGES;
@@ -157,7 +177,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint64_t* acc_full = empty_s + C::SSTAGES;
     uint64_t* acc_empty = acc_full + C::NHAND;
     uint64_t* drain_bar = acc_empty + C::NHAND;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    uint64_t* y_full = drain_bar + 1;      // a tile's y staged (epilogue warps)
+    uint64_t* y_empty = y_full + 1;        // the stage read (combine warps)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(y_empty + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -180,6 +202,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(&acc_empty[i], C::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(y_full, C::EPI_WARPS);
+        mbar_init(y_empty, 2);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -209,7 +233,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int r = q * 32 + lane;                            // this thread's weight row in the tile
         const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
         int buf = 0, ss = 0;
-        uint32_t bph = 0, sph = 0;
+        uint32_t bph = 0, sph = 0, yph = 0;
         bool ok = true;
         int4 g4 = (int)blockIdx.x < num_tiles ? p.tiles[blockIdx.x / p.n_tiles] : make_int4(0, 0, 0, 0);
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -296,6 +320,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = y[j].x;
                     if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = y[j].y;
                 }
+            } else if constexpr (C::STAGE_Y) {
+                // this warp's token columns of y into the stage, [token][row]: lanes write
+                // 32 consecutive rows (conflict-free); the stage must have been read out
+                if (!mbar_wait(y_empty, yph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC)) break;
+#pragma unroll
+                for (int j = 0; j < C::CPW / 2; ++j) {
+                    ystage[(tok0 + 2 * j) * C::BM + r] = y[j].x;
+                    ystage[(tok0 + 2 * j + 1) * C::BM + r] = y[j].y;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(y_full);
+                yph ^= 1u;
             } else {
                 // Y[token, n] += weight * y for this warp's token columns: lane l holds the
                 // token and weight of columns l, l+32, ...; each column's pair is broadcast
@@ -469,6 +505,44 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 drain_ring(drain_bar, 1, 1, p.err);
             }
             __syncwarp();
+        } else if (COMBINE && C::comb_slot(warp) >= 0) {
+            // ------------------------------------------------------------ combine warps (staged y)
+            // warp cw takes tokens [64 cw, 64 cw + 64) of each tile: Y[token][n0 + 4 lane ..]
+            // += weight * y[token][4 lane ..] as one 16-byte reduction per lane and token
+            const int cw = C::comb_slot(warp);
+            uint32_t yph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const int entry = t / p.n_tiles;
+                const int n0 = (t - entry * p.n_tiles) * C::BM;
+                const int4 g4 = p.tiles[entry];
+                int tk[2];
+                float wt[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int c = cw * 64 + 32 * i + lane;
+                    tk[i] = c < g4.z ? __ldg(p.src + g4.y + c) : 0;
+                    wt[i] = c < g4.z ? __ldg(p.wrow + g4.y + c) : 0.f;
+                }
+                if (!mbar_wait(y_full, yph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                    ok = false;
+                    break;
+                }
+                float* ybase = static_cast<float*>(p.Y) + n0 + 4 * lane;
+                const uint32_t ys = smem_u32(ystage) + (uint32_t)(lane * 16);
+                const int ncol = min(64, g4.z - cw * 64);
+#pragma unroll 4
+                for (int c = 0; c < ncol; ++c) {
+                    const int tok = __shfl_sync(0xffffffffu, tk[c >> 5], c & 31);
+                    const float wc = __shfl_sync(0xffffffffu, wt[c >> 5], c & 31);
+                    const uint4 v = lds128(ys + (uint32_t)((cw * 64 + c) * C::BM * 4));
+                    red_add_v4(ybase + (long)tok * p.ldy, wc * __uint_as_float(v.x), wc * __uint_as_float(v.y),
+                               wc * __uint_as_float(v.z), wc * __uint_as_float(v.w));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(y_empty);
+                yph ^= 1u;
+            }
         } else if (C::conv_slot(warp) >= 0) {
             // ------------------------------------------------------------ converters (IQ4 indices -> f16)
             const int ct = C::conv_slot(warp) * 32 + lane;
