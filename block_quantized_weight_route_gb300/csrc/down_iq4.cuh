@@ -28,6 +28,8 @@
 //   warps 4 .. 4+EPI_WARPS-1: epilogue (EPI_WARPS/4 per TMEM lane quarter)
 //   warps 1, 3 (and with four converters two more after the epilogue, on
 //   sub-partitions 0 and 2): IQ4 converters; warp 1 also allocates TMEM.
+//   With four converters and the fused combine, the remaining two warps after
+//   the epilogue (sub-partitions 1 and 3) add each staged tile into Y.
 // A warp's SM sub-partition is its index mod 4, the same as the TMEM lane
 // quarter it may read, so every sub-partition holds EPI_WARPS/4 epilogue warps
 // and one of the producer, a converter or the MMA issuer.  The producer and
@@ -38,7 +40,7 @@
 namespace qmm {
 
 #ifndef QMM_DOWN_CSTAGES
-#define QMM_DOWN_CSTAGES 2
+#define QMM_DOWN_CSTAGES 3
 #endif
 #ifndef QMM_DOWN_PAIR
 #define QMM_DOWN_PAIR 1
@@ -92,10 +94,11 @@ struct DownCfgT {
     static constexpr int DH_BYTES = KG_MAX * BN * 4;          // d_H of one tile, [block][token] fp32
     static constexpr int DW_BYTES = BM * KG_MAX * 2;          // d_W of one tile, [row][block] fp16
     static constexpr int SSTAGE_BYTES = DH_BYTES + DW_BYTES;
-    // Fused combine, staged: the epilogue leaves a finished tile's y [token][row]
+    // Staged tile outputs: the epilogue leaves a finished tile's y [token][row]
     // fp32 in shared memory and goes on to the next tile; two combine warps (the
     // warps without a role under the register split, 13 and 15) add weight x y into
-    // Y[token] with 16-byte reductions while the next tile is folded.
+    // Y[token] with 16-byte reductions (per-slot form: store the rows of Yslot)
+    // while the next tile is folded.
     static constexpr bool STAGE_Y = REG_SPLIT;
     static constexpr int YS_BYTES = STAGE_Y ? BN * BM * 4 : 0;
     __device__ static int comb_slot(int warp) {
@@ -115,9 +118,9 @@ struct DownCfgT {
 // Measured on the 5268-token stage (down with the fused combine): 8 epilogue
 // warps (64 token columns each, both TMEM loads of a block issued before one
 // wait), 4 converters under the register split, accumulators handed over in
-// pairs, 5 TMA and 2 converted stages: 0.506 ms, against 0.519 ms with 2
-// converters and 0.530 ms with 2 converters and one hand-off per block (16
-// epilogue warps were slower still).
+// pairs, the staged combine, 3 TMA and 3 expanded-weight stages: 0.404 ms
+// (4 + 2 stages: 0.412; before the staged combine, 5 + 2 stages: 0.506; with 2
+// converters and one hand-off per block: 0.530; 16 epilogue warps were slower).
 #ifndef QMM_DOWN_EPI_WARPS
 #define QMM_DOWN_EPI_WARPS 8
 #endif
@@ -125,7 +128,7 @@ struct DownCfgT {
 #define QMM_DOWN_CONV_WARPS 4
 #endif
 #ifndef QMM_DOWN_TSTAGES
-#define QMM_DOWN_TSTAGES 4
+#define QMM_DOWN_TSTAGES 3
 #endif
 using DownCfg = DownCfgT<QMM_DOWN_EPI_WARPS, QMM_DOWN_CONV_WARPS, QMM_DOWN_TSTAGES>;
 
@@ -312,15 +315,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             if (!ok) break;
             const int tok0 = cq * C::CPW;
-            if constexpr (!COMBINE) {
-                // Yslot[row, n] for this warp's token columns; lanes write consecutive n
-                float* out = static_cast<float*>(p.Y) + (long)g4.y * p.ldy + n0 + r;
-#pragma unroll
-                for (int j = 0; j < C::CPW / 2; ++j) {
-                    if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = y[j].x;
-                    if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = y[j].y;
-                }
-            } else if constexpr (C::STAGE_Y) {
+            if constexpr (C::STAGE_Y) {
                 // this warp's token columns of y into the stage, [token][row]: lanes write
                 // 32 consecutive rows (conflict-free); the stage must have been read out
                 if (!mbar_wait(y_empty, yph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC)) break;
@@ -332,6 +327,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(y_full);
                 yph ^= 1u;
+            } else if constexpr (!COMBINE) {
+                // Yslot[row, n] for this warp's token columns; lanes write consecutive n
+                float* out = static_cast<float*>(p.Y) + (long)g4.y * p.ldy + n0 + r;
+#pragma unroll
+                for (int j = 0; j < C::CPW / 2; ++j) {
+                    if (tok0 + 2 * j < g4.z) out[(long)(tok0 + 2 * j) * p.ldy] = y[j].x;
+                    if (tok0 + 2 * j + 1 < g4.z) out[(long)(tok0 + 2 * j + 1) * p.ldy] = y[j].y;
+                }
             } else {
                 // Y[token, n] += weight * y for this warp's token columns: lane l holds the
                 // token and weight of columns l, l+32, ...; each column's pair is broadcast
@@ -505,10 +508,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 drain_ring(drain_bar, 1, 1, p.err);
             }
             __syncwarp();
-        } else if (COMBINE && C::comb_slot(warp) >= 0) {
+        } else if (C::comb_slot(warp) >= 0) {
             // ------------------------------------------------------------ combine warps (staged y)
             // warp cw takes tokens [64 cw, 64 cw + 64) of each tile: Y[token][n0 + 4 lane ..]
-            // += weight * y[token][4 lane ..] as one 16-byte reduction per lane and token
+            // += weight * y[token][4 lane ..] as one 16-byte reduction per lane and token, or
+            // (per-slot form) Yslot[row][n0 + 4 lane ..] = y[token][4 lane ..]
             const int cw = C::comb_slot(warp);
             uint32_t yph = 0;
             bool ok = true;
@@ -516,13 +520,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int entry = t / p.n_tiles;
                 const int n0 = (t - entry * p.n_tiles) * C::BM;
                 const int4 g4 = p.tiles[entry];
-                int tk[2];
-                float wt[2];
+                int tk[2] = {0, 0};
+                float wt[2] = {0.f, 0.f};
+                if constexpr (COMBINE) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int c = cw * 64 + 32 * i + lane;
-                    tk[i] = c < g4.z ? __ldg(p.src + g4.y + c) : 0;
-                    wt[i] = c < g4.z ? __ldg(p.wrow + g4.y + c) : 0.f;
+                    for (int i = 0; i < 2; ++i) {
+                        const int c = cw * 64 + 32 * i + lane;
+                        tk[i] = c < g4.z ? __ldg(p.src + g4.y + c) : 0;
+                        wt[i] = c < g4.z ? __ldg(p.wrow + g4.y + c) : 0.f;
+                    }
                 }
                 if (!mbar_wait(y_full, yph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
                     ok = false;
@@ -533,11 +539,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int ncol = min(64, g4.z - cw * 64);
 #pragma unroll 4
                 for (int c = 0; c < ncol; ++c) {
-                    const int tok = __shfl_sync(0xffffffffu, tk[c >> 5], c & 31);
-                    const float wc = __shfl_sync(0xffffffffu, wt[c >> 5], c & 31);
                     const uint4 v = lds128(ys + (uint32_t)((cw * 64 + c) * C::BM * 4));
-                    red_add_v4(ybase + (long)tok * p.ldy, wc * __uint_as_float(v.x), wc * __uint_as_float(v.y),
-                               wc * __uint_as_float(v.z), wc * __uint_as_float(v.w));
+                    if constexpr (COMBINE) {
+                        const int tok = __shfl_sync(0xffffffffu, tk[c >> 5], c & 31);
+                        const float wc = __shfl_sync(0xffffffffu, wt[c >> 5], c & 31);
+                        red_add_v4(ybase + (long)tok * p.ldy, wc * __uint_as_float(v.x), wc * __uint_as_float(v.y),
+                                   wc * __uint_as_float(v.z), wc * __uint_as_float(v.w));
+                    } else {
+                        *reinterpret_cast<uint4*>(ybase + (long)(g4.y + cw * 64 + c) * p.ldy) = v;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(y_empty);
