@@ -24,17 +24,36 @@
 //
 //   warp 0: TMA producer (Q8_0 codes + f16 activation codes per K step of 64,
 //           scale chunks); warp 2: MMA issuer; warps 1, 3: int8 -> f16 converters;
-//   warps 4..11: epilogue (two per TMEM lane quarter, 64 token columns each).
+//   warps 4..11: epilogue (two per TMEM lane quarter, 64 token columns each),
+//           accumulators handed over two 32-K blocks at a time;
+//   warps 12..15: the q8_1 rounding of each finished tile, which the epilogue
+//           leaves in shared memory before it goes on to the next tile.
 #include "down_iq4.cuh"
 
 namespace qmm {
 
+#ifndef QMM_Q8_TSTAGES
+#define QMM_Q8_TSTAGES 3
+#endif
+#ifndef QMM_Q8_CSTAGES
+#define QMM_Q8_CSTAGES 3
+#endif
 struct Q8Cfg {
     static constexpr int BM = 128, BN = 128, BK = 64, GROUP_K = 32;
     static constexpr int EPI_WARPS = 8, EPI_BASE = 4, CPW = 64, CONV_WARPS = 2;
-    static constexpr int THREADS = 32 * (EPI_BASE + EPI_WARPS);
+    // 16 warps launched at 128 registers a thread: the two epilogue warpgroups
+    // raised to 168 (running sums + two 32-column loads), the other two lowered to
+    // 88 - the shares add up to exactly the launch's 16 x 128.  Warps 12..15 round
+    // each finished tile, staged in shared memory, to q8_1 while the epilogue
+    // folds the next tile.
+    static constexpr int THREADS = 512, QUANT_BASE = 12, QUANT_WARPS = 4;
+    static constexpr int REGS_LAUNCH = 128, REGS_EPI = 168, REGS_OTHER = 88;
+    static_assert(8 * REGS_EPI + 8 * REGS_OTHER == 16 * REGS_LAUNCH, "register shares = launch registers");
     static constexpr int MMA_WARP = 2;
-    static constexpr int TSTAGES = 4, CSTAGES = 2, SSTAGES = 2, NBUF = 4;
+    static constexpr int TSTAGES = QMM_Q8_TSTAGES, CSTAGES = QMM_Q8_CSTAGES, SSTAGES = 2, NBUF = 4;
+    // the accumulators of a K step's two 32-K blocks are handed over together (one
+    // commit, one wait and one release per pair of TMEM buffers)
+    static constexpr int NHAND = NBUF / 2;
     static constexpr int TMA_GROUPS = TSTAGES;
     static constexpr int CHUNK_STEPS = 4;                         // K steps of 64 per scale chunk
     static constexpr int CHUNK_BLOCKS = CHUNK_STEPS * BK / GROUP_K;   // 8 blocks of 32
@@ -46,9 +65,10 @@ struct Q8Cfg {
     static constexpr int DW_BYTES = BM * CHUNK_BLOCKS * 2;        // [row][block] fp16
     static constexpr int SSTAGE_BYTES = 8192;                     // DX + DW, padded to 1 KB multiples
     static constexpr uint32_t IDESC = idesc_kind_f16(BM, BN, false);
-    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * SSTAGES + 2 * NBUF + 1;
+    static constexpr int YS_BYTES = BN * BM * 4;                  // a finished tile, [token][row] fp32
+    static constexpr int BAR_COUNT = 2 * TSTAGES + 2 * CSTAGES + 2 * SSTAGES + 2 * NBUF + 3;   // (NHAND <= NBUF)
     static constexpr int SMEM_BYTES = 1024 + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES +
-                                      SSTAGES * SSTAGE_BYTES + BAR_COUNT * 8 + 64;
+                                      SSTAGES * SSTAGE_BYTES + YS_BYTES + BAR_COUNT * 8 + 64;
     static_assert(DX_BYTES + DW_BYTES <= SSTAGE_BYTES, "scale stage");
     static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0 && SSTAGE_BYTES % 1024 == 0, "align");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -100,7 +120,8 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
     uint8_t* tstage = smem;
     uint8_t* cstage = tstage + C::TSTAGES * C::TSTAGE_BYTES;
     uint8_t* sstage = cstage + C::CSTAGES * C::CSTAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sstage + C::SSTAGES * C::SSTAGE_BYTES);
+    float* ystage = reinterpret_cast<float*>(sstage + C::SSTAGES * C::SSTAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sstage + C::SSTAGES * C::SSTAGE_BYTES + C::YS_BYTES);
     uint64_t* full_t = bars;
     uint64_t* empty_t = full_t + C::TSTAGES;
     uint64_t* full_c = empty_t + C::TSTAGES;
@@ -108,9 +129,11 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
     uint64_t* full_s = empty_c + C::CSTAGES;
     uint64_t* empty_s = full_s + C::SSTAGES;
     uint64_t* acc_full = empty_s + C::SSTAGES;
-    uint64_t* acc_empty = acc_full + C::NBUF;
-    uint64_t* drain_bar = acc_empty + C::NBUF;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    uint64_t* acc_empty = acc_full + C::NHAND;
+    uint64_t* drain_bar = acc_empty + C::NHAND;
+    uint64_t* y_full = drain_bar + 1;      // a finished tile staged (epilogue warps)
+    uint64_t* y_empty = y_full + 1;        // the stage read (q8_1 warps)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(y_empty + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -127,11 +150,13 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
             mbar_init(&full_s[i], 1);
             mbar_init(&empty_s[i], C::EPI_WARPS);
         }
-        for (int i = 0; i < C::NBUF; ++i) {
+        for (int i = 0; i < C::NHAND; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], C::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(y_full, C::EPI_WARPS);
+        mbar_init(y_empty, C::QUANT_WARPS);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -152,7 +177,102 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
     const int entries = min(*p.num_entries, p.max_entries);
     const int num_tiles = entries * p.n_tiles;
 
-    if (warp == 0) {
+    // Roles.  Each warpgroup runs exactly one setmaxnreg (the epilogue warpgroups
+    // the inc, the others the dec), at the top of the code it governs.
+    if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
+        setmaxnreg_inc<C::REGS_EPI>();
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int cq = (warp - C::EPI_BASE) >> 2;   // this warp's block of 64 token columns
+        const int r = q * 32 + lane;                 // this thread's weight row in the tile
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+        int buf = 0, ss = 0;
+        uint32_t bph = 0, sph = 0, yph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            float2 y[C::CPW / 2];
+#pragma unroll
+            for (int j = 0; j < C::CPW / 2; ++j) y[j] = make_float2(0.f, 0.f);
+            for (int kc = 0; kc < nchunks && ok; ++kc) {
+                if (!mbar_wait(&full_s[ss], sph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sbase = smem_u32(sstage + ss * C::SSTAGE_BYTES);
+                const uint32_t dh_base = sbase + cq * C::CPW * 4;
+                const uint32_t dw_row = sbase + C::DX_BYTES + r * 16;   // this row's 8 block scales
+#pragma unroll 1
+                for (int gi = 0; gi < C::CHUNK_BLOCKS; gi += 2) {
+                    if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        const float dwf = __half2float(__ushort_as_half((unsigned short)lds_u16(dw_row + (gi + h) * 2)));
+                        const float2 dw2 = make_float2(dwf, dwf);
+                        const uint32_t acc = lane_addr + (uint32_t)((2 * buf + h) * C::BN + cq * C::CPW);
+                        uint32_t v[2][32];
+                        tmem_ld32(acc, v[0]);
+                        tmem_ld32(acc + 32, v[1]);
+                        tmem_ld_wait();
+                        if (h == 1) {
+                            // both blocks of the pair read: the buffers go back
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                        }
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint4 dh = lds128(dh_base + (uint32_t)(((gi + h) * C::BN + c * 32 + 4 * j) * 4));
+                                const float2 i01 =
+                                    make_float2(__uint_as_float(v[c][4 * j]), __uint_as_float(v[c][4 * j + 1]));
+                                const float2 i23 =
+                                    make_float2(__uint_as_float(v[c][4 * j + 2]), __uint_as_float(v[c][4 * j + 3]));
+                                const float2 d01 = make_float2(__uint_as_float(dh.x), __uint_as_float(dh.y));
+                                const float2 d23 = make_float2(__uint_as_float(dh.z), __uint_as_float(dh.w));
+                                // y += (I * d_X) * d_W, both products rounded to fp32
+                                float2& y01 = y[c * 16 + 2 * j];
+                                float2& y23 = y[c * 16 + 2 * j + 1];
+                                y01 = __ffma2_rn(__fmul2_rn(i01, d01), dw2, y01);
+                                y23 = __ffma2_rn(__fmul2_rn(i23, d23), dw2, y23);
+                            }
+                        }
+                    }
+                    if (++buf == C::NHAND) {
+                        buf = 0;
+                        bph ^= 1u;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_s[ss]);
+                if (++ss == C::SSTAGES) {
+                    ss = 0;
+                    sph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            // the finished tile into the stage, [token][row] (lanes write 32 consecutive
+            // rows: conflict-free), once the q8_1 warps have read the previous one
+            if (!mbar_wait(y_empty, yph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC)) break;
+            {
+                const int tok0 = cq * C::CPW;
+#pragma unroll
+                for (int j = 0; j < C::CPW / 2; ++j) {
+                    ystage[(tok0 + 2 * j) * C::BM + r] = y[j].x;
+                    ystage[(tok0 + 2 * j + 1) * C::BM + r] = y[j].y;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(y_full);
+            yph ^= 1u;
+        }
+    } else {
+        setmaxnreg_dec<C::REGS_OTHER>();
+        if (warp == 0) {
         // ------------------------------------------------------------ producer (one warp)
         // Each copy of a stage comes from its own lane (a thread has one TMA copy
         // executing at a time); scale chunks from lanes 30 and 31.
@@ -213,7 +333,7 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
             drain_ring(full_s, s_issued, C::SSTAGES, p.err);
         }
         __syncwarp();
-    } else if (warp == C::MMA_WARP) {
+        } else if (warp == C::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer (one lane)
         if (lane == 0) {
             int cs = 0, ts = 0, buf = 0;
@@ -229,25 +349,25 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
                     }
                     const uint64_t ad = smem_desc_sw128(smem_u32(cstage + cs * C::CSTAGE_BYTES));
                     const uint64_t bd = smem_desc_sw128(smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES);
+                    // the step's two 32-K blocks, each into its own accumulator: the two
+                    // buffers of hand-off pair buf
+                    if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
                     for (int h = 0; h < C::BK / C::GROUP_K; ++h) {
-                        // one 32-K block: two K=16 MMAs into its own accumulator
-                        if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::BN);
+                        const uint32_t dtmem = tmem_base + (uint32_t)((2 * buf + h) * C::BN);
                         // descriptor start addresses in 16-byte units: 64 bytes per 32-K block
                         tc_mma_f16(dtmem, ad + (uint64_t)(h * 4), bd + (uint64_t)(h * 4), C::IDESC, 0u);
                         tc_mma_f16(dtmem, ad + (uint64_t)(h * 4 + 2), bd + (uint64_t)(h * 4 + 2), C::IDESC, 1u);
-                        tc_commit(&acc_full[buf]);
-                        if (++buf == C::NBUF) {
-                            buf = 0;
-                            bph ^= 1u;
-                        }
                     }
-                    if (!ok) break;
+                    tc_commit(&acc_full[buf]);
+                    if (++buf == C::NHAND) {
+                        buf = 0;
+                        bph ^= 1u;
+                    }
                     tc_commit(&empty_c[cs]);
                     tc_commit(&empty_t[ts]);
                     if (++cs == C::CSTAGES) {
@@ -261,104 +381,7 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
             drain_ring(drain_bar, 1, 1, p.err);
         }
         __syncwarp();
-    } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
-        // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;
-        const int cq = (warp - C::EPI_BASE) >> 2;   // this warp's block of 64 token columns
-        const int r = q * 32 + lane;                 // this thread's weight row in the tile
-        const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
-        int buf = 0, ss = 0;
-        uint32_t bph = 0, sph = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const int entry = t / p.n_tiles;
-            const int n0 = (t - entry * p.n_tiles) * C::BM;
-            const int4 g4 = p.tiles[entry];
-            float2 y[C::CPW / 2];
-#pragma unroll
-            for (int j = 0; j < C::CPW / 2; ++j) y[j] = make_float2(0.f, 0.f);
-            for (int kc = 0; kc < nchunks && ok; ++kc) {
-                if (!mbar_wait(&full_s[ss], sph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t sbase = smem_u32(sstage + ss * C::SSTAGE_BYTES);
-                const uint32_t dh_base = sbase + cq * C::CPW * 4;
-                const uint32_t dw_row = sbase + C::DX_BYTES + r * 16;   // this row's 8 block scales
-#pragma unroll 1
-                for (int gi = 0; gi < C::CHUNK_BLOCKS; ++gi) {
-                    if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const float dwf = __half2float(__ushort_as_half((unsigned short)lds_u16(dw_row + gi * 2)));
-                    const float2 dw2 = make_float2(dwf, dwf);
-                    const uint32_t acc = lane_addr + (uint32_t)(buf * C::BN + cq * C::CPW);
-                    uint32_t v[2][32];
-                    tmem_ld32(acc, v[0]);
-                    tmem_ld32(acc + 32, v[1]);
-                    tmem_ld_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[buf]);
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint4 dh = lds128(dh_base + (uint32_t)((gi * C::BN + c * 32 + 4 * j) * 4));
-                            const float2 i01 = make_float2(__uint_as_float(v[c][4 * j]), __uint_as_float(v[c][4 * j + 1]));
-                            const float2 i23 =
-                                make_float2(__uint_as_float(v[c][4 * j + 2]), __uint_as_float(v[c][4 * j + 3]));
-                            const float2 d01 = make_float2(__uint_as_float(dh.x), __uint_as_float(dh.y));
-                            const float2 d23 = make_float2(__uint_as_float(dh.z), __uint_as_float(dh.w));
-                            // y += (I * d_X) * d_W, both products rounded to fp32
-                            float2& y01 = y[c * 16 + 2 * j];
-                            float2& y23 = y[c * 16 + 2 * j + 1];
-                            y01 = __ffma2_rn(__fmul2_rn(i01, d01), dw2, y01);
-                            y23 = __ffma2_rn(__fmul2_rn(i23, d23), dw2, y23);
-                        }
-                    }
-                    if (++buf == C::NBUF) {
-                        buf = 0;
-                        bph ^= 1u;
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty_s[ss]);
-                if (++ss == C::SSTAGES) {
-                    ss = 0;
-                    sph ^= 1u;
-                }
-            }
-            if (!ok) break;
-            // q8_1 rounding of each token row's 32 columns n0 + 32q .. +31 (this warp's
-            // lanes): d = max|y|/127, q = round-half-away(y/d) clamped to +-127, s = d * sum q
-            const int tok0 = cq * C::CPW;
-            const int ncol = n0 + r;
-            const int nblk = (n0 >> 5) + q;
-#pragma unroll
-            for (int c = 0; c < C::CPW; ++c) {
-                if (tok0 + c >= g4.z) continue;   // warp-uniform
-                const float yv = (c & 1) ? y[c >> 1].y : y[c >> 1].x;
-                const long m = (long)g4.y + tok0 + c;
-                const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(yv))));
-                float d = 0.f, qf = 0.f;
-                if (amax > 0.f) {
-                    d = amax / 127.0f;
-                    qf = fminf(fmaxf(roundf(yv / d), -127.f), 127.f);
-                }
-                const int qi = (int)qf;
-                const int sum = __reduce_add_sync(0xffffffffu, qi);
-                o.Yq[m * p.N + ncol] = (int8_t)qi;
-                if (lane == 0) {
-                    o.Yd[m * (p.N / 32) + nblk] = __float2half_rn(d);
-                    o.Ys[m * (p.N / 32) + nblk] = __float2half_rn(d * (float)sum);
-                }
-                if (o.Y) o.Y[m * p.N + ncol] = yv;
-            }
-        }
-    } else if (warp == 1 || warp == 3) {
+        } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------------------ converters (int8 -> f16)
         const int ct = (warp == 1 ? 0 : 1) * 32 + lane;
         int ts = 0, cs = 0;
@@ -391,6 +414,59 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
                 }
             }
         }
+            } else if (warp >= C::QUANT_BASE) {
+            // ---------------------------------------------------------- q8_1 rounding of the staged tile
+            // warp w takes tokens [32 w, 32 w + 32); lane l holds n0 + 4l .. 4l + 3 of a token
+            // row, so each block of 32 outputs is 8 lanes: d = max|y|/127, q =
+            // round-half-away(y/d) clamped to +-127, s = d * sum q
+            const int qw = warp - C::QUANT_BASE;
+            uint32_t yph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const int entry = t / p.n_tiles;
+                const int n0 = (t - entry * p.n_tiles) * C::BM;
+                const int4 g4 = p.tiles[entry];
+                if (!mbar_wait(y_full, yph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                    ok = false;
+                    break;
+                }
+                const int ncol = n0 + 4 * lane;
+                const int nblk = (n0 >> 5) + (lane >> 3);
+                const int cend = min(32, g4.z - 32 * qw);
+#pragma unroll 2
+                for (int c = 0; c < cend; ++c) {
+                    const int tok = 32 * qw + c;
+                    const uint4 u = lds128(smem_u32(ystage) + (uint32_t)((tok * C::BM + 4 * lane) * 4));
+                    const float v[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                        __uint_as_float(u.w)};
+                    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+                    for (int sh = 1; sh < 8; sh <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+                    float d = 0.f;
+                    int qi[4] = {0, 0, 0, 0};
+                    if (amax > 0.f) {
+                        d = amax / 127.0f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) qi[i] = (int)fminf(fmaxf(roundf(v[i] / d), -127.f), 127.f);
+                    }
+                    int sum = qi[0] + qi[1] + qi[2] + qi[3];
+#pragma unroll
+                    for (int sh = 1; sh < 8; sh <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+                    const long m = (long)g4.y + tok;
+                    const uint32_t packed = (uint32_t)(qi[0] & 0xFF) | ((uint32_t)(qi[1] & 0xFF) << 8) |
+                                            ((uint32_t)(qi[2] & 0xFF) << 16) | ((uint32_t)(qi[3] & 0xFF) << 24);
+                    *reinterpret_cast<uint32_t*>(o.Yq + m * p.N + ncol) = packed;
+                    if ((lane & 7) == 0) {
+                        o.Yd[m * (p.N / 32) + nblk] = __float2half_rn(d);
+                        o.Ys[m * (p.N / 32) + nblk] = __float2half_rn(d * (float)sum);
+                    }
+                    if (o.Y) *reinterpret_cast<uint4*>(o.Y + m * p.N + ncol) = u;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(y_empty);
+                yph ^= 1u;
+            }
+        }
     }
 
     __syncthreads();
@@ -420,6 +496,13 @@ cudaError_t launch_q8_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
     cudaError_t e =
         cudaFuncSetAttribute(q8_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Q8Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // the warpgroups' register shares add up to 128 a thread: launch only if the
+    // kernel is allocated exactly that many (more shares than the pool would leave
+    // a setmaxnreg.inc waiting)
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, q8_dense_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != Q8Cfg::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
     Q8Out o{Yq, Yd, Ys, Y, M};
     q8_dense_kernel<<<grid, Q8Cfg::THREADS, Q8Cfg::SMEM_BYTES, s>>>(tmA, tmB, tmW, p, o);
     return cudaGetLastError();
