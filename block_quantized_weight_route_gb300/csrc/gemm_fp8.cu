@@ -9,8 +9,11 @@ namespace qmm {
 // halves the E4M3 -> bf16 conversion per FLOP; the fold then needs 16 epilogue
 // warps so that the two sub-tiles' running sums fit in registers, and two
 // converter warps expand two weight rows per thread.
+#ifndef QMM_FP8_CONV
+#define QMM_FP8_CONV 4
+#endif
 template <int CN>
-using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 2, 16, 4, 4, false, CN, 2>;
+using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, QMM_FP8_CONV, 16, 4, 4, false, CN, 2>;
 // CTA pair: 256 x 256 tiles, each CTA 128 token rows and 128 weight rows (one
 // 128 x 128 scale block), the fold over its 128 rows x both CTAs' columns.
 using CfgFp8Pair = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 2, 16, 5, 4, false, 2, 1, true>;

@@ -273,148 +273,148 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
     } else {
         setmaxnreg_dec<C::REGS_OTHER>();
         if (warp == 0) {
-        // ------------------------------------------------------------ producer (one warp)
-        // Each copy of a stage comes from its own lane (a thread has one TMA copy
-        // executing at a time); scale chunks from lanes 30 and 31.
-        int s = 0, ss = 0;
-        uint32_t ph = 0, sph = 0;
-        long issued = 0, s_issued = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const int entry = t / p.n_tiles;
-            const int n0 = (t - entry * p.n_tiles) * C::BM;
-            const int4 g = p.tiles[entry];
-            for (int kc = 0; kc < nchunks && ok; ++kc) {
-                const bool got_s = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
-                if (__any_sync(0xffffffffu, !got_s)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* sst = sstage + ss * C::SSTAGE_BYTES;
-                if (lane == 30) mbar_arrive_expect_tx(&full_s[ss], C::DX_BYTES + C::DW_BYTES);
-                __syncwarp();
-                if (lane == 30)
-                    bulk_load(sst, p.dH32 + ((long)entry * groups + kc * C::CHUNK_BLOCKS) * C::BN, C::DX_BYTES,
-                              &full_s[ss]);
-                else if (lane == 31)
-                    tma_load_2d(sst + C::DX_BYTES, &tmW, &full_s[ss], kc * C::CHUNK_BLOCKS, n0);
-                __syncwarp();
-                ++s_issued;
-                if (++ss == C::SSTAGES) {
-                    ss = 0;
-                    sph ^= 1u;
-                }
-                for (int kq = 0; kq < C::CHUNK_STEPS; ++kq) {
-                    const int kb = kc * C::CHUNK_STEPS + kq;
-                    const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
-                    if (__any_sync(0xffffffffu, !got)) {
+            // ------------------------------------------------------------ producer (one warp)
+            // Each copy of a stage comes from its own lane (a thread has one TMA copy
+            // executing at a time); scale chunks from lanes 30 and 31.
+            int s = 0, ss = 0;
+            uint32_t ph = 0, sph = 0;
+            long issued = 0, s_issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const int entry = t / p.n_tiles;
+                const int n0 = (t - entry * p.n_tiles) * C::BM;
+                const int4 g = p.tiles[entry];
+                for (int kc = 0; kc < nchunks && ok; ++kc) {
+                    const bool got_s = mbar_wait(&empty_s[ss], sph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                    if (__any_sync(0xffffffffu, !got_s)) {
                         ok = false;
                         break;
                     }
-                    const int l0 = 2 * (s % C::TMA_GROUPS);
-                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                    if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                    uint8_t* sst = sstage + ss * C::SSTAGE_BYTES;
+                    if (lane == 30) mbar_arrive_expect_tx(&full_s[ss], C::DX_BYTES + C::DW_BYTES);
                     __syncwarp();
-                    if (lane == l0)
-                        tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, n0);
-                    else if (lane == l0 + 1)
-                        tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
+                    if (lane == 30)
+                        bulk_load(sst, p.dH32 + ((long)entry * groups + kc * C::CHUNK_BLOCKS) * C::BN, C::DX_BYTES,
+                                  &full_s[ss]);
+                    else if (lane == 31)
+                        tma_load_2d(sst + C::DX_BYTES, &tmW, &full_s[ss], kc * C::CHUNK_BLOCKS, n0);
                     __syncwarp();
-                    ++issued;
-                    if (++s == C::TSTAGES) {
-                        s = 0;
-                        ph ^= 1u;
+                    ++s_issued;
+                    if (++ss == C::SSTAGES) {
+                        ss = 0;
+                        sph ^= 1u;
+                    }
+                    for (int kq = 0; kq < C::CHUNK_STEPS; ++kq) {
+                        const int kb = kc * C::CHUNK_STEPS + kq;
+                        const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                        if (__any_sync(0xffffffffu, !got)) {
+                            ok = false;
+                            break;
+                        }
+                        const int l0 = 2 * (s % C::TMA_GROUPS);
+                        uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                        if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                        __syncwarp();
+                        if (lane == l0)
+                            tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, n0);
+                        else if (lane == l0 + 1)
+                            tma_load_2d(st + C::A_RAW_BYTES, &tmB, &full_t[s], kb * C::BK, g.y);
+                        __syncwarp();
+                        ++issued;
+                        if (++s == C::TSTAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
                     }
                 }
             }
-        }
-        if (lane == 0) {
-            drain_ring(full_t, issued, C::TSTAGES, p.err);
-            drain_ring(full_s, s_issued, C::SSTAGES, p.err);
-        }
-        __syncwarp();
+            if (lane == 0) {
+                drain_ring(full_t, issued, C::TSTAGES, p.err);
+                drain_ring(full_s, s_issued, C::SSTAGES, p.err);
+            }
+            __syncwarp();
         } else if (warp == C::MMA_WARP) {
-        // ------------------------------------------------------------ MMA issuer (one lane)
-        if (lane == 0) {
-            int cs = 0, ts = 0, buf = 0;
-            uint32_t cph = 0, bph = 0;
+            // ------------------------------------------------------------ MMA issuer (one lane)
+            if (lane == 0) {
+                int cs = 0, ts = 0, buf = 0;
+                uint32_t cph = 0, bph = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    for (int kb = 0; kb < ksteps && ok; ++kb) {
+                        // converted weights ready: the converters arrive on full_c only after they
+                        // saw the TMA stage (weight and activation codes) complete
+                        if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint64_t ad = smem_desc_sw128(smem_u32(cstage + cs * C::CSTAGE_BYTES));
+                        const uint64_t bd = smem_desc_sw128(smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES);
+                        // the step's two 32-K blocks, each into its own accumulator: the two
+                        // buffers of hand-off pair buf
+                        if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int h = 0; h < C::BK / C::GROUP_K; ++h) {
+                            const uint32_t dtmem = tmem_base + (uint32_t)((2 * buf + h) * C::BN);
+                            // descriptor start addresses in 16-byte units: 64 bytes per 32-K block
+                            tc_mma_f16(dtmem, ad + (uint64_t)(h * 4), bd + (uint64_t)(h * 4), C::IDESC, 0u);
+                            tc_mma_f16(dtmem, ad + (uint64_t)(h * 4 + 2), bd + (uint64_t)(h * 4 + 2), C::IDESC, 1u);
+                        }
+                        tc_commit(&acc_full[buf]);
+                        if (++buf == C::NHAND) {
+                            buf = 0;
+                            bph ^= 1u;
+                        }
+                        tc_commit(&empty_c[cs]);
+                        tc_commit(&empty_t[ts]);
+                        if (++cs == C::CSTAGES) {
+                            cs = 0;
+                            cph ^= 1u;
+                        }
+                        if (++ts == C::TSTAGES) ts = 0;
+                    }
+                }
+                tc_commit(drain_bar);
+                drain_ring(drain_bar, 1, 1, p.err);
+            }
+            __syncwarp();
+        } else if (warp == 1 || warp == 3) {
+            // ------------------------------------------------------------ converters (int8 -> f16)
+            const int ct = (warp == 1 ? 0 : 1) * 32 + lane;
+            int ts = 0, cs = 0;
+            uint32_t tph = 0, cph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < ksteps && ok; ++kb) {
-                    // converted weights ready: the converters arrive on full_c only after they
-                    // saw the TMA stage (weight and activation codes) complete
-                    if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                for (int kb = 0; kb < ksteps; ++kb) {
+                    if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
+                        !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    const uint64_t ad = smem_desc_sw128(smem_u32(cstage + cs * C::CSTAGE_BYTES));
-                    const uint64_t bd = smem_desc_sw128(smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES);
-                    // the step's two 32-K blocks, each into its own accumulator: the two
-                    // buffers of hand-off pair buf
-                    if (!mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)) {
-                        ok = false;
-                        break;
+                    const uint32_t traw = smem_u32(tstage + ts * C::TSTAGE_BYTES);
+                    const uint32_t cbase = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+                    convert_i8_row(traw, cbase, ct);
+                    convert_i8_row(traw, cbase, ct + 64);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&full_c[cs]);
+                        mbar_arrive(&empty_t[ts]);
                     }
-                    tc_fence_after();
-#pragma unroll
-                    for (int h = 0; h < C::BK / C::GROUP_K; ++h) {
-                        const uint32_t dtmem = tmem_base + (uint32_t)((2 * buf + h) * C::BN);
-                        // descriptor start addresses in 16-byte units: 64 bytes per 32-K block
-                        tc_mma_f16(dtmem, ad + (uint64_t)(h * 4), bd + (uint64_t)(h * 4), C::IDESC, 0u);
-                        tc_mma_f16(dtmem, ad + (uint64_t)(h * 4 + 2), bd + (uint64_t)(h * 4 + 2), C::IDESC, 1u);
+                    if (++ts == C::TSTAGES) {
+                        ts = 0;
+                        tph ^= 1u;
                     }
-                    tc_commit(&acc_full[buf]);
-                    if (++buf == C::NHAND) {
-                        buf = 0;
-                        bph ^= 1u;
-                    }
-                    tc_commit(&empty_c[cs]);
-                    tc_commit(&empty_t[ts]);
                     if (++cs == C::CSTAGES) {
                         cs = 0;
                         cph ^= 1u;
                     }
-                    if (++ts == C::TSTAGES) ts = 0;
                 }
             }
-            tc_commit(drain_bar);
-            drain_ring(drain_bar, 1, 1, p.err);
-        }
-        __syncwarp();
-        } else if (warp == 1 || warp == 3) {
-        // ------------------------------------------------------------ converters (int8 -> f16)
-        const int ct = (warp == 1 ? 0 : 1) * 32 + lane;
-        int ts = 0, cs = 0;
-        uint32_t tph = 0, cph = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            for (int kb = 0; kb < ksteps; ++kb) {
-                if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
-                    !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t traw = smem_u32(tstage + ts * C::TSTAGE_BYTES);
-                const uint32_t cbase = smem_u32(cstage + cs * C::CSTAGE_BYTES);
-                convert_i8_row(traw, cbase, ct);
-                convert_i8_row(traw, cbase, ct + 64);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&full_c[cs]);
-                    mbar_arrive(&empty_t[ts]);
-                }
-                if (++ts == C::TSTAGES) {
-                    ts = 0;
-                    tph ^= 1u;
-                }
-                if (++cs == C::CSTAGES) {
-                    cs = 0;
-                    cph ^= 1u;
-                }
-            }
-        }
-            } else if (warp >= C::QUANT_BASE) {
+        } else if (warp >= C::QUANT_BASE) {
             // ---------------------------------------------------------- q8_1 rounding of the staged tile
             // warp w takes tokens [32 w, 32 w + 32); lane l holds n0 + 4l .. 4l + 3 of a token
             // row, so each block of 32 outputs is 8 lanes: d = max|y|/127, q =

@@ -79,12 +79,18 @@ struct GemmCfg {
     // 16 fold warps (FP8 with two row sub-tiles): 20 warps, five per
     // sub-partition (a sixth would cap registers at 80), the two converters on
     // warps 2 and 3
-    static constexpr int THREADS = (EPI_WARPS_ == 16) ? 32 * 20 : 512;
+    // 16 fold warps with 4 converters: 24 warps launched at 80 registers a thread,
+    // the four fold warpgroups raised to 96 (two sub-tiles x 32 running sums), the
+    // other two lowered to 48 - the shares add up to exactly the launch's 24 x 80
+    static constexpr bool REG_SPLIT = (EPI_WARPS_ == 16 && CONV_WARPS_ == 4);
+    static constexpr int REGS_LAUNCH = 80, REGS_EPI = 96, REGS_OTHER = 48;
+    static_assert(!REG_SPLIT || 16 * REGS_EPI + 8 * REGS_OTHER == 24 * REGS_LAUNCH, "register shares = launch registers");
+    static constexpr int THREADS = REG_SPLIT ? 32 * 24 : ((EPI_WARPS_ == 16) ? 32 * 20 : 512);
     // one CTA per SM: each sub-partition's 16384 registers shared by its warps,
     // in the allocation unit of 8 per thread
     static constexpr int WARPS_PER_SMSP = (THREADS / 32 + 3) / 4;
     static constexpr int MAXNREG_RAW = 16384 / (WARPS_PER_SMSP * 32) / 8 * 8;
-    static constexpr int MAXNREG = MAXNREG_RAW > 255 ? 255 : MAXNREG_RAW;
+    static constexpr int MAXNREG = REG_SPLIT ? REGS_LAUNCH : (MAXNREG_RAW > 255 ? 255 : MAXNREG_RAW);
     // fold epilogue: token columns per warp, and the TMEM load width
     static constexpr int FOLD_CPW = ACC_N / (EPI_WARPS_ >= 8 ? EPI_WARPS_ / 4 : 1);
     static constexpr int FOLD_LDW = (EPI_WARPS_ == 16) ? 16 : 32;
@@ -132,7 +138,7 @@ struct GemmCfg {
     static_assert(NBUF >= 1, "TMEM columns");
     static_assert(CLUSTER_N == 1 || CLUSTER_N == 2 || CLUSTER_N == 4, "cluster size");
     static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4) ||
-                      (EPI_WARPS == 16 && CONV_WARPS == 2),
+                      (EPI_WARPS == 16 && (CONV_WARPS == 2 || CONV_WARPS == 4)),
                   "warp layout");
     // relay threads of a pair's odd CTA: lane 0 of the MMA warp (slot 0) and of the
     // warps without a role (slots 1, 2: warps 5 and 9 with 4 epilogue warps)
@@ -153,10 +159,13 @@ struct GemmCfg {
     // converter slot of a warp, -1 if it is not a converter:
     //   4 epilogue warps (12..15):  converters on warps 2,3,4,6,7,8,10,11
     //   8 epilogue warps (4..11):   converters on warps 2,3,12,14
-    //   16 epilogue warps (4..19):  converters on warps 2,3
+    //   16 epilogue warps (4..19):  converters on warps 2,3 (and 20, 23 with four)
     __device__ static int conv_slot(int warp) {
         if constexpr (EPI_WARPS == 16) {
-            return (warp == 2 || warp == 3) ? warp - 2 : -1;
+            if (warp == 2 || warp == 3) return warp - 2;
+            if (CONV_WARPS == 4 && warp == 20) return 2;
+            if (CONV_WARPS == 4 && warp == 23) return 3;
+            return -1;
         } else {
             // slot + 1 per warp, one nibble each (0: not a converter)
             constexpr unsigned long long tab = (EPI_WARPS == 4) ? 0x870654032100ull : 0x403000000002100ull;
@@ -569,185 +578,11 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         }
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        {
-            int s = 0;
-            uint32_t ph = 0;
-            long issued = 0;
-            bool ok = true;
-            TileInfo ti_next{};
-            if (cid < num_tiles) ti_next = decode_tile<C>(p, cid, crank);
-            for (int t = cid; t < num_tiles && ok; t += ncl) {
-                const TileInfo ti = ti_next;                 // read one tile ahead
-                if (t + ncl < num_tiles) ti_next = decode_tile<C>(p, t + ncl, crank);
-                // the weight codes' tensor map: the expert's own (pointer-table form), or
-                // the kernel parameter over the contiguous [E][...] array
-                const CUtensorMap* bmap = p.wmaps ? p.wmaps + ti.expert : &tmB;
-                if (p.wmaps) tensormap_acquire(bmap);
-                for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
-                    const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
-                    if (__any_sync(0xffffffffu, !got)) {
-                        ok = false;
-                        break;
-                    }
-                    // A thread has one TMA copy executing at a time, so each copy of stage s
-                    // comes from its own lane of lane group s % TMA_GROUPS: copies of
-                    // different stages and kinds overlap.
-                    const int l0 = (s % C::TMA_GROUPS) * 4;
-                    uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                    if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
-                    __syncwarp();
-                    if (lane == l0) {
-                        if constexpr (C::PAIR) {
-                            // this CTA's 128 rows of the pair's 256-row tile
-                            tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
-                        } else if constexpr (C::CLUSTER_N > 1) {
-                            // this CTA's slice of the activation tile, written into every CTA of the cluster
-                            tma_load_2d_multicast(st + crank * C::A_SLICE_ROWS * 128, &tmA, &full_t[s], kb * C::BK,
-                                                  ti.row0 + crank * C::A_SLICE_ROWS,
-                                                  (uint16_t)((1u << C::CLUSTER_N) - 1));
-                        } else {
-                            tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
-                        }
-                    } else if (lane == l0 + 1 || lane == l0 + 2) {
-                        uint8_t* bdst = st + C::A_RAW_BYTES;
-                        const int kx = kb * C::B_ROW_BYTES;
-                        if constexpr (C::EPI == Epi::SWIGLU_Q81) {
-                            // gate rows n0 .. +BN/2 (lane l0+1), up rows F + n0 .. +BN/2 (lane l0+2) of
-                            // the expert's [2F] rows (row e*2F + ... of the contiguous array)
-                            const int base = (p.wmaps ? 0 : ti.expert * 2 * p.F) + ti.n0;
-                            if (lane == l0 + 1)
-                                tma_load_2d(bdst, bmap, &full_t[s], kx, base);
-                            else
-                                tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, bmap, &full_t[s], kx, base + p.F);
-                        } else if (lane == l0 + 1) {
-                            tma_load_2d(bdst, bmap, &full_t[s], kx, (p.wmaps ? 0 : ti.expert * p.N) + ti.n0);
-                        }
-                    }
-                    __syncwarp();
-                    ++issued;
-                    if (++s == C::TSTAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            // Teardown: every copy issued must have landed before the CTA exits.
-            if (lane == 0) drain_ring(full_t, issued, C::TSTAGES, p.err);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (one lane)
-        // One thread runs the whole issue loop: the descriptors of a K block are
-        // built once and advanced by constants, and there is no election or warp
-        // synchronisation between MMAs.  Pair: the even CTA issues for both.
-        if (lane == 0 && pair_leader) {
-            int ts = 0, cs = 0, buf = 0;
-            uint32_t cph = 0, bph = 0;
-            bool ok = true;
-            // the work item, read one ahead so the descriptor load is off the issue
-            // path: its K range, and the sub-tiles holding at least one live row (a
-            // tile of <= 128 rows skips the second)
-            TileInfo mi_next{};
-            if (cid < num_tiles) mi_next = decode_tile<C>(p, cid, crank);
-            for (int t = cid; t < num_tiles && ok; t += ncl) {
-                const TileInfo mi = mi_next;
-                if (t + ncl < num_tiles) mi_next = decode_tile<C>(p, t + ncl, crank);
-                const int nsub = (C::MSUB == 2 && mi.rows <= 128) ? 1 : C::MSUB;
-                for (int kb = mi.kb0; kb < mi.kb1; ++kb) {
-                    // Only the converted weights are waited on: the converters arrive on
-                    // full_c after they saw this stage's TMA copies complete (full_t), so
-                    // full_c also orders the activation tile.
-                    // (pair: both CTAs' converters arrive here, after their own TMA stage)
-                    const bool got_c = C::PAIR ? mbar_wait_cl(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)
-                                               : mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
-                    if (!got_c) {
-                        ok = false;
-                        break;
-                    }
-                    // first / last K block of an accumulation group (the item's K range, or
-                    // one 128-K block = two K blocks for the FP8 fold)
-                    bool first, last;
-                    if constexpr (C::GROUP_K == 128) {
-                        first = (kb & 1) == 0;
-                        last = (kb & 1) == 1;
-                    } else {
-                        first = kb == mi.kb0;
-                        last = kb == mi.kb1 - 1;
-                    }
-                    if (first) {
-                        const bool got_a =
-                            C::PAIR ? mbar_wait_cl(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)
-                                    : mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY);
-                        if (!got_a) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    // (no tcgen05 fence per K block: the operands are ordered by the mbarrier
-                    // and the writers' proxy fence; such a fence would drain the MMA pipe)
-                    // descriptor start addresses are in 16-byte units: +2 per K step of 16
-                    // (32 bytes), +1024 per 128-row sub-tile (16 KB)
-                    const uint64_t ad = smem_desc_sw128(smem_u32(tstage + ts * C::TSTAGE_BYTES));
-                    const uint64_t bd = smem_desc_sw128(smem_u32(cstage + cs * C::CSTAGE_BYTES));
-                    const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::MSUB * C::ACC_N);
-                    if constexpr (C::PAIR) {
-                        // M = 256 over the pair, N = 2 * BN: both CTAs' stages at the same offsets
-#pragma unroll
-                        for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk)
-                            tc_mma_f16_pair(dtmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), C::IDESC,
-                                            (first && kk == 0) ? 0u : 1u);
-                        if (last) {
-                            tc_commit_pair(&acc_full[buf], 3);
-                            if (++buf == C::NBUF) {
-                                buf = 0;
-                                bph ^= 1u;
-                            }
-                        }
-                        tc_commit_pair(&empty_c[cs], 3);
-                        tc_commit_pair(&empty_t[ts], 3);
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-#pragma unroll
-                            for (int m = 0; m < C::MSUB; ++m)
-                                if (m < nsub)
-                                    tc_mma_f16(dtmem + (uint32_t)(m * C::BN), ad + (uint64_t)(m * 1024 + kk * 2),
-                                               bd + (uint64_t)(kk * 2), C::IDESC, (first && kk == 0) ? 0u : 1u);
-                        }
-                        if (last) {
-                            tc_commit(&acc_full[buf]);
-                            if (++buf == C::NBUF) {
-                                buf = 0;
-                                bph ^= 1u;
-                            }
-                        }
-                        tc_commit(&empty_c[cs]);
-                        if constexpr (C::CLUSTER_N > 1)
-                            tc_commit_multicast(&empty_t[ts], (uint16_t)((1u << C::CLUSTER_N) - 1));
-                        else
-                            tc_commit(&empty_t[ts]);
-                    }
-                    if (++ts == C::TSTAGES) ts = 0;
-                    if (++cs == C::CSTAGES) {
-                        cs = 0;
-                        cph ^= 1u;
-                    }
-                }
-            }
-            // Teardown: wait until every MMA issued has completed before TMEM is freed.
-            if constexpr (C::PAIR)
-                tc_commit_pair(drain_bar, 1);
-            else
-                tc_commit(drain_bar);
-            drain_ring(drain_bar, 1, 1, p.err);
-        }
-        if constexpr (C::PAIR) {
-            if (lane == 0 && !pair_leader) relay_stages(0);
-        }
-        __syncwarp();
-    } else if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
+    // Roles.  With the register split, each warpgroup runs exactly one setmaxnreg
+    // (the fold warpgroups the inc, the others the dec), at the top of the code it
+    // governs.
+    if (warp >= C::EPI_BASE && warp < C::EPI_BASE + C::EPI_WARPS) {
+        if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::REGS_EPI>();
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                         // TMEM lane quarter of this warp
         const int row = q * 32 + lane;                  // accumulator row = TMEM lane
@@ -960,163 +795,344 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 }
             }
         }
-    } else if (C::conv_slot(warp) >= 0) {
-        // ------------------------------------------------------------ converters
-        const int ct = C::conv_slot(warp) * 32 + lane;
-        const int crow = ct % C::BN;                      // this thread's weight row in every tile
-        const int chalf = ct / C::BN;                     // and its K half (TPR == 2)
-        int ts = 0, cs = 0;
-        uint32_t tph = 0, cph = 0;
-        bool ok = true;
-        // W4 scales: 16-byte loads covering 4 K blocks, one chunk ahead (K % 256 == 0),
-        // else one 4-byte load per K block.
-        const bool vec_scales = (p.K % 256) == 0;
-        // this thread's weight row of a tile: its E4M3 scale row (K/16 bytes)
-        auto scale_row = [&](const TileInfo& tt, bool& in_range) -> const uint8_t* {
-            if constexpr (C::EPI == Epi::SWIGLU_Q81) {
-                const int hr = (crow < C::BN / 2) ? (tt.n0 + crow) : (p.F + tt.n0 + crow - C::BN / 2);
-                in_range = true;
-                if (p.wscale_tab) return p.wscale_tab[tt.expert] + (long)hr * (p.K / 16);
-                return p.w_scale + ((long)tt.expert * 2 * p.F + hr) * (p.K / 16);
-            } else {
-                in_range = (long)tt.n0 + crow < p.N;
-                return p.w_scale + ((long)tt.n0 + crow) * (p.K / 16);
-            }
-        };
-        // Scale prefetch two 4-K-block chunks ahead, through a cursor that walks
-        // this CTA's work items (and each item's K range) in the order they are
-        // converted: the next item's descriptor is read one chunk before its first
-        // scales are needed, so neither global load (descriptor, then scales) sits
-        // on the critical path.
-        int pf_t = cid, pf_ch = 0;
-        TileInfo pf_ti{};
-        if (pf_t < num_tiles) {
-            pf_ti = decode_tile<C>(p, pf_t, crank);
-            pf_ch = pf_ti.kb0 / 4;
-        }
-        auto next_chunk = [&]() -> uint4 {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (pf_t < num_tiles) {
-                bool in_range;
-                const uint8_t* srow = scale_row(pf_ti, in_range);
-                if (in_range) v = ldg_nc_v4(srow + pf_ch * 16);
-                if (++pf_ch == pf_ti.kb1 / 4) {
-                    pf_t += ncl;
-                    if (pf_t < num_tiles) {
-                        pf_ti = decode_tile<C>(p, pf_t, crank);
-                        pf_ch = pf_ti.kb0 / 4;
-                    }
-                }
-            }
-            return v;
-        };
-        uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = make_uint4(0, 0, 0, 0), sc_next2 = make_uint4(0, 0, 0, 0);
-        if constexpr (C::B == BMode::W4) {
-            if (vec_scales) {
-                sc_next = next_chunk();
-                sc_next2 = next_chunk();
-            }
-        }
-        // Converted stages are handed to the MMA CONV_BATCH at a time: one proxy
-        // fence (and, for a pair, one cluster-scope release) per batch.  Each costs
-        // a few hundred cycles of the converter's own time, which would otherwise
-        // be paid per K block on the pipeline's critical path.
-        int pend = 0, pend_first = 0;
-        auto flush = [&]() {
-            if (pend == 0) return;
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                for (int i = 0, c = pend_first; i < pend; ++i, c = (c + 1 == C::CSTAGES) ? 0 : c + 1) {
-                    // (pair, odd CTA: to the relay thread, which forwards the stage to the
-                    // even CTA's barrier with a cluster-scope release; a converter's own
-                    // cluster-scope release would wait for its scale loads in flight)
-                    if (C::PAIR && crank != 0)
-                        mbar_arrive(&conv_done[c]);
-                    else
-                        mbar_arrive(&full_c[c]);
-                }
-            }
-            pend = 0;
-        };
-        // one K block: wait for its raw codes and a free converted stage, expand,
-        // hand the stage to the MMA (with its batch); false if a wait timed out
-        auto convert_step = [&](uint32_t sbytes) -> bool {
-            if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
-                !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY))
-                return false;
-            const uint32_t braw = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
-            const uint32_t bconv = smem_u32(cstage + cs * C::CSTAGE_BYTES);
-            if constexpr (C::B == BMode::W4) {
-                if constexpr (C::TPR == 2)
-                    convert_w4_half(braw, bconv, crow, chalf, sbytes);
-                else
-                    convert_w4_row(braw, bconv, crow, sbytes);
-            } else {
-                convert_fp8_rows<C::RPT>(braw, bconv, crow, C::BN / C::RPT);
-            }
-            if (pend++ == 0) pend_first = cs;
-            if (pend == C::CONV_BATCH) flush();
-            if (++ts == C::TSTAGES) {
-                ts = 0;
-                tph ^= 1u;
-            }
-            if (++cs == C::CSTAGES) {
-                cs = 0;
-                cph ^= 1u;
-            }
-            return true;
-        };
-        for (int t = cid; t < num_tiles && ok; t += ncl) {
-            const TileInfo ti = decode_tile<C>(p, t, crank);
-            if (C::B == BMode::W4 && vec_scales) {
-                // K % 256 == 0: the item's K range is whole 4-K-block chunks; the chunk's
-                // four scale words are picked at compile time in the unrolled steps
-                for (int ch = ti.kb0 >> 2; ch < (ti.kb1 >> 2) && ok; ++ch) {
-                    if constexpr (C::B == BMode::W4) {
-                        sc_cur = sc_next;
-                        sc_next = sc_next2;
-                        sc_next2 = next_chunk();
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t sbytes = (C::B == BMode::W4)
-                                                    ? (j == 0 ? sc_cur.x : (j == 1 ? sc_cur.y : (j == 2 ? sc_cur.z : sc_cur.w)))
-                                                    : 0u;
-                        if (!convert_step(sbytes)) {
+    } else {
+        if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
+        if (warp == 0) {
+            // ------------------------------------------------------------ producer
+            {
+                int s = 0;
+                uint32_t ph = 0;
+                long issued = 0;
+                bool ok = true;
+                TileInfo ti_next{};
+                if (cid < num_tiles) ti_next = decode_tile<C>(p, cid, crank);
+                for (int t = cid; t < num_tiles && ok; t += ncl) {
+                    const TileInfo ti = ti_next;                 // read one tile ahead
+                    if (t + ncl < num_tiles) ti_next = decode_tile<C>(p, t + ncl, crank);
+                    // the weight codes' tensor map: the expert's own (pointer-table form), or
+                    // the kernel parameter over the contiguous [E][...] array
+                    const CUtensorMap* bmap = p.wmaps ? p.wmaps + ti.expert : &tmB;
+                    if (p.wmaps) tensormap_acquire(bmap);
+                    for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                        const bool got = mbar_wait(&empty_t[s], ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_TMA_EMPTY);
+                        if (__any_sync(0xffffffffu, !got)) {
                             ok = false;
                             break;
                         }
-                    }
-                }
-            } else {
-                for (int kb = ti.kb0; kb < ti.kb1 && ok; ++kb) {
-                    uint32_t sbytes = 0;
-                    if constexpr (C::B == BMode::W4) {
-                        bool in_range;
-                        const uint8_t* srow = scale_row(ti, in_range);
-                        if (!in_range) {
-                            sbytes = 0u;
-                        } else if ((p.K & 63) == 0) {
-                            sbytes = __ldg(reinterpret_cast<const uint32_t*>(srow + kb * 4));
-                        } else {
-                            // K % 64 == 32: scale rows are not 4-byte aligned, and the last K
-                            // block has two scale bytes (its other 32 K are zero-filled codes,
-                            // given scale 0 so that no NaN scale byte of the next row enters)
-                            const int nsc = p.K / 16;
-                            sbytes = 0u;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                if (kb * 4 + i < nsc) sbytes |= (uint32_t)__ldg(srow + kb * 4 + i) << (8 * i);
+                        // A thread has one TMA copy executing at a time, so each copy of stage s
+                        // comes from its own lane of lane group s % TMA_GROUPS: copies of
+                        // different stages and kinds overlap.
+                        const int l0 = (s % C::TMA_GROUPS) * 4;
+                        uint8_t* st = tstage + s * C::TSTAGE_BYTES;
+                        if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                        __syncwarp();
+                        if (lane == l0) {
+                            if constexpr (C::PAIR) {
+                                // this CTA's 128 rows of the pair's 256-row tile
+                                tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
+                            } else if constexpr (C::CLUSTER_N > 1) {
+                                // this CTA's slice of the activation tile, written into every CTA of the cluster
+                                tma_load_2d_multicast(st + crank * C::A_SLICE_ROWS * 128, &tmA, &full_t[s], kb * C::BK,
+                                                      ti.row0 + crank * C::A_SLICE_ROWS,
+                                                      (uint16_t)((1u << C::CLUSTER_N) - 1));
+                            } else {
+                                tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
+                            }
+                        } else if (lane == l0 + 1 || lane == l0 + 2) {
+                            uint8_t* bdst = st + C::A_RAW_BYTES;
+                            const int kx = kb * C::B_ROW_BYTES;
+                            if constexpr (C::EPI == Epi::SWIGLU_Q81) {
+                                // gate rows n0 .. +BN/2 (lane l0+1), up rows F + n0 .. +BN/2 (lane l0+2) of
+                                // the expert's [2F] rows (row e*2F + ... of the contiguous array)
+                                const int base = (p.wmaps ? 0 : ti.expert * 2 * p.F) + ti.n0;
+                                if (lane == l0 + 1)
+                                    tma_load_2d(bdst, bmap, &full_t[s], kx, base);
+                                else
+                                    tma_load_2d(bdst + (C::BN / 2) * C::B_ROW_BYTES, bmap, &full_t[s], kx, base + p.F);
+                            } else if (lane == l0 + 1) {
+                                tma_load_2d(bdst, bmap, &full_t[s], kx, (p.wmaps ? 0 : ti.expert * p.N) + ti.n0);
+                            }
+                        }
+                        __syncwarp();
+                        ++issued;
+                        if (++s == C::TSTAGES) {
+                            s = 0;
+                            ph ^= 1u;
                         }
                     }
-                    if (!convert_step(sbytes)) ok = false;
+                }
+                // Teardown: every copy issued must have landed before the CTA exits.
+                if (lane == 0) drain_ring(full_t, issued, C::TSTAGES, p.err);
+            }
+        } else if (warp == 1) {
+            // ------------------------------------------------------------ MMA issuer (one lane)
+            // One thread runs the whole issue loop: the descriptors of a K block are
+            // built once and advanced by constants, and there is no election or warp
+            // synchronisation between MMAs.  Pair: the even CTA issues for both.
+            if (lane == 0 && pair_leader) {
+                int ts = 0, cs = 0, buf = 0;
+                uint32_t cph = 0, bph = 0;
+                bool ok = true;
+                // the work item, read one ahead so the descriptor load is off the issue
+                // path: its K range, and the sub-tiles holding at least one live row (a
+                // tile of <= 128 rows skips the second)
+                TileInfo mi_next{};
+                if (cid < num_tiles) mi_next = decode_tile<C>(p, cid, crank);
+                for (int t = cid; t < num_tiles && ok; t += ncl) {
+                    const TileInfo mi = mi_next;
+                    if (t + ncl < num_tiles) mi_next = decode_tile<C>(p, t + ncl, crank);
+                    const int nsub = (C::MSUB == 2 && mi.rows <= 128) ? 1 : C::MSUB;
+                    for (int kb = mi.kb0; kb < mi.kb1; ++kb) {
+                        // Only the converted weights are waited on: the converters arrive on
+                        // full_c after they saw this stage's TMA copies complete (full_t), so
+                        // full_c also orders the activation tile.
+                        // (pair: both CTAs' converters arrive here, after their own TMA stage)
+                        const bool got_c = C::PAIR ? mbar_wait_cl(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)
+                                                   : mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV);
+                        if (!got_c) {
+                            ok = false;
+                            break;
+                        }
+                        // first / last K block of an accumulation group (the item's K range, or
+                        // one 128-K block = two K blocks for the FP8 fold)
+                        bool first, last;
+                        if constexpr (C::GROUP_K == 128) {
+                            first = (kb & 1) == 0;
+                            last = (kb & 1) == 1;
+                        } else {
+                            first = kb == mi.kb0;
+                            last = kb == mi.kb1 - 1;
+                        }
+                        if (first) {
+                            const bool got_a =
+                                C::PAIR ? mbar_wait_cl(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY)
+                                        : mbar_wait(&acc_empty[buf], bph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY);
+                            if (!got_a) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        // (no tcgen05 fence per K block: the operands are ordered by the mbarrier
+                        // and the writers' proxy fence; such a fence would drain the MMA pipe)
+                        // descriptor start addresses are in 16-byte units: +2 per K step of 16
+                        // (32 bytes), +1024 per 128-row sub-tile (16 KB)
+                        const uint64_t ad = smem_desc_sw128(smem_u32(tstage + ts * C::TSTAGE_BYTES));
+                        const uint64_t bd = smem_desc_sw128(smem_u32(cstage + cs * C::CSTAGE_BYTES));
+                        const uint32_t dtmem = tmem_base + (uint32_t)(buf * C::MSUB * C::ACC_N);
+                        if constexpr (C::PAIR) {
+                            // M = 256 over the pair, N = 2 * BN: both CTAs' stages at the same offsets
+#pragma unroll
+                            for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk)
+                                tc_mma_f16_pair(dtmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), C::IDESC,
+                                                (first && kk == 0) ? 0u : 1u);
+                            if (last) {
+                                tc_commit_pair(&acc_full[buf], 3);
+                                if (++buf == C::NBUF) {
+                                    buf = 0;
+                                    bph ^= 1u;
+                                }
+                            }
+                            tc_commit_pair(&empty_c[cs], 3);
+                            tc_commit_pair(&empty_t[ts], 3);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+#pragma unroll
+                                for (int m = 0; m < C::MSUB; ++m)
+                                    if (m < nsub)
+                                        tc_mma_f16(dtmem + (uint32_t)(m * C::BN), ad + (uint64_t)(m * 1024 + kk * 2),
+                                                   bd + (uint64_t)(kk * 2), C::IDESC, (first && kk == 0) ? 0u : 1u);
+                            }
+                            if (last) {
+                                tc_commit(&acc_full[buf]);
+                                if (++buf == C::NBUF) {
+                                    buf = 0;
+                                    bph ^= 1u;
+                                }
+                            }
+                            tc_commit(&empty_c[cs]);
+                            if constexpr (C::CLUSTER_N > 1)
+                                tc_commit_multicast(&empty_t[ts], (uint16_t)((1u << C::CLUSTER_N) - 1));
+                            else
+                                tc_commit(&empty_t[ts]);
+                        }
+                        if (++ts == C::TSTAGES) ts = 0;
+                        if (++cs == C::CSTAGES) {
+                            cs = 0;
+                            cph ^= 1u;
+                        }
+                    }
+                }
+                // Teardown: wait until every MMA issued has completed before TMEM is freed.
+                if constexpr (C::PAIR)
+                    tc_commit_pair(drain_bar, 1);
+                else
+                    tc_commit(drain_bar);
+                drain_ring(drain_bar, 1, 1, p.err);
+            }
+            if constexpr (C::PAIR) {
+                if (lane == 0 && !pair_leader) relay_stages(0);
+            }
+            __syncwarp();
+        } else if (C::conv_slot(warp) >= 0) {
+            // ------------------------------------------------------------ converters
+            const int ct = C::conv_slot(warp) * 32 + lane;
+            const int crow = ct % C::BN;                      // this thread's weight row in every tile
+            const int chalf = ct / C::BN;                     // and its K half (TPR == 2)
+            int ts = 0, cs = 0;
+            uint32_t tph = 0, cph = 0;
+            bool ok = true;
+            // W4 scales: 16-byte loads covering 4 K blocks, one chunk ahead (K % 256 == 0),
+            // else one 4-byte load per K block.
+            const bool vec_scales = (p.K % 256) == 0;
+            // this thread's weight row of a tile: its E4M3 scale row (K/16 bytes)
+            auto scale_row = [&](const TileInfo& tt, bool& in_range) -> const uint8_t* {
+                if constexpr (C::EPI == Epi::SWIGLU_Q81) {
+                    const int hr = (crow < C::BN / 2) ? (tt.n0 + crow) : (p.F + tt.n0 + crow - C::BN / 2);
+                    in_range = true;
+                    if (p.wscale_tab) return p.wscale_tab[tt.expert] + (long)hr * (p.K / 16);
+                    return p.w_scale + ((long)tt.expert * 2 * p.F + hr) * (p.K / 16);
+                } else {
+                    in_range = (long)tt.n0 + crow < p.N;
+                    return p.w_scale + ((long)tt.n0 + crow) * (p.K / 16);
+                }
+            };
+            // Scale prefetch two 4-K-block chunks ahead, through a cursor that walks
+            // this CTA's work items (and each item's K range) in the order they are
+            // converted: the next item's descriptor is read one chunk before its first
+            // scales are needed, so neither global load (descriptor, then scales) sits
+            // on the critical path.
+            int pf_t = cid, pf_ch = 0;
+            TileInfo pf_ti{};
+            if (pf_t < num_tiles) {
+                pf_ti = decode_tile<C>(p, pf_t, crank);
+                pf_ch = pf_ti.kb0 / 4;
+            }
+            auto next_chunk = [&]() -> uint4 {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (pf_t < num_tiles) {
+                    bool in_range;
+                    const uint8_t* srow = scale_row(pf_ti, in_range);
+                    if (in_range) v = ldg_nc_v4(srow + pf_ch * 16);
+                    if (++pf_ch == pf_ti.kb1 / 4) {
+                        pf_t += ncl;
+                        if (pf_t < num_tiles) {
+                            pf_ti = decode_tile<C>(p, pf_t, crank);
+                            pf_ch = pf_ti.kb0 / 4;
+                        }
+                    }
+                }
+                return v;
+            };
+            uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_next = make_uint4(0, 0, 0, 0), sc_next2 = make_uint4(0, 0, 0, 0);
+            if constexpr (C::B == BMode::W4) {
+                if (vec_scales) {
+                    sc_next = next_chunk();
+                    sc_next2 = next_chunk();
                 }
             }
-        }
-        flush();
-    } else if (C::PAIR && C::RELAYS > 1 && C::relay_slot(warp) > 0) {
-        if (lane == 0 && !pair_leader) relay_stages(C::relay_slot(warp));
+            // Converted stages are handed to the MMA CONV_BATCH at a time: one proxy
+            // fence (and, for a pair, one cluster-scope release) per batch.  Each costs
+            // a few hundred cycles of the converter's own time, which would otherwise
+            // be paid per K block on the pipeline's critical path.
+            int pend = 0, pend_first = 0;
+            auto flush = [&]() {
+                if (pend == 0) return;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int i = 0, c = pend_first; i < pend; ++i, c = (c + 1 == C::CSTAGES) ? 0 : c + 1) {
+                        // (pair, odd CTA: to the relay thread, which forwards the stage to the
+                        // even CTA's barrier with a cluster-scope release; a converter's own
+                        // cluster-scope release would wait for its scale loads in flight)
+                        if (C::PAIR && crank != 0)
+                            mbar_arrive(&conv_done[c]);
+                        else
+                            mbar_arrive(&full_c[c]);
+                    }
+                }
+                pend = 0;
+            };
+            // one K block: wait for its raw codes and a free converted stage, expand,
+            // hand the stage to the MMA (with its batch); false if a wait timed out
+            auto convert_step = [&](uint32_t sbytes) -> bool {
+                if (!mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL) ||
+                    !mbar_wait(&empty_c[cs], cph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_CONV_EMPTY))
+                    return false;
+                const uint32_t braw = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
+                const uint32_t bconv = smem_u32(cstage + cs * C::CSTAGE_BYTES);
+                if constexpr (C::B == BMode::W4) {
+                    if constexpr (C::TPR == 2)
+                        convert_w4_half(braw, bconv, crow, chalf, sbytes);
+                    else
+                        convert_w4_row(braw, bconv, crow, sbytes);
+                } else {
+                    convert_fp8_rows<C::RPT>(braw, bconv, crow, C::BN / C::RPT);
+                }
+                if (pend++ == 0) pend_first = cs;
+                if (pend == C::CONV_BATCH) flush();
+                if (++ts == C::TSTAGES) {
+                    ts = 0;
+                    tph ^= 1u;
+                }
+                if (++cs == C::CSTAGES) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
+                return true;
+            };
+            for (int t = cid; t < num_tiles && ok; t += ncl) {
+                const TileInfo ti = decode_tile<C>(p, t, crank);
+                if (C::B == BMode::W4 && vec_scales) {
+                    // K % 256 == 0: the item's K range is whole 4-K-block chunks; the chunk's
+                    // four scale words are picked at compile time in the unrolled steps
+                    for (int ch = ti.kb0 >> 2; ch < (ti.kb1 >> 2) && ok; ++ch) {
+                        if constexpr (C::B == BMode::W4) {
+                            sc_cur = sc_next;
+                            sc_next = sc_next2;
+                            sc_next2 = next_chunk();
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t sbytes = (C::B == BMode::W4)
+                                                        ? (j == 0 ? sc_cur.x : (j == 1 ? sc_cur.y : (j == 2 ? sc_cur.z : sc_cur.w)))
+                                                        : 0u;
+                            if (!convert_step(sbytes)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
+                } else {
+                    for (int kb = ti.kb0; kb < ti.kb1 && ok; ++kb) {
+                        uint32_t sbytes = 0;
+                        if constexpr (C::B == BMode::W4) {
+                            bool in_range;
+                            const uint8_t* srow = scale_row(ti, in_range);
+                            if (!in_range) {
+                                sbytes = 0u;
+                            } else if ((p.K & 63) == 0) {
+                                sbytes = __ldg(reinterpret_cast<const uint32_t*>(srow + kb * 4));
+                            } else {
+                                // K % 64 == 32: scale rows are not 4-byte aligned, and the last K
+                                // block has two scale bytes (its other 32 K are zero-filled codes,
+                                // given scale 0 so that no NaN scale byte of the next row enters)
+                                const int nsc = p.K / 16;
+                                sbytes = 0u;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    if (kb * 4 + i < nsc) sbytes |= (uint32_t)__ldg(srow + kb * 4 + i) << (8 * i);
+                            }
+                        }
+                        if (!convert_step(sbytes)) ok = false;
+                    }
+                }
+            }
+            flush();
+        } else if (C::PAIR && C::RELAYS > 1 && C::relay_slot(warp) > 0) {
+            if (lane == 0 && !pair_leader) relay_stages(C::relay_slot(warp));
+            }
     }
 
     __syncthreads();
@@ -1141,6 +1157,15 @@ cudaError_t launch_qgemm(const CUtensorMap& tmA, const CUtensorMap& tmB, GemmPar
     static_assert(C::SMEM_BYTES <= 232448, "shared memory");
     cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    if constexpr (C::REG_SPLIT) {
+        // the warpgroups' register shares add up to the launch's: launch only if the
+        // kernel is allocated exactly that many (more shares than the pool would
+        // leave a setmaxnreg.inc waiting)
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, qgemm_kernel<C>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != C::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
+    }
     if (C::CLUSTER_N > 1) {
         e = cudaFuncSetAttribute(qgemm_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
         if (e != cudaSuccess) return e;
