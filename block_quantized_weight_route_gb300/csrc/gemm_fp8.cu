@@ -16,7 +16,7 @@ template <int CN>
 using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, QMM_FP8_CONV, 16, 4, 4, false, CN, 2>;
 // CTA pair: 256 x 256 tiles, each CTA 128 token rows and 128 weight rows (one
 // 128 x 128 scale block), the fold over its 128 rows x both CTAs' columns.
-using CfgFp8Pair = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, 2, 16, 5, 4, false, 2, 1, true>;
+using CfgFp8Pair = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, QMM_FP8_CONV, 16, 5, 4, false, 2, 1, true>;
 static_assert(CfgFp8<1>::TILE_M == CfgFp8Pair::TILE_M, "one routing of rows for both forms");
 
 int fp8_tile_rows() { return CfgFp8<1>::TILE_M; }
