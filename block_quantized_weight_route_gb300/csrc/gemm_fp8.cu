@@ -12,8 +12,13 @@ namespace qmm {
 #ifndef QMM_FP8_CONV
 #define QMM_FP8_CONV 4
 #endif
+// Operands swapped (weights as the MMA's A, M = 128; the 256 token rows as its B,
+// N = 256): one N = 256 MMA per K step of 16.
+#ifndef QMM_FP8_SWAP
+#define QMM_FP8_SWAP 1
+#endif
 template <int CN>
-using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, QMM_FP8_CONV, 16, 4, 4, false, CN, 2>;
+using CfgFp8 = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, QMM_FP8_CONV, 16, 4, 4, false, CN, 2, false, QMM_FP8_SWAP != 0>;
 // CTA pair: 256 x 256 tiles, each CTA 128 token rows and 128 weight rows (one
 // 128 x 128 scale block), the fold over its 128 rows x both CTAs' columns.
 using CfgFp8Pair = GemmCfg<BMode::FP8, Epi::FOLD_FP8, 128, QMM_FP8_CONV, 16, 5, 4, false, 2, 1, true>;

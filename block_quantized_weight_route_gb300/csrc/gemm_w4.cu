@@ -23,8 +23,14 @@ using CfgW4DenseWide = GemmCfg<BMode::W4, Epi::STORE, 256, 8, 4, 3, 2, false, CN
 template <int CN>
 using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 128, 8, 4, 4, 3, false, CN, 2>;
 // Gate/up: 256 token rows x (64 gate + 64 up) weight rows per tile.
+// Operands swapped: the converted 128 weight rows as the MMA's A (M = 128), the
+// 256 token rows as its B (N = 256, or a short tile's live rows rounded up to 16).
+#ifndef QMM_GU_SWAP
+#define QMM_GU_SWAP 1
+#endif
 template <int CN>
-using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, QMM_GU_TSTAGES, QMM_GU_CSTAGES, true, CN, 2>;
+using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, QMM_GU_TSTAGES, QMM_GU_CSTAGES, true, CN, 2, false,
+                            QMM_GU_SWAP != 0>;
 // CTA-pair forms (clusters of 2): 256 token rows x 256 weight rows per pair,
 // each CTA 128 token rows and 128 weight rows (gate/up: 64 gate + 64 up).
 #ifndef QMM_PAIR_TSTAGES

@@ -41,13 +41,47 @@ namespace qmm {
 #define QMM_PAIR 0
 #endif
 
+// Short tiles (at most 128 live rows of 256) load half the activation tile.
+#ifndef QMM_HALF_A
+#define QMM_HALF_A 1
+#endif
+
 enum class BMode { W4, FP8 };
 enum class Epi { STORE, SWIGLU_Q81, FOLD_FP8 };
 
 template <BMode B_, Epi E_, int BN_, int CONV_WARPS_, int EPI_WARPS_, int TSTAGES_, int CSTAGES_, bool GROUPED_,
-          int CLUSTER_N_ = 1, int MSUB_ = 1, bool PAIR_ = false>
+          int CLUSTER_N_ = 1, int MSUB_ = 1, bool PAIR_ = false, bool SWAP_ = false>
 struct GemmCfg {
     static constexpr BMode B = B_;
+    // Operands swapped (FP8 fold, gate/up): the converted weight tile is the
+    // MMA's A operand (M = 128 weight rows) and the 256-row activation tile its B
+    // operand (N = 256 token rows, or the tile's live rows rounded up to 16), one
+    // MMA per K step of 16 instead of one per 128-row sub-tile.  An N = 256 MMA
+    // reads 12 KB of shared-memory operands per 128 cycles, two N = 128 MMAs 16 KB,
+    // and shared-memory bandwidth (operand reads, converter stores, TMA writes)
+    // bounds these kernels.  The accumulator is transposed: TMEM lane = weight
+    // row, column = token row.
+    static constexpr bool SWAP = SWAP_;
+    static_assert(!SWAP_ || (MSUB_ == 2 && !PAIR_ && BN_ == 128 &&
+                             ((E_ == Epi::FOLD_FP8 && EPI_WARPS_ == 16) || (E_ == Epi::SWIGLU_Q81 && EPI_WARPS_ == 4))),
+                  "swapped operands: FP8 fold or gate/up over 256 x 128 tiles");
+    // gate/up, swapped: the converted rows are placed so that TMEM lane quarter q
+    // holds gate rows f = 16q .. 16q + 15 (lanes 0..15) and the up rows of the same
+    // f (lanes 16..31); SwiGLU pairs lanes l and l + 16, and h passes through a
+    // shared stage of 32 tokens x 64 f (two buffers, rows padded to 65 floats) to
+    // be rounded to q8_1 along f
+    static constexpr bool SWAP_GU = SWAP_ && E_ == Epi::SWIGLU_Q81;
+    static constexpr int HS_STRIDE = 65, HS_FLOATS = 32 * HS_STRIDE;
+    static constexpr int HS_BYTES = SWAP_GU ? 2 * HS_FLOATS * 4 : 0;
+    __device__ static int conv_dst_row(int r) {
+        if constexpr (SWAP_GU) {
+            const int f = r & 63, up = r >> 6;
+            return ((f >> 4) << 5) | (up << 4) | (f & 15);
+        } else {
+            return r;
+        }
+    }
+
     // CTA pair (cta_group::2): the two CTAs of a cluster of 2 compute one
     // 256 x 2*BN tile with M = 256 MMAs issued by the even CTA.  Each CTA holds
     // 128 activation rows and converts BN weight rows (its half of the MMA's N);
@@ -121,9 +155,9 @@ struct GemmCfg {
     // converter threads per weight row, or weight rows per converter thread
     static constexpr int TPR = (CONV_WARPS_ * 32 >= BN_) ? CONV_WARPS_ * 32 / BN_ : 1;
     static constexpr int RPT = (CONV_WARPS_ * 32 >= BN_) ? 1 : BN_ / (CONV_WARPS_ * 32);
-    static constexpr int BAR_COUNT = 2 * TSTAGES + 3 * CSTAGES + 2 * NBUF + 1;
+    static constexpr int BAR_COUNT = 2 * TSTAGES + 3 * CSTAGES + 2 * NBUF + 1 + (SWAP_GU ? 2 : 0);
     static constexpr int SMEM_BYTES =
-        1024 /*align slack*/ + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES + BAR_COUNT * 8 + 64;
+        1024 /*align slack*/ + TSTAGES * TSTAGE_BYTES + CSTAGES * CSTAGE_BYTES + HS_BYTES + BAR_COUNT * 8 + 64;
     static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
     static_assert(!FOLD || EPI_WARPS == 8 || EPI_WARPS == 16, "fold epilogue: two or four warps per lane quarter");
@@ -304,8 +338,9 @@ constexpr uint32_t kF16x2_1152 = 0x64806480u;
 // into 64 exact 16-bit operand values, written as 8 chunks of 16 bytes into a
 // 128-byte-swizzled K-major tile.
 
-// W4: 64 e2m1 codes (32 bytes, 32-byte-swizzled rows) and 4 E4M3 scale bytes.
-__device__ __forceinline__ void convert_w4_row(uint32_t raw_tile, uint32_t dst_tile, int r, uint32_t sbytes) {
+// W4: 64 e2m1 codes (32 bytes, 32-byte-swizzled rows) and 4 E4M3 scale bytes;
+// raw row r becomes row rd of the operand tile.
+__device__ __forceinline__ void convert_w4_row(uint32_t raw_tile, uint32_t dst_tile, int r, int rd, uint32_t sbytes) {
     const int sw = (r >> 2) & 1;
     const uint4 c0 = lds128(raw_tile + r * 32 + ((0 ^ sw) << 4));
     const uint4 c1 = lds128(raw_tile + r * 32 + ((1 ^ sw) << 4));
@@ -319,12 +354,12 @@ __device__ __forceinline__ void convert_w4_row(uint32_t raw_tile, uint32_t dst_t
         cvt_e2m1x8_f16x2(words[w], h);
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(h[i]), sc[w >> 1]);
-        sts128(dst_tile + sw128_off(r, w), o[0], o[1], o[2], o[3]);
+        sts128(dst_tile + sw128_off(rd, w), o[0], o[1], o[2], o[3]);
     }
 }
 
 // W4, half a row: the 32 codes of K half h (one 16-byte chunk) and their 2 scales.
-__device__ __forceinline__ void convert_w4_half(uint32_t raw_tile, uint32_t dst_tile, int r, int h, uint32_t sbytes) {
+__device__ __forceinline__ void convert_w4_half(uint32_t raw_tile, uint32_t dst_tile, int r, int rd, int h, uint32_t sbytes) {
     const int sw = (r >> 2) & 1;
     const uint4 c = lds128(raw_tile + r * 32 + ((h ^ sw) << 4));
     const uint32_t sc0 = w4_scale_bf16x2(sbytes >> (16 * h));
@@ -336,7 +371,7 @@ __device__ __forceinline__ void convert_w4_half(uint32_t raw_tile, uint32_t dst_
         cvt_e2m1x8_f16x2(words[w], hh);
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(hh[i]), (w < 2) ? sc0 : sc1);
-        sts128(dst_tile + sw128_off(r, 4 * h + w), o[0], o[1], o[2], o[3]);
+        sts128(dst_tile + sw128_off(rd, 4 * h + w), o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -489,7 +524,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tstage = smem;
     uint8_t* cstage = tstage + C::TSTAGES * C::TSTAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(cstage + C::CSTAGES * C::CSTAGE_BYTES);
+    float* hstage = reinterpret_cast<float*>(cstage + C::CSTAGES * C::CSTAGE_BYTES);   // gate/up swapped: h
+    uint64_t* bars = reinterpret_cast<uint64_t*>(cstage + C::CSTAGES * C::CSTAGE_BYTES + C::HS_BYTES);
     uint64_t* full_t = bars;
     uint64_t* empty_t = full_t + C::TSTAGES;
     uint64_t* full_c = empty_t + C::TSTAGES;
@@ -498,7 +534,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
     uint64_t* acc_empty = acc_full + C::NBUF;
     uint64_t* drain_bar = acc_empty + C::NBUF;
     uint64_t* conv_done = drain_bar + 1;   // pair, odd CTA: its converters' local hand-off to the relay
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(conv_done + C::CSTAGES);
+    uint64_t* hs_full = conv_done + C::CSTAGES;   // gate/up swapped: h stage buffer written by every epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(hs_full + (C::SWAP_GU ? 2 : 0));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -523,6 +560,10 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             mbar_init(&acc_empty[i], (C::PAIR ? 2 : 1) * C::EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
+        if constexpr (C::SWAP_GU) {
+            mbar_init(&hs_full[0], C::EPI_WARPS);
+            mbar_init(&hs_full[1], C::EPI_WARPS);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -590,6 +631,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
         int buf = 0;
         uint32_t bph = 0;
         bool ok = true;
+        int hc = 0;   // gate/up swapped: 32-token chunks staged so far (h stage buffer hc & 1)
         // K splits: this CTA's partial tile of split s, [BM][ACC_N] fp32
         constexpr long kTileFloats = (long)C::BM * C::ACC_N;
         auto split_part = [&](const TileInfo& tt, int s_) -> float* {
@@ -605,8 +647,91 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     break;
                 }
                 tc_fence_after();
+                if constexpr (C::SWAP_GU) {
+                    // SwiGLU over the transposed accumulator, 32 tokens at a time: lane l < 16
+                    // holds gate f = 16q + l, lane l + 16 the up row of the same f; the two
+                    // swap halves so that each lane forms h for 16 of the 32 tokens
+                    const float s2 = p.scale2[ti.expert];
+                    const int nch = (ti.rows + 31) >> 5;
+                    const uint32_t acc0 = lane_addr + (uint32_t)(buf * C::MSUB * C::ACC_N);
+                    const bool hi = lane >= 16;
+                    const int fl = 16 * q + (lane & 15);
+                    // rounding: warp q takes f block q >> 1 of tokens 16 (q & 1) .. +15, two
+                    // lanes (16 f each) per token
+                    const int qblk = q >> 1, qtok = (q & 1) * 16 + (lane >> 1), qhalf = lane & 1;
+                    const int col = n0p + qblk * 32;
 #pragma unroll 1
-                for (int m = 0; m < C::MSUB; ++m) {
+                    for (int c = 0; c < nch; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(acc0 + c * 32, r);
+                        tmem_ld_wait();
+                        float* hb = hstage + (hc & 1) * C::HS_FLOATS;
+                        float* hw = hb + (hi ? 16 : 0) * C::HS_STRIDE + fl;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint32_t send = hi ? r[j] : r[16 + j];
+                            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                            const float gv = __uint_as_float(hi ? recv : r[j]) * s2;
+                            const float uv = __uint_as_float(hi ? r[16 + j] : recv) * s2;
+                            // silu(g) * u, the same fast intrinsics and cap as the unswapped form
+                            hw[j * C::HS_STRIDE] = __fdividef(gv, 1.0f + __expf(fminf(-gv, 80.0f))) * uv;
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&hs_full[hc & 1]);
+                        if (!mbar_wait(&hs_full[hc & 1], (uint32_t)((hc >> 1) & 1), abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                            ok = false;
+                            break;
+                        }
+                        const int tok = c * 32 + qtok;
+                        const float* hr = hb + qtok * C::HS_STRIDE + qblk * 32 + qhalf * 16;
+                        float h[16];
+                        float amax = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            h[i] = hr[i];
+                            amax = fmaxf(amax, fabsf(h[i]));
+                        }
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                        uint32_t packed[8];
+                        int sum = 0;
+                        float d = 0.f;
+                        if (amax > 0.f) {
+                            d = amax / 127.0f;
+                            const float rd = __frcp_rn(d);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                float v0 = roundf(h[2 * j] * rd), v1 = roundf(h[2 * j + 1] * rd);
+                                v0 = fminf(fmaxf(v0, -127.f), 127.f);
+                                v1 = fminf(fmaxf(v1, -127.f), 127.f);
+                                sum += (int)v0 + (int)v1;
+                                const __half2 hv = __floats2half2_rn(v0, v1);
+                                packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) packed[j] = 0;
+                        }
+                        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                        if (tok < ti.rows) {
+                            const long grow = (long)ti.row0 + tok;
+                            uint4* hq = reinterpret_cast<uint4*>(p.Hq + grow * p.F + col + qhalf * 16);
+                            hq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            hq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                            if (qhalf == 0) {
+                                const long bidx = grow * (p.F / 32) + col / 32;
+                                const __half d16 = __float2half_rn(d);
+                                p.Hd[bidx] = d16;
+                                p.Hs[bidx] = __float2half_rn(d * (float)sum);
+                                p.Hd32[((long)(ti.entry + (tok >> 7)) * (p.F / 32) + col / 32) * 128 + (tok & 127)] =
+                                    __half2float(d16);
+                            }
+                        }
+                        ++hc;
+                    }
+                    if (!ok) break;
+                }
+#pragma unroll 1
+                for (int m = 0; m < (C::SWAP_GU ? 0 : C::MSUB); ++m) {
                     if (m * 128 >= ti.rows) break;   // the MMA skipped this sub-tile: nothing to read
                     // row sub-tile m: rows m*128 + lane of this warp's quarter
                     const bool valid = m * 128 + row < ti.rows;
@@ -707,6 +832,65 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 if (++buf == C::NBUF) {
                     buf = 0;
                     bph ^= 1u;
+                }
+            } else if constexpr (C::SWAP) {
+                // FP8 fold, operands swapped: this thread's TMEM lane is weight row `row`
+                // (output column n0 + row), the accumulator's 256 columns the tile's token
+                // rows.  Warp cq of a lane quarter folds token columns [64 cq, 64 cq + 64),
+                // skipping the 16-column chunks past the tile's live rows.
+                constexpr int CPW = 64, LDW = 16;
+                const int cq = (warp - C::EPI_BASE) >> 2;
+                const int nld = min(CPW / LDW, max(0, (ti.rows - cq * CPW + LDW - 1) / LDW));
+                const int groups = p.K / C::GROUP_K;
+                float sum[CPW];
+#pragma unroll
+                for (int j = 0; j < CPW; ++j) sum[j] = 0.f;
+                // the tile's 128 weight rows are one scale block
+                const int wblk = n0p / 128;
+                const bool wblk_ok = wblk < p.N / 128;
+                for (int g = ti.kb0 / 2; g < ti.kb1 / 2; ++g) {
+                    const float s = wblk_ok ? __ldg(p.blk_scale + (long)wblk * groups + g) : 0.f;
+                    if (!mbar_wait(&acc_full[buf], bph, abort_flag, p.err, DEV_TIMEOUT_ACC)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t acc = lane_addr + (uint32_t)(buf * C::MSUB * C::ACC_N + cq * CPW);
+#pragma unroll
+                    for (int c = 0; c < CPW / LDW; ++c) {
+                        if (c < nld) {
+                            uint32_t r[LDW];
+                            tmem_ld16(acc + c * LDW, r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < LDW; ++j) sum[c * LDW + j] = fmaf(s, __uint_as_float(r[j]), sum[c * LDW + j]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                    if (++buf == C::NBUF) {
+                        buf = 0;
+                        bph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (ti.split >= 0) {
+                    // K split: the partial tile in the same [token row][weight row] layout
+                    // as the unswapped form (lanes write 32 consecutive columns)
+                    float* dst = split_part(ti, ti.s) + (long)(cq * CPW) * C::ACC_N + row;
+#pragma unroll
+                    for (int j = 0; j < CPW; ++j) dst[(long)j * C::ACC_N] = sum[j];
+                    continue;
+                }
+                const int col = n0p + row;
+                const int nrow = min(CPW, ti.rows - cq * CPW);
+                if (col < p.N && nrow > 0) {
+                    // Y[token][col]: the 32 lanes store 32 consecutive columns of one row
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.Y) + (long)(ti.row0 + cq * CPW) * p.ldy + col;
+#pragma unroll
+                    for (int j = 0; j < CPW; ++j)
+                        if (j < nrow) dst[(long)j * p.ldy] = __float2bfloat16_rn(sum[j]);
                 }
             } else {
                 // FP8 fold: one accumulator per 128-K block and row sub-tile, folded into
@@ -824,7 +1008,13 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                         // different stages and kinds overlap.
                         const int l0 = (s % C::TMA_GROUPS) * 4;
                         uint8_t* st = tstage + s * C::TSTAGE_BYTES;
-                        if (lane == l0) mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES);
+                        // A tile of at most 128 live rows reads only the first 128-row slice of
+                        // the activation tile: the CTA that would load the second slice skips
+                        // it, and every CTA of the cluster expects that many bytes less.
+                        constexpr bool kHalfA = QMM_HALF_A && !C::PAIR && C::CLUSTER_N == 2 && C::MSUB == 2;
+                        const bool half_a = kHalfA && ti.rows <= 128;
+                        if (lane == l0)
+                            mbar_arrive_expect_tx(&full_t[s], C::TSTAGE_BYTES - (half_a ? C::A_SLICE_ROWS * 128 : 0));
                         __syncwarp();
                         if (lane == l0) {
                             if constexpr (C::PAIR) {
@@ -832,7 +1022,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                                 tma_load_2d(st, &tmA, &full_t[s], kb * C::BK, ti.row0);
                             } else if constexpr (C::CLUSTER_N > 1) {
                                 // this CTA's slice of the activation tile, written into every CTA of the cluster
-                                tma_load_2d_multicast(st + crank * C::A_SLICE_ROWS * 128, &tmA, &full_t[s], kb * C::BK,
+                                if (!(half_a && crank == 1))
+                                    tma_load_2d_multicast(st + crank * C::A_SLICE_ROWS * 128, &tmA, &full_t[s], kb * C::BK,
                                                       ti.row0 + crank * C::A_SLICE_ROWS,
                                                       (uint16_t)((1u << C::CLUSTER_N) - 1));
                             } else {
@@ -882,6 +1073,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                     const TileInfo mi = mi_next;
                     if (t + ncl < num_tiles) mi_next = decode_tile<C>(p, t + ncl, crank);
                     const int nsub = (C::MSUB == 2 && mi.rows <= 128) ? 1 : C::MSUB;
+                    const uint32_t idesc_swap = idesc_kind_f16(128, min(256, max(16, (mi.rows + 15) & ~15)), true);
                     for (int kb = mi.kb0; kb < mi.kb1; ++kb) {
                         // Only the converted weights are waited on: the converters arrive on
                         // full_c after they saw this stage's TMA copies complete (full_t), so
@@ -936,13 +1128,22 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                             tc_commit_pair(&empty_c[cs], 3);
                             tc_commit_pair(&empty_t[ts], 3);
                         } else {
+                            if constexpr (C::SWAP) {
+                                // A: the converted weights (128 rows); B: the activation tile, N = its
+                                // live rows rounded up to 16
 #pragma unroll
-                            for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+                                for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk)
+                                    tc_mma_f16(dtmem, bd + (uint64_t)(kk * 2), ad + (uint64_t)(kk * 2), idesc_swap,
+                                               (first && kk == 0) ? 0u : 1u);
+                            } else {
 #pragma unroll
-                                for (int m = 0; m < C::MSUB; ++m)
-                                    if (m < nsub)
-                                        tc_mma_f16(dtmem + (uint32_t)(m * C::BN), ad + (uint64_t)(m * 1024 + kk * 2),
-                                                   bd + (uint64_t)(kk * 2), C::IDESC, (first && kk == 0) ? 0u : 1u);
+                                for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+#pragma unroll
+                                    for (int m = 0; m < C::MSUB; ++m)
+                                        if (m < nsub)
+                                            tc_mma_f16(dtmem + (uint32_t)(m * C::BN), ad + (uint64_t)(m * 1024 + kk * 2),
+                                                       bd + (uint64_t)(kk * 2), C::IDESC, (first && kk == 0) ? 0u : 1u);
+                                }
                             }
                             if (last) {
                                 tc_commit(&acc_full[buf]);
@@ -980,6 +1181,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             const int ct = C::conv_slot(warp) * 32 + lane;
             const int crow = ct % C::BN;                      // this thread's weight row in every tile
             const int chalf = ct / C::BN;                     // and its K half (TPR == 2)
+            const int cdrow = C::conv_dst_row(crow);          // its row in the operand tile
             int ts = 0, cs = 0;
             uint32_t tph = 0, cph = 0;
             bool ok = true;
@@ -1064,9 +1266,9 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 const uint32_t bconv = smem_u32(cstage + cs * C::CSTAGE_BYTES);
                 if constexpr (C::B == BMode::W4) {
                     if constexpr (C::TPR == 2)
-                        convert_w4_half(braw, bconv, crow, chalf, sbytes);
+                        convert_w4_half(braw, bconv, crow, cdrow, chalf, sbytes);
                     else
-                        convert_w4_row(braw, bconv, crow, sbytes);
+                        convert_w4_row(braw, bconv, crow, cdrow, sbytes);
                 } else {
                     convert_fp8_rows<C::RPT>(braw, bconv, crow, C::BN / C::RPT);
                 }
