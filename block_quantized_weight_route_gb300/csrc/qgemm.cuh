@@ -106,20 +106,23 @@ struct GemmCfg {
     static constexpr bool GROUPED = GROUPED_;
     static constexpr int BM = 128 * MSUB_, BN = BN_, BK = 64, UMMA_K = 16;
     static constexpr int CONV_WARPS = CONV_WARPS_, EPI_WARPS = EPI_WARPS_;
-    // 16 warps (20 for the FP8 fold).  Warp w runs on SM sub-partition w % 4; the MMA issuer (warp 1)
+    // 16 warps (20, 24 or 28 for the FP8 fold).  Warp w runs on SM sub-partition w % 4; the MMA issuer (warp 1)
     // must not share its sub-partition with ALU-heavy converter warps, or its
     // mbarrier waits are starved and the tensor pipe idles.
     static constexpr int EPI_BASE = (EPI_WARPS_ == 4) ? 12 : 4;
-    // 16 fold warps (FP8 with two row sub-tiles): 20 warps, five per
-    // sub-partition (a sixth would cap registers at 80), the two converters on
-    // warps 2 and 3
+    // 16 fold warps (FP8 with two row sub-tiles) and 2 converters: 20 warps, five
+    // per sub-partition, the converters on warps 2 and 3.
     // 16 fold warps with 4 converters: 24 warps launched at 80 registers a thread,
-    // the four fold warpgroups raised to 96 (two sub-tiles x 32 running sums), the
-    // other two lowered to 48 - the shares add up to exactly the launch's 24 x 80
-    static constexpr bool REG_SPLIT = (EPI_WARPS_ == 16 && CONV_WARPS_ == 4);
-    static constexpr int REGS_LAUNCH = 80, REGS_EPI = 96, REGS_OTHER = 48;
-    static_assert(!REG_SPLIT || 16 * REGS_EPI + 8 * REGS_OTHER == 24 * REGS_LAUNCH, "register shares = launch registers");
-    static constexpr int THREADS = REG_SPLIT ? 32 * 24 : ((EPI_WARPS_ == 16) ? 32 * 20 : 512);
+    // the four fold warpgroups raised to 96 (64 running sums a thread), the other
+    // two lowered to 48 - the shares add up to exactly the launch's 24 x 80.
+    // With 8 converters (two threads per weight row): 28 warps launched at 72, the
+    // fold warpgroups raised to 96 and the other three lowered to 40.
+    static constexpr bool REG_SPLIT = (EPI_WARPS_ == 16 && (CONV_WARPS_ == 4 || CONV_WARPS_ == 8));
+    static constexpr int SPLIT_WARPS = (CONV_WARPS_ == 8) ? 28 : 24;
+    static constexpr int REGS_LAUNCH = (CONV_WARPS_ == 8) ? 72 : 80, REGS_EPI = 96, REGS_OTHER = (CONV_WARPS_ == 8) ? 40 : 48;
+    static_assert(!REG_SPLIT || 16 * REGS_EPI + (SPLIT_WARPS - 16) * REGS_OTHER == SPLIT_WARPS * REGS_LAUNCH,
+                  "register shares = launch registers");
+    static constexpr int THREADS = REG_SPLIT ? 32 * SPLIT_WARPS : ((EPI_WARPS_ == 16) ? 32 * 20 : 512);
     // one CTA per SM: each sub-partition's 16384 registers shared by its warps,
     // in the allocation unit of 8 per thread
     static constexpr int WARPS_PER_SMSP = (THREADS / 32 + 3) / 4;
@@ -164,7 +167,7 @@ struct GemmCfg {
     static_assert(!FOLD || FOLD_CPW % 8 == 0, "fold columns per warp: whole 16-byte runs");
     static_assert(GROUPED_ || 128 * MSUB_ * ACC_N <= 65536, "split partial tile at most 256 x 256");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
-    static_assert(TPR == 1 || (TPR == 2 && B_ == BMode::W4), "one or (W4) two converter threads per weight row");
+    static_assert(TPR == 1 || TPR == 2, "one or two converter threads per weight row");
     static_assert(CONV_WARPS * 32 * RPT == TPR * BN, "converters cover the weight rows");
     static_assert(RPT == 1 || (RPT == 2 && B_ == BMode::FP8), "two rows per converter thread: FP8 only");
     static_assert(MSUB == 1 || MSUB == 2, "row sub-tiles");
@@ -172,7 +175,7 @@ struct GemmCfg {
     static_assert(NBUF >= 1, "TMEM columns");
     static_assert(CLUSTER_N == 1 || CLUSTER_N == 2 || CLUSTER_N == 4, "cluster size");
     static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4) ||
-                      (EPI_WARPS == 16 && (CONV_WARPS == 2 || CONV_WARPS == 4)),
+                      (EPI_WARPS == 16 && (CONV_WARPS == 2 || CONV_WARPS == 4 || CONV_WARPS == 8)),
                   "warp layout");
     // relay threads of a pair's odd CTA: lane 0 of the MMA warp (slot 0) and of the
     // warps without a role (slots 1, 2: warps 5 and 9 with 4 epilogue warps)
@@ -193,12 +196,16 @@ struct GemmCfg {
     // converter slot of a warp, -1 if it is not a converter:
     //   4 epilogue warps (12..15):  converters on warps 2,3,4,6,7,8,10,11
     //   8 epilogue warps (4..11):   converters on warps 2,3,12,14
-    //   16 epilogue warps (4..19):  converters on warps 2,3 (and 20, 23 with four)
+    //   16 epilogue warps (4..19):  converters on warps 2,3 (and 20, 23 with four;
+    //                               20, 22, 23, 24, 26, 27 with eight)
     __device__ static int conv_slot(int warp) {
         if constexpr (EPI_WARPS == 16) {
             if (warp == 2 || warp == 3) return warp - 2;
             if (CONV_WARPS == 4 && warp == 20) return 2;
             if (CONV_WARPS == 4 && warp == 23) return 3;
+            // 8 converters: warps 2, 3, 20, 22, 23, 24, 26, 27 (none on sub-partition 1)
+            if (CONV_WARPS == 8 && warp >= 20 && warp < 28)
+                return (int)((0x87065403u >> (4 * (warp - 20))) & 15u) - 1;   // slot + 1 per warp, one nibble each
             return -1;
         } else {
             // slot + 1 per warp, one nibble each (0: not a converter)
@@ -403,6 +410,29 @@ __device__ __forceinline__ void convert_fp8_rows(uint32_t raw_tile, uint32_t dst
             sts128(dst_tile + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
             sts128(dst_tile + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
         }
+    }
+}
+
+// FP8, half a row: the 32 E4M3 bytes of K half h (two 16-byte chunks).
+__device__ __forceinline__ void convert_fp8_half(uint32_t raw_tile, uint32_t dst_tile, int r, int h) {
+    const int sw = (r >> 1) & 3;
+    uint4 v[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) v[i] = lds128(raw_tile + r * 64 + (((2 * h + i) ^ sw) << 4));
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t words[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t hh[2];
+            cvt_e4m3x4_f16x2(words[w], hh);
+            o[2 * w] = bf16x2_mul(f16x2_to_bf16x2_2m112(hh[0]), kBf16x2_2p112);
+            o[2 * w + 1] = bf16x2_mul(f16x2_to_bf16x2_2m112(hh[1]), kBf16x2_2p112);
+        }
+        const int c = 2 * h + i;
+        sts128(dst_tile + sw128_off(r, 2 * c), o[0], o[1], o[2], o[3]);
+        sts128(dst_tile + sw128_off(r, 2 * c + 1), o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -1269,6 +1299,8 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                         convert_w4_half(braw, bconv, crow, cdrow, chalf, sbytes);
                     else
                         convert_w4_row(braw, bconv, crow, cdrow, sbytes);
+                } else if constexpr (C::TPR == 2) {
+                    convert_fp8_half(braw, bconv, crow, chalf);
                 } else {
                     convert_fp8_rows<C::RPT>(braw, bconv, crow, C::BN / C::RPT);
                 }
