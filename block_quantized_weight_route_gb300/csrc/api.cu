@@ -459,7 +459,7 @@ static qmm_status run_gate_up(DeviceState* d, const uint16_t* Xp, int P, int D, 
     const TileShape sh = w4_gate_up_shape();
     const int hstep = sh.bn / 2;
     if (F % hstep) return fail(QMM_ERR_UNSUPPORTED_SHAPE, "expert stage: F %% %d != 0 (F=%d)", hstep, F);
-    const int gu_cn = cluster_for(F / hstep);
+    const int gu_cn = gate_up_cluster(F / hstep);
     CUtensorMap ta, tb;
     if ((st = make_tmap(&ta, Xp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, P, (uint64_t)D * 2, 64, sh.rows / gu_cn,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)

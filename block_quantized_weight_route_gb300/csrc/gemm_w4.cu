@@ -68,6 +68,19 @@ int cluster_for(int n_tiles) {
     if (QMM_MAX_CLUSTER >= 2 && n_tiles % 2 == 0) return 2;
     return 1;
 }
+// Gate/up: no clusters.  A multicast activation stage is refilled only once the
+// MMAs of both CTAs have read it, which couples the two CTAs' pipelines; each CTA
+// loading its own activation tiles was faster (5268-token stage: 0.349 against
+// 0.355 ms; 21504 tokens: 1.67 against 1.71 ms).
+#ifndef QMM_GU_MAX_CLUSTER
+#define QMM_GU_MAX_CLUSTER 1
+#endif
+int gate_up_cluster(int n_tiles) {
+    if (QMM_PAIR) return cluster_for(n_tiles);   // the CTA-pair build: pairs wherever they fit
+    if (QMM_GU_MAX_CLUSTER >= 4 && n_tiles % 4 == 0) return 4;
+    if (QMM_GU_MAX_CLUSTER >= 2 && n_tiles % 2 == 0) return 2;
+    return 1;
+}
 
 cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                cudaStream_t s) {

@@ -54,6 +54,7 @@ struct GemmParams {
 // cluster of cn loads that slice and multicasts it), tmB for the raw weight
 // codes; cn must divide p.n_tiles (cluster_for picks it).
 int cluster_for(int n_tiles);
+int gate_up_cluster(int n_tiles);   // the same choice for the gate/up GEMM
 cudaError_t launch_w4a16_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
                                cudaStream_t s);
 cudaError_t launch_w4_gate_up_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int cn,
