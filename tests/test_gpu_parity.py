@@ -255,7 +255,10 @@ def test_router_projection_then_expert_stage(qlib):
 
 # ---------------------------------------------------------------- dense FP8 block-128
 
-@pytest.mark.parametrize("M,K,N", [(130, 384, 256), (1, 128, 128), (257, 640, 384), (300, 2048, 640)])
+# (300, 512, 512) and (40, 1024, 256) run in clusters of 2 with a last row tile of
+# at most 128 rows, whose second activation slice is not loaded.
+@pytest.mark.parametrize("M,K,N", [(130, 384, 256), (1, 128, 128), (257, 640, 384), (300, 2048, 640), (300, 512, 512),
+                                   (40, 1024, 256)])
 def test_fp8_blk128_matches_oracle(qlib, M, K, N):
     g = wl.gen_fp8_blk128(M, K, N, seed=M * 3 + N)
     Y = qlib.qmm_fp8_blk128(bf16_dev(g["X"]), dev(g["W"]), dev(g["S"]))
