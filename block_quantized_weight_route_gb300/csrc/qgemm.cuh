@@ -1,7 +1,7 @@
 // Warp-specialised block-quantised GEMM for sm_103a (one CTA per SM, persistent).
 //
 //   warp 0        : TMA producer (activations tile + raw quantised weight tile)
-//   warp 1        : TMEM owner and MMA issuer (one elected thread issues tcgen05.mma)
+//   warp 1        : TMEM owner and MMA issuer (one thread issues tcgen05.mma)
 //   epilogue warps: read fp32 accumulators from TMEM, scale / fold / quantise, store
 //                   (12..15; 4..19 for the FP8 fold over two row sub-tiles)
 //   converter warps: turn raw weight codes into the exact 16-bit operand tiles
@@ -10,7 +10,9 @@
 //
 // Tile: 128*MSUB rows (tokens) x BN columns (weight rows), K step 64.  The MMA
 // is tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16), MSUB of them per K
-// step (one per 128-row sub-tile), fp32 accumulation in TMEM.  Operands are
+// step (one per 128-row sub-tile), fp32 accumulation in TMEM; or, with the
+// operands swapped (FP8 fold, gate/up), one M=128 (weight rows), N=256 (token
+// rows) MMA per K step, the accumulator transposed.  Operands are
 // K-major in the canonical 128-byte-swizzled layout.  Dense problems whose last
 // wave of tiles would leave half the clusters idle split those tiles along K
 // (fp32 partials in the caller's workspace, added in split order by
