@@ -334,13 +334,16 @@ __device__ __forceinline__ uint32_t w4_scale_bf16x2(uint32_t byte) {
     return u | (u << 16);
 }
 
-// IQ4_NL codebook + 128 as bytes (index 0..15), four per word.
-constexpr uint32_t kIq4T0 = 0x3F2D1801u;   // -127 -104  -83  -65
-constexpr uint32_t kIq4T1 = 0x766A5D4Fu;   //  -49  -35  -22  -10
-constexpr uint32_t kIq4T2 = 0xA6998D81u;   //    1   13   25   38
-constexpr uint32_t kIq4T3 = 0xF1D9C5B5u;   //   53   69   89  113
-// f16 bits 0x64XX are 1024 + XX; subtracting 1152 leaves XX - 128.
+// f16 bits 0x64XX are 1024 + XX; subtracting 1152 leaves XX - 128 (int8 codes
+// biased by 128 into exact f16).
 constexpr uint32_t kF16x2_1152 = 0x64806480u;
+// The f16 bit patterns of the IQ4_NL codebook values (index 0..15: -127 -104 -83
+// -65 -49 -35 -22 -10 1 13 25 38 53 69 89 113) as a low-byte and a high-byte
+// table, four entries per word: the expansion needs only byte permutes, no f16
+// arithmetic on the FMA pipes that the down product's fold uses (measured: the
+// down product 2% faster than building value + 128 and subtracting in f16).
+constexpr uint32_t kIq4L0 = 0x103080F0u, kIq4L1 = 0x00806020u, kIq4L2 = 0xC0408000u, kIq4L3 = 0x109050A0u;
+constexpr uint32_t kIq4H0 = 0xD4D5D6D7u, kIq4H1 = 0xC9CDD0D2u, kIq4H2 = 0x504E4A3Cu, kIq4H3 = 0x57555452u;
 
 // ---------------------------------------------------------------------------
 // Row converters: one thread turns one row of raw codes for a 64-wide K block
@@ -449,16 +452,16 @@ __device__ __forceinline__ void convert_iq4_row(uint32_t raw_tile, uint32_t dst_
         const uint32_t x = words[w];
         const uint32_t x4 = x << 4;
         const uint32_t xh = x >> 16;
-        // elements 0..3 (low 16 bits) and 4..7 (high 16 bits): codebook byte from
-        // entries 0-7 or 8-15 chosen by bit 3 of each index
-        const uint32_t v_a = bitselect(prmt(kIq4T0, kIq4T1, x), prmt(kIq4T2, kIq4T3, x & 0x7777u), prmt(x4, x, 0xD9C8u));
-        const uint32_t v_b =
-            bitselect(prmt(kIq4T0, kIq4T1, xh), prmt(kIq4T2, kIq4T3, xh & 0x7777u), prmt(x4, x, 0xFBEAu));
-        const uint32_t o0 = f16x2_sub(prmt(v_a, 0x64646464u, 0x5140u), kF16x2_1152);
-        const uint32_t o1 = f16x2_sub(prmt(v_a, 0x64646464u, 0x5342u), kF16x2_1152);
-        const uint32_t o2 = f16x2_sub(prmt(v_b, 0x64646464u, 0x5140u), kF16x2_1152);
-        const uint32_t o3 = f16x2_sub(prmt(v_b, 0x64646464u, 0x5342u), kF16x2_1152);
-        sts128(dst_tile + sw128_off(r, w), o0, o1, o2, o3);
+        // elements 0..3 (low 16 bits) and 4..7 (high 16 bits): table entries 0-7 or
+        // 8-15 chosen by bit 3 of each index (a byte mask of it by sign replication)
+        const uint32_t ma = prmt(x4, x, 0xD9C8u), mb = prmt(x4, x, 0xFBEAu);
+        // low and high bytes of the f16 values, interleaved into f16 pairs
+        const uint32_t la = bitselect(prmt(kIq4L0, kIq4L1, x), prmt(kIq4L2, kIq4L3, x & 0x7777u), ma);
+        const uint32_t ha = bitselect(prmt(kIq4H0, kIq4H1, x), prmt(kIq4H2, kIq4H3, x & 0x7777u), ma);
+        const uint32_t lb = bitselect(prmt(kIq4L0, kIq4L1, xh), prmt(kIq4L2, kIq4L3, xh & 0x7777u), mb);
+        const uint32_t hb = bitselect(prmt(kIq4H0, kIq4H1, xh), prmt(kIq4H2, kIq4H3, xh & 0x7777u), mb);
+        sts128(dst_tile + sw128_off(r, w), prmt(la, ha, 0x5140u), prmt(la, ha, 0x7362u), prmt(lb, hb, 0x5140u),
+               prmt(lb, hb, 0x7362u));
     }
 }
 
