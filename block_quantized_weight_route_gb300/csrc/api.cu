@@ -316,24 +316,25 @@ qmm_status qmm_fp8_blk128_ws(const uint16_t* X, int M, int K, int N, const uint8
 // ---------------------------------------------------------------- dense Q8_0 x q8_1
 
 // Workspace of qmm_q8_0_q8_1: f16 activation codes [M][K], the activations' d per
-// 128-row tile [entries][K/32][128] fp32, the tile list and its count.
-static void q8_layout(int M, int K, size_t* off) {
+// 128-row tile [entries][K/32][128] fp32, the tile list and its count, and the
+// weight codes as f16 [N][K] (the kernel reads both operands expanded).
+static void q8_layout(int M, int K, int N, size_t* off) {
     const int entries = (M + 127) / 128;
-    const size_t sz[4] = {(size_t)M * K * 2, (size_t)entries * (K / 32) * 128 * 4, (size_t)entries * 16, 16};
+    const size_t sz[5] = {(size_t)M * K * 2, (size_t)entries * (K / 32) * 128 * 4, (size_t)entries * 16, 16,
+                          q8_weights_f16() ? (size_t)N * K * 2 : 0};
     size_t o = 0;
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 5; ++i) {
         off[i] = o;
         o = align_up(o + sz[i], 256);
     }
-    off[4] = o;
+    off[5] = o;
 }
 
 size_t qmm_q8_0_q8_1_workspace_size(int M, int K, int N) {
-    (void)N;
-    if (M < 1 || K < 256 || K % 256) return 0;
-    size_t off[5];
-    q8_layout(M, K, off);
-    return off[4];
+    if (M < 1 || K < 256 || K % 256 || N < 128 || N % 128) return 0;
+    size_t off[6];
+    q8_layout(M, K, N, off);
+    return off[5];
 }
 
 qmm_status qmm_q8_0_q8_1(const int8_t* Xq, const uint16_t* Xd, int M, int K, int N, const int8_t* Wq,
@@ -352,21 +353,27 @@ qmm_status qmm_q8_0_q8_1(const int8_t* Xq, const uint16_t* Xd, int M, int K, int
     DeviceState* d = nullptr;
     qmm_status st = device_state(&d);
     if (st != QMM_OK) return st;
-    size_t off[5];
-    q8_layout(M, K, off);
+    size_t off[6];
+    q8_layout(M, K, N, off);
     uint8_t* base = static_cast<uint8_t*>(ws);
     __half* X16 = reinterpret_cast<__half*>(base + off[0]);
     float* dX32 = reinterpret_cast<float*>(base + off[1]);
     int4* tiles = reinterpret_cast<int4*>(base + off[2]);
     int32_t* count = reinterpret_cast<int32_t*>(base + off[3]);
+    __half* W16 = reinterpret_cast<__half*>(base + off[4]);
     const int entries = (M + 127) / 128;
+    const bool wf16 = q8_weights_f16();
     cudaError_t e = launch_dense_tiles(M, tiles, count, stream);
     if (e == cudaSuccess) e = launch_codes_i8_to_f16(Xq, X16, (long)M * K, stream);
+    if (e == cudaSuccess && wf16) e = launch_codes_i8_to_f16(Wq, W16, (long)N * K, stream);
     if (e == cudaSuccess)
         e = launch_hd_to_entries(reinterpret_cast<const __half*>(Xd), tiles, count, entries, K / 32, dX32, stream);
     if (e != cudaSuccess) return cuda_fail(e, "qmm_q8_0_q8_1: operand layout");
     CUtensorMap ta, tb, tw;
-    if ((st = make_tmap(&ta, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) != QMM_OK)
+    if ((st = wf16 ? make_tmap(&ta, W16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, N, (uint64_t)K * 2, 64, 128,
+                               CU_TENSOR_MAP_SWIZZLE_128B)
+                    : make_tmap(&ta, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+        QMM_OK)
         return st;
     if ((st = make_tmap(&tb, X16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, M, (uint64_t)K * 2, 64, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != QMM_OK)

@@ -22,8 +22,10 @@
 // by a TMA box [128 rows][8 blocks] fp16 and d_X by a bulk copy of the chunk's
 // [8 blocks][128 rows] fp32 from a per-128-row-tile layout a pre-pass writes.
 //
-//   warp 0: TMA producer (Q8_0 codes + f16 activation codes per K step of 64,
-//           scale chunks); warp 2: MMA issuer; warps 1, 3: int8 -> f16 converters;
+//   warp 0: TMA producer (the weight and activation codes as f16 per K step of
+//           64 - both expanded once per call by a pre-pass - and the scale
+//           chunks); warp 2: MMA issuer; (with int8 weight codes, build option
+//           QMM_Q8_WF16=0: warps 1, 3 expand them per K step);
 //   warps 4..11: epilogue (two per TMEM lane quarter, 64 token columns each),
 //           accumulators handed over two 32-K blocks at a time;
 //   warps 12..15: the q8_1 rounding of each finished tile, which the epilogue
@@ -32,15 +34,25 @@
 
 namespace qmm {
 
+// WF16: the weight codes arrive already expanded to f16 (a pre-pass per call,
+// like the activations), so the TMA stage holds both MMA operands as loaded and
+// there are no converter warps: their f16 subtracts would share the FMA pipes
+// with the fold, and their stores shared memory with the MMA.  Measured at
+// M=2048, K=5120, N=8064 (whole call, pre-passes included): 0.514 ms against
+// 0.540 with the int8 codes expanded per K step in the kernel.
+#ifndef QMM_Q8_WF16
+#define QMM_Q8_WF16 1
+#endif
 #ifndef QMM_Q8_TSTAGES
-#define QMM_Q8_TSTAGES 3
+#define QMM_Q8_TSTAGES (QMM_Q8_WF16 ? 4 : 3)
 #endif
 #ifndef QMM_Q8_CSTAGES
-#define QMM_Q8_CSTAGES 3
+#define QMM_Q8_CSTAGES (QMM_Q8_WF16 ? 0 : 3)
 #endif
 struct Q8Cfg {
     static constexpr int BM = 128, BN = 128, BK = 64, GROUP_K = 32;
-    static constexpr int EPI_WARPS = 8, EPI_BASE = 4, CPW = 64, CONV_WARPS = 2;
+    static constexpr bool WF16 = QMM_Q8_WF16 != 0;
+    static constexpr int EPI_WARPS = 8, EPI_BASE = 4, CPW = 64, CONV_WARPS = WF16 ? 0 : 2;
     // 16 warps launched at 128 registers a thread: the two epilogue warpgroups
     // raised to 168 (running sums + two 32-column loads), the other two lowered to
     // 88 - the shares add up to exactly the launch's 16 x 128.  Warps 12..15 round
@@ -57,10 +69,10 @@ struct Q8Cfg {
     static constexpr int TMA_GROUPS = TSTAGES;
     static constexpr int CHUNK_STEPS = 4;                         // K steps of 64 per scale chunk
     static constexpr int CHUNK_BLOCKS = CHUNK_STEPS * BK / GROUP_K;   // 8 blocks of 32
-    static constexpr int A_RAW_BYTES = BM * BK;                   // int8 weight codes, 64-byte rows
+    static constexpr int A_RAW_BYTES = WF16 ? BM * BK * 2 : BM * BK;   // weight codes: f16 128-byte or int8 64-byte rows
     static constexpr int B_BYTES = BN * BK * 2;                   // f16 activation codes, 128-byte rows
     static constexpr int TSTAGE_BYTES = A_RAW_BYTES + B_BYTES;
-    static constexpr int CSTAGE_BYTES = BM * BK * 2;              // expanded weight codes
+    static constexpr int CSTAGE_BYTES = WF16 ? 0 : BM * BK * 2;   // expanded weight codes
     static constexpr int DX_BYTES = CHUNK_BLOCKS * BN * 4;        // [block][token] fp32
     static constexpr int DW_BYTES = BM * CHUNK_BLOCKS * 2;        // [row][block] fp16
     static constexpr int SSTAGE_BYTES = 8192;                     // DX + DW, padded to 1 KB multiples
@@ -71,6 +83,7 @@ struct Q8Cfg {
                                       SSTAGES * SSTAGE_BYTES + YS_BYTES + BAR_COUNT * 8 + 64;
     static_assert(DX_BYTES + DW_BYTES <= SSTAGE_BYTES, "scale stage");
     static_assert(TSTAGE_BYTES % 1024 == 0 && CSTAGE_BYTES % 1024 == 0 && SSTAGE_BYTES % 1024 == 0, "align");
+    static_assert(WF16 == (CSTAGES == 0), "converted stages only with int8 weight codes");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -108,7 +121,8 @@ struct Q8Out {
     int M;
 };
 
-// tmA: Q8_0 codes [N][K] int8, box {64, 128}, 64-byte swizzle.
+// tmA: Q8_0 codes [N][K] int8, box {64, 128}, 64-byte swizzle; or (WF16) the same
+// codes as f16 values, box {64, 128}, 128-byte swizzle.
 // tmB: activation codes [M][K] f16, box {64, 128}, 128-byte swizzle.
 // tmW: weight scales [N][K/32] fp16, box {8, 128}, no swizzle.
 __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
@@ -140,7 +154,7 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::TSTAGES; ++i) {
             mbar_init(&full_t[i], 1);
-            mbar_init(&empty_t[i], C::CONV_WARPS + 1);   // converters (codes read) + MMA commit
+            mbar_init(&empty_t[i], C::CONV_WARPS + 1);   // converters (codes read, int8 form) + MMA commit
         }
         for (int i = 0; i < C::CSTAGES; ++i) {
             mbar_init(&full_c[i], C::CONV_WARPS);
@@ -337,17 +351,20 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
             // ------------------------------------------------------------ MMA issuer (one lane)
             if (lane == 0) {
                 int cs = 0, ts = 0, buf = 0;
-                uint32_t cph = 0, bph = 0;
+                uint32_t cph = 0, bph = 0, tph = 0;
                 bool ok = true;
                 for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                     for (int kb = 0; kb < ksteps && ok; ++kb) {
-                        // converted weights ready: the converters arrive on full_c only after they
-                        // saw the TMA stage (weight and activation codes) complete
-                        if (!mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV)) {
+                        // WF16: both operands as loaded (the TMA stage); int8 form: converted
+                        // weights ready - the converters arrive on full_c only after they saw the
+                        // TMA stage (weight and activation codes) complete
+                        if (!(C::WF16 ? mbar_wait(&full_t[ts], tph, abort_flag, p.err, DEV_TIMEOUT_TMA_FULL)
+                                      : mbar_wait(&full_c[cs], cph, abort_flag, p.err, DEV_TIMEOUT_CONV))) {
                             ok = false;
                             break;
                         }
-                        const uint64_t ad = smem_desc_sw128(smem_u32(cstage + cs * C::CSTAGE_BYTES));
+                        const uint64_t ad = smem_desc_sw128(C::WF16 ? smem_u32(tstage + ts * C::TSTAGE_BYTES)
+                                                                    : smem_u32(cstage + cs * C::CSTAGE_BYTES));
                         const uint64_t bd = smem_desc_sw128(smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES);
                         // the step's two 32-K blocks, each into its own accumulator: the two
                         // buffers of hand-off pair buf
@@ -368,20 +385,25 @@ __global__ void __launch_bounds__(Q8Cfg::THREADS, 1)
                             buf = 0;
                             bph ^= 1u;
                         }
-                        tc_commit(&empty_c[cs]);
-                        tc_commit(&empty_t[ts]);
-                        if (++cs == C::CSTAGES) {
-                            cs = 0;
-                            cph ^= 1u;
+                        if constexpr (!C::WF16) {
+                            tc_commit(&empty_c[cs]);
+                            if (++cs == C::CSTAGES) {
+                                cs = 0;
+                                cph ^= 1u;
+                            }
                         }
-                        if (++ts == C::TSTAGES) ts = 0;
+                        tc_commit(&empty_t[ts]);
+                        if (++ts == C::TSTAGES) {
+                            ts = 0;
+                            tph ^= 1u;
+                        }
                     }
                 }
                 tc_commit(drain_bar);
                 drain_ring(drain_bar, 1, 1, p.err);
             }
             __syncwarp();
-        } else if (warp == 1 || warp == 3) {
+        } else if (!C::WF16 && (warp == 1 || warp == 3)) {
             // ------------------------------------------------------------ converters (int8 -> f16)
             const int ct = (warp == 1 ? 0 : 1) * 32 + lane;
             int ts = 0, cs = 0;
@@ -490,6 +512,7 @@ cudaError_t launch_dense_tiles(int M, int4* tiles, int32_t* num_entries, cudaStr
 }
 
 int smem_q8_dense() { return Q8Cfg::SMEM_BYTES; }
+bool q8_weights_f16() { return Q8Cfg::WF16; }
 
 cudaError_t launch_q8_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmW, const GemmParams& p,
                             int8_t* Yq, __half* Yd, __half* Ys, float* Y, int M, int grid, cudaStream_t s) {

@@ -77,9 +77,11 @@ cudaError_t launch_iq4_down(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
 int smem_iq4_down();
 
 // Dense Q8_0 x q8_1 projection re-quantised to q8_1 (gemm_q8.cu): tmA Q8_0 codes
-// [N][K] int8, tmB activation codes [M][K] f16, tmW weight scales [N][K/32] fp16;
+// [N][K] int8 (or, when q8_weights_f16(), the same codes as f16, 128-byte swizzle),
+// tmB activation codes [M][K] f16, tmW weight scales [N][K/32] fp16;
 // p.tiles / num_entries: 128-row tiles of M (launch_dense_tiles), p.dH32: the
 // activations' d per tile [entry][K/32][128] fp32.
+bool q8_weights_f16();
 cudaError_t launch_dense_tiles(int M, int4* tiles, int32_t* num_entries, cudaStream_t s);
 cudaError_t launch_q8_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmW, const GemmParams& p,
                             int8_t* Yq, __half* Yd, __half* Ys, float* Y, int M, int grid, cudaStream_t s);

@@ -121,7 +121,9 @@ qmm_status qmm_fp8_blk128_ws(const uint16_t *X, int M, int K, int N, const uint8
  *   Wq [N][K] int8, Wd [N][K/32] fp16 (Q8_0: 32 codes and one scale per block);
  *   Yq [M][N] int8, Yd / Ys [M][N/32] fp16; Y [M][N] fp32 before the rounding, or NULL.
  *   ws: device scratch of at least qmm_q8_0_q8_1_workspace_size(M, K, N) bytes,
- *   256-byte aligned (the activation codes as f16 and per-tile d tables).
+ *   256-byte aligned (both operands' codes as f16 -- 2 (M + N) K bytes -- and
+ *   per-tile d tables); qmm_q8_0_q8_1_workspace_size returns 0 for a shape it
+ *   does not take.
  * Shapes: M >= 1, K % 256 == 0, N % 128 == 0.
  */
 size_t qmm_q8_0_q8_1_workspace_size(int M, int K, int N);

@@ -96,8 +96,9 @@ def test_argument_checks_return_before_any_device_work(L):
     assert L.qmm_q8_0_q8_1(None, None, 64, 256, 128, *([None] * 7), 1 << 30, None) == 1
     L.qmm_q8_0_q8_1_workspace_size.restype = sz
     L.qmm_q8_0_q8_1_workspace_size.argtypes = [ctypes.c_int] * 3
-    assert L.qmm_q8_0_q8_1_workspace_size(2048, 5120, 8064) >= 2048 * 5120 * 2
+    assert L.qmm_q8_0_q8_1_workspace_size(2048, 5120, 8064) >= (2048 + 8064) * 5120 * 2   # both operands as f16
     assert L.qmm_q8_0_q8_1_workspace_size(2048, 100, 8064) == 0
+    assert L.qmm_q8_0_q8_1_workspace_size(2048, 5120, 100) == 0
     # the stage with options: an unknown flag bit is rejected before any device work
     L.moe_expert_stage_w4_iq4_ex.restype = ctypes.c_int
     L.moe_expert_stage_w4_iq4_ex.argtypes = [P, P] + [ctypes.c_int] * 5 + [P] * 7 + [sz, ctypes.c_uint, P]
