@@ -111,7 +111,10 @@ struct GemmCfg {
     // 16 warps (20, 24 or 28 for the FP8 fold).  Warp w runs on SM sub-partition w % 4; the MMA issuer (warp 1)
     // must not share its sub-partition with ALU-heavy converter warps, or its
     // mbarrier waits are starved and the tensor pipe idles.
-    static constexpr int EPI_BASE = (EPI_WARPS_ == 4) ? 12 : 4;
+    // WIDE16: the wide W4 tile (256 weight rows) with 16 converter warps, two
+    // threads per weight row: 28 warps, the epilogue on warps 24..27
+    static constexpr bool WIDE16 = (B_ == BMode::W4 && E_ == Epi::STORE && BN_ == 256 && CONV_WARPS_ == 16);
+    static constexpr int EPI_BASE = WIDE16 ? 24 : ((EPI_WARPS_ == 4) ? 12 : 4);
     // 16 fold warps (FP8 with two row sub-tiles) and 2 converters: 20 warps, five
     // per sub-partition, the converters on warps 2 and 3.
     // 16 fold warps with 4 converters: 24 warps launched at 80 registers a thread,
@@ -119,10 +122,11 @@ struct GemmCfg {
     // two lowered to 48 - the shares add up to exactly the launch's 24 x 80.
     // With 8 converters (two threads per weight row): 28 warps launched at 72, the
     // fold warpgroups raised to 96 and the other three lowered to 40.
-    static constexpr bool REG_SPLIT = (EPI_WARPS_ == 16 && (CONV_WARPS_ == 4 || CONV_WARPS_ == 8));
-    static constexpr int SPLIT_WARPS = (CONV_WARPS_ == 8) ? 28 : 24;
-    static constexpr int REGS_LAUNCH = (CONV_WARPS_ == 8) ? 72 : 80, REGS_EPI = 96, REGS_OTHER = (CONV_WARPS_ == 8) ? 40 : 48;
-    static_assert(!REG_SPLIT || 16 * REGS_EPI + (SPLIT_WARPS - 16) * REGS_OTHER == SPLIT_WARPS * REGS_LAUNCH,
+    static constexpr bool REG_SPLIT = (EPI_WARPS_ == 16 && (CONV_WARPS_ == 4 || CONV_WARPS_ == 8)) || WIDE16;
+    static constexpr int SPLIT_WARPS = (CONV_WARPS_ == 8 || WIDE16) ? 28 : 24;
+    static constexpr int REGS_LAUNCH = (CONV_WARPS_ == 8 || WIDE16) ? 72 : 80;
+    static constexpr int REGS_EPI = WIDE16 ? 120 : 96, REGS_OTHER = WIDE16 ? 64 : ((CONV_WARPS_ == 8) ? 40 : 48);
+    static_assert(!REG_SPLIT || EPI_WARPS_ * REGS_EPI + (SPLIT_WARPS - EPI_WARPS_) * REGS_OTHER == SPLIT_WARPS * REGS_LAUNCH,
                   "register shares = launch registers");
     static constexpr int THREADS = REG_SPLIT ? 32 * SPLIT_WARPS : ((EPI_WARPS_ == 16) ? 32 * 20 : 512);
     // one CTA per SM: each sub-partition's 16384 registers shared by its warps,
@@ -177,7 +181,7 @@ struct GemmCfg {
     static_assert(NBUF >= 1, "TMEM columns");
     static_assert(CLUSTER_N == 1 || CLUSTER_N == 2 || CLUSTER_N == 4, "cluster size");
     static_assert((EPI_WARPS == 4 && CONV_WARPS == 8) || (EPI_WARPS == 8 && CONV_WARPS == 4) ||
-                      (EPI_WARPS == 16 && (CONV_WARPS == 2 || CONV_WARPS == 4 || CONV_WARPS == 8)),
+                      (EPI_WARPS == 16 && (CONV_WARPS == 2 || CONV_WARPS == 4 || CONV_WARPS == 8)) || WIDE16,
                   "warp layout");
     // relay threads of a pair's odd CTA: lane 0 of the MMA warp (slot 0) and of the
     // warps without a role (slots 1, 2: warps 5 and 9 with 4 epilogue warps)
@@ -201,6 +205,12 @@ struct GemmCfg {
     //   16 epilogue warps (4..19):  converters on warps 2,3 (and 20, 23 with four;
     //                               20, 22, 23, 24, 26, 27 with eight)
     __device__ static int conv_slot(int warp) {
+        if constexpr (WIDE16) {
+            // warps 2..22 not on sub-partition 1: 2,3,4,6,7,8,10,11,12,14,15,16,18,19,20,22
+            if (warp < 2 || warp > 22 || (warp & 3) == 1) return -1;
+            const int r = warp - 2 - (warp - 1) / 4;   // drop the sub-partition-1 warps below
+            return r < 16 ? r : -1;
+        }
         if constexpr (EPI_WARPS == 16) {
             if (warp == 2 || warp == 3) return warp - 2;
             if (CONV_WARPS == 4 && warp == 20) return 2;
