@@ -33,9 +33,14 @@ using CfgW4Dense = GemmCfg<BMode::W4, Epi::STORE, 128, 8, 4, 4, 3, false, CN, 2>
 #ifndef QMM_GU_SWAP
 #define QMM_GU_SWAP 1
 #endif
+// 16 converter warps, four threads per weight row (a quarter row each; 28 warps
+// under a 120 / 64 register split): 0.3486 against 0.3499 ms with 8 at T=5268.
+#ifndef QMM_GU_CONV
+#define QMM_GU_CONV 16
+#endif
 template <int CN>
-using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, 8, 4, QMM_GU_TSTAGES, QMM_GU_CSTAGES, true, CN, 2, false,
-                            QMM_GU_SWAP != 0>;
+using CfgW4GateUp = GemmCfg<BMode::W4, Epi::SWIGLU_Q81, 128, QMM_GU_CONV, 4, QMM_GU_TSTAGES, QMM_GU_CSTAGES, true, CN, 2,
+                            false, QMM_GU_SWAP != 0>;
 // CTA-pair forms (clusters of 2): 256 token rows x 256 weight rows per pair,
 // each CTA 128 token rows and 128 weight rows (gate/up: 64 gate + 64 up).
 #ifndef QMM_PAIR_TSTAGES

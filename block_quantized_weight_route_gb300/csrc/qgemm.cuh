@@ -111,9 +111,10 @@ struct GemmCfg {
     // 16 warps (20, 24 or 28 for the FP8 fold).  Warp w runs on SM sub-partition w % 4; the MMA issuer (warp 1)
     // must not share its sub-partition with ALU-heavy converter warps, or its
     // mbarrier waits are starved and the tensor pipe idles.
-    // WIDE16: the wide W4 tile (256 weight rows) with 16 converter warps, two
-    // threads per weight row: 28 warps, the epilogue on warps 24..27
-    static constexpr bool WIDE16 = (B_ == BMode::W4 && E_ == Epi::STORE && BN_ == 256 && CONV_WARPS_ == 16);
+    // WIDE16: a W4 tile with 16 converter warps (the wide 256-row tile, two
+    // threads per weight row, or gate/up's 128 rows, four threads per row): 28
+    // warps, the epilogue on warps 24..27
+    static constexpr bool WIDE16 = (B_ == BMode::W4 && EPI_WARPS_ == 4 && CONV_WARPS_ == 16 && !PAIR_);
     static constexpr int EPI_BASE = WIDE16 ? 24 : ((EPI_WARPS_ == 4) ? 12 : 4);
     // 16 fold warps (FP8 with two row sub-tiles) and 2 converters: 20 warps, five
     // per sub-partition, the converters on warps 2 and 3.
@@ -173,7 +174,7 @@ struct GemmCfg {
     static_assert(!FOLD || FOLD_CPW % 8 == 0, "fold columns per warp: whole 16-byte runs");
     static_assert(GROUPED_ || 128 * MSUB_ * ACC_N <= 65536, "split partial tile at most 256 x 256");
     static_assert(FOLD || EPI_WARPS == 4, "store epilogue uses one warpgroup");
-    static_assert(TPR == 1 || TPR == 2, "one or two converter threads per weight row");
+    static_assert(TPR == 1 || TPR == 2 || (TPR == 4 && B_ == BMode::W4), "one, two or (W4) four converter threads per weight row");
     static_assert(CONV_WARPS * 32 * RPT == TPR * BN, "converters cover the weight rows");
     static_assert(RPT == 1 || (RPT == 2 && B_ == BMode::FP8), "two rows per converter thread: FP8 only");
     static_assert(MSUB == 1 || MSUB == 2, "row sub-tiles");
@@ -394,6 +395,27 @@ __device__ __forceinline__ void convert_w4_half(uint32_t raw_tile, uint32_t dst_
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(hh[i]), (w < 2) ? sc0 : sc1);
         sts128(dst_tile + sw128_off(rd, 4 * h + w), o[0], o[1], o[2], o[3]);
+    }
+}
+
+// W4, a quarter row: the 16 codes of K quarter qt (8 bytes) and their scale.
+__device__ __forceinline__ void convert_w4_quarter(uint32_t raw_tile, uint32_t dst_tile, int r, int rd, int qt,
+                                                   uint32_t sbytes) {
+    const int sw = (r >> 2) & 1;
+    uint32_t c0, c1;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                 : "=r"(c0), "=r"(c1)
+                 : "r"(raw_tile + r * 32 + (((qt >> 1) ^ sw) << 4) + (qt & 1) * 8)
+                 : "memory");
+    const uint32_t sc = w4_scale_bf16x2(sbytes >> (8 * qt));
+    const uint32_t words[2] = {c0, c1};
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        uint32_t hh[4], o[4];
+        cvt_e2m1x8_f16x2(words[w], hh);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = bf16x2_mul(f16x2_to_bf16x2_2m112(hh[i]), sc);
+        sts128(dst_tile + sw128_off(rd, 2 * qt + w), o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -1225,7 +1247,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
             // ------------------------------------------------------------ converters
             const int ct = C::conv_slot(warp) * 32 + lane;
             const int crow = ct % C::BN;                      // this thread's weight row in every tile
-            const int chalf = ct / C::BN;                     // and its K half (TPR == 2)
+            const int chalf = ct / C::BN;                     // and its K half (TPR == 2) or quarter (4)
             const int cdrow = C::conv_dst_row(crow);          // its row in the operand tile
             int ts = 0, cs = 0;
             uint32_t tph = 0, cph = 0;
@@ -1310,7 +1332,9 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXNREG)
                 const uint32_t braw = smem_u32(tstage + ts * C::TSTAGE_BYTES) + C::A_RAW_BYTES;
                 const uint32_t bconv = smem_u32(cstage + cs * C::CSTAGE_BYTES);
                 if constexpr (C::B == BMode::W4) {
-                    if constexpr (C::TPR == 2)
+                    if constexpr (C::TPR == 4)
+                        convert_w4_quarter(braw, bconv, crow, cdrow, chalf, sbytes);
+                    else if constexpr (C::TPR == 2)
                         convert_w4_half(braw, bconv, crow, cdrow, chalf, sbytes);
                     else
                         convert_w4_row(braw, bconv, crow, cdrow, sbytes);
